@@ -1,0 +1,202 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) MoE-layer forward library.
+ *
+ * The library computes the forward pass of a Qwen3-MoE-style mixture-of-experts
+ * layer on one GPU, as the page "基于Atlas A3、950训练/推理集群的Qwen3-MoE模型低时延
+ * 推理性能优化实践" decomposes it into fused operators:
+ *   router logits -> gating top-k softmax (§快速选择专家) -> init_routing and
+ *   compute_expert_tokens (§高效排序和token路由) -> grouped matmul over the merged
+ *   gate/up weight w13 with SwiGLU (§计算分解, §高性能专家计算) -> grouped matmul
+ *   over down_proj -> finalize_routing (§高效排序和token路由).
+ * Each expert is the MLP  y = down( SiLU(x . gate) * (x . up) ), w13 = [gate | up].
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Pointers are DEVICE pointers of the current CUDA device unless stated, owned
+ *    by the caller; the library never allocates or frees device memory.  Buffers
+ *    named "ws" are caller-provided scratch of at least the queried size, 256-byte
+ *    aligned; their contents on entry do not matter.
+ *  - All calls are asynchronous on `stream` (0 = legacy default stream) and return
+ *    after validating arguments and enqueueing work.  The return value reports
+ *    host-side validation and launch errors only.
+ *  - Problems found by kernels (an expert id outside [0,E), a wait that ran out of
+ *    time) are OR-ed into a per-device status word, read with
+ *    moe_get_device_status (synchronises the stream) and cleared with
+ *    moe_clear_device_status.  Kernels never trap.
+ *  - bf16 tensors are passed as raw 16-bit patterns (moe_bf16), row-major.
+ *    Matrix pointers must be 16-byte aligned.
+ *  - Shapes: 1 <= T; H % 128 == 0; I % 64 == 0; 1 <= E <= 256; 1 <= k <= min(E, 32);
+ *    T*k < 2^31.  Other shapes return MOE_ERR_UNSUPPORTED_SHAPE.
+ *  - The library runs only on compute capability 10.3 (GB300, sm_103a); other
+ *    devices return MOE_ERR_UNSUPPORTED_ARCH.
+ *  - Token-expert pairs are numbered token-major: pair j = t*k + s is slot s of
+ *    token t.  P = T*k.
+ */
+#ifndef MOE_GB300_H_
+#define MOE_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+typedef uint16_t moe_bf16;                /* bfloat16 bit pattern */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,       /* null / misaligned pointer, negative size */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set above */
+  MOE_ERR_UNSUPPORTED_ARCH = 3,  /* current device is not sm_103 */
+  MOE_ERR_WORKSPACE = 4,         /* ws too small or misaligned */
+  MOE_ERR_CUDA = 5               /* a CUDA runtime call or launch failed */
+} moe_status;
+
+/* Bits of the device status word. */
+#define MOE_DEV_BAD_EXPERT_ID 0x1 /* a topk id outside [0,E): that pair was skipped */
+#define MOE_DEV_WAIT_TIMEOUT 0x2  /* a bounded device wait expired; outputs invalid */
+
+/* Version of this ABI (bumped on any signature change). */
+MOE_API int moe_abi_version(void);
+
+/* Human-readable text for a moe_status value (static storage). */
+MOE_API const char* moe_status_string(int status);
+
+/* Reads (after synchronising `stream`) the current device's status word. */
+MOE_API moe_status moe_get_device_status(int32_t* status_out /* host */, moe_stream_t stream);
+/* Clears the current device's status word (asynchronously on `stream`). */
+MOE_API moe_status moe_clear_device_status(moe_stream_t stream);
+
+/* ---------------------------------------------------------------- router --
+ * Router scores logits[t,e] = sum_h x[t,h] * Wg[h,e], fp32 FMA accumulation.
+ * The page's §融合RMSNorm Cast keeps the gate (router) computation in FP32.
+ *   x       (T,H)  bf16
+ *   Wg      (H,E)  fp32
+ *   logits  (T,E)  fp32, written
+ *   ws      >= moe_router_logits_workspace_size(T,H,E) bytes (may be 0 -> NULL ok)
+ * Deterministic: the split-K partial sums are added in a fixed order.
+ */
+MOE_API size_t moe_router_logits_workspace_size(int T, int H, int E);
+MOE_API moe_status moe_router_logits(const moe_bf16* x, const float* Wg, int T, int H, int E,
+                             float* logits, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ----------------------------------------------------------------- gating --
+ * §快速选择专家: one fused op for "softmax over experts, top-k".  Per token:
+ * experts are ranked by (fp32 logit descending, expert id ascending); the first k
+ * are kept, slot s holding the s-th ranked.  With renormalize != 0 the weights are
+ * softmax over the k kept logits (= full softmax, top-k, renormalised to sum 1);
+ * with renormalize == 0 they are the full-softmax probabilities of the kept ones.
+ *   logits   (T,E) fp32 (finite values)
+ *   topk_ids (T,k) int32, written
+ *   topk_w   (T,k) fp32, written
+ */
+MOE_API moe_status moe_gating_topk_softmax(const float* logits, int T, int E, int k, int renormalize,
+                                   int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- routing --
+ * §高效排序和token路由 (init_routing): stable counting sort of the P pairs by
+ * expert id.  Pair j goes to row p(j) = expert_offsets[id_j] + #{j' < j with the
+ * same id}.
+ *   x                (T,H) bf16; may be NULL when expanded_x is NULL
+ *   topk_ids         (T,k) int32 ids in [0,E); an id outside sets
+ *                    MOE_DEV_BAD_EXPERT_ID and that pair is dropped
+ *                    (expanded_row_idx = -1, not counted)
+ *   expanded_x       (P,H) bf16 or NULL: row p = x[sorted_row_idx[p] / k]
+ *   expanded_row_idx (P)   int32 pair -> row  (j -> p(j))
+ *   sorted_row_idx   (P)   int32 row  -> pair (inverse permutation)
+ *   expert_offsets   (E+1) int32 exclusive prefix sum of the counts
+ *   counts           (E)   int32 or NULL: pairs per expert
+ *   ws               >= moe_init_routing_workspace_size(T,E,k) bytes
+ */
+MOE_API size_t moe_init_routing_workspace_size(int T, int E, int k);
+MOE_API moe_status moe_init_routing(const moe_bf16* x, const int32_t* topk_ids, int T, int H, int E, int k,
+                            moe_bf16* expanded_x, int32_t* expanded_row_idx,
+                            int32_t* sorted_row_idx, int32_t* expert_offsets, int32_t* counts,
+                            void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* §高效排序和token路由 (compute_expert_tokens): tokens each expert must compute.
+ *   topk_ids (P) int32;  counts (E) int32 written;  expert_offsets (E+1) or NULL. */
+MOE_API moe_status moe_compute_expert_tokens(const int32_t* topk_ids, int P, int E, int32_t* counts,
+                                     int32_t* expert_offsets, moe_stream_t stream);
+
+/* ----------------------------------------------------- weight packing ----
+ * Load-time, untimed.  Rewrites the logical weights into the K-major tiles the
+ * grouped GEMMs stream with TMA.
+ *   w13  (E,H,2I) bf16: columns [0,I) gate_proj, [I,2I) up_proj (§计算分解: the
+ *        SwiGLU op chunks the merged product in two and gates the first half)
+ *   down (E,I,H)  bf16
+ *   w13_packed  >= moe_packed_weight_bytes(E,H,I,0) bytes: per expert 2I rows of H
+ *        (row block b of 128 rows = gate columns 64b..64b+63, then the matching up
+ *        columns)
+ *   down_packed >= moe_packed_weight_bytes(E,H,I,1) bytes: per expert H rows of I
+ * Either input may be NULL to skip it.
+ */
+MOE_API size_t moe_packed_weight_bytes(int E, int H, int I, int which /* 0: w13, 1: down */);
+MOE_API moe_status moe_pack_weights(const moe_bf16* w13, const moe_bf16* down, int E, int H, int I,
+                            void* w13_packed, void* down_packed, moe_stream_t stream);
+
+/* --------------------------------------------------------- grouped GEMMs --
+ * §高性能专家计算 (grouped_matmul) fused with §计算分解's SwiGLU: for each expert e,
+ * the rows r in [expert_offsets[e], expert_offsets[e+1]) of A:
+ *   h[r, c] = SiLU(g) * u,  g = sum_k A[r,k] w13[e][k][c],  u = sum_k A[r,k] w13[e][k][I+c]
+ * fp32 accumulation in tensor memory, h rounded once to bf16.
+ *   A  (P,K) bf16 expert-sorted rows (K = H);  w13_packed from moe_pack_weights;
+ *   expert_offsets (E+1) int32 (device), offsets[E] <= P;  h (P,N) bf16 (N = I).
+ *   ws >= moe_grouped_matmul_workspace_size() bytes (NULL when 0).
+ * Rows of A or h past expert_offsets[E] are not read / written.
+ */
+MOE_API size_t moe_grouped_matmul_workspace_size(void);
+MOE_API moe_status moe_grouped_matmul_swiglu(const moe_bf16* A, const void* w13_packed,
+                                     const int32_t* expert_offsets, int E, int P, int K, int N,
+                                     moe_bf16* h, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Plain grouped GEMM (the down projection): y[r, n] = sum_k A[r,k] down[e][k][n]
+ * for r in expert e's rows; fp32 accumulation, y rounded once to bf16.
+ *   A (P,K) bf16 (K = I); w_packed = down_packed; y (P,N) bf16 (N = H). */
+MOE_API moe_status moe_grouped_matmul(const moe_bf16* A, const void* w_packed,
+                              const int32_t* expert_offsets, int E, int P, int K, int N,
+                              moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* -------------------------------------------------------------- finalize --
+ * §高效排序和token路由 (finalize_routing): put expert outputs back in token order
+ * and add them with the router weights:
+ *   out[t,:] = sum_{s<k} topk_w[t,s] * y2[expanded_row_idx[t*k+s], :]
+ * summed in fp32 in slot order (deterministic), rounded once to bf16.  Pairs with
+ * expanded_row_idx < 0 are skipped.
+ *   y2 (P,H) bf16; topk_w (T,k) fp32; expanded_row_idx (P) int32; out (T,H) bf16.
+ */
+MOE_API moe_status moe_finalize_routing(const moe_bf16* y2, const float* topk_w,
+                                const int32_t* expanded_row_idx, int T, int k, int H,
+                                moe_bf16* out, moe_stream_t stream);
+
+/* --------------------------------------------------------- whole layer ----
+ * The full layer in one call: router -> gating (renormalised) -> init_routing ->
+ * grouped GEMM + SwiGLU -> grouped GEMM -> finalize.  Both GEMMs run in one
+ * persistent launch; a down-projection tile starts once every gate/up tile of its
+ * expert has been written.
+ *   x (T,H) bf16; Wg (H,E) fp32
+ *   logits_override (T,E) fp32 or NULL: when given, replaces the router output
+ *   w13_packed, down_packed from moe_pack_weights
+ *   out (T,H) bf16
+ *   topk_ids_out (T,k) int32 or NULL; topk_w_out (T,k) fp32 or NULL
+ *   ws >= moe_forward_workspace_size(T,H,E,k,I) bytes
+ */
+MOE_API size_t moe_forward_workspace_size(int T, int H, int E, int k, int I);
+MOE_API moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_override,
+                       const void* w13_packed, const void* down_packed, int T, int H, int E, int k,
+                       int I, moe_bf16* out, int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H_ */

@@ -1,0 +1,84 @@
+"""Test helpers: tensor conversion, tolerance checks, lazy per-expert weight access."""
+import numpy as np
+import pytest
+import torch
+
+# Output tolerance of the bf16 layer against the fp64 oracle: relative Frobenius
+# error <= 1e-2 and max-abs error <= 3e-2 * max|ref|.  The GPU rounds h, y2 and the
+# output to bf16 once each (relative 2^-9 per rounding) and accumulates in fp32, so
+# the expected error is a few 1e-3; the bound leaves margin without hiding a wrong
+# term (a dropped expert or a swapped gate/up moves the error to O(1)).
+REL_FRO = 1e-2
+MAX_ABS_FRAC = 3e-2
+# MXFP8 layer against the oracle on dequantised inputs.
+REL_FRO_MX = 4e-2
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        t = t.float()
+    return t.cpu().numpy()
+
+
+def rel_fro(got, ref) -> float:
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def assert_close_layer(got, ref, rel=REL_FRO, max_abs_frac=MAX_ABS_FRAC, what="output"):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    rf = rel_fro(got, ref)
+    ma = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    lim = max_abs_frac * float(np.max(np.abs(ref))) if ref.size else 0.0
+    assert rf <= rel, f"{what}: relative Frobenius error {rf:.3e} > {rel:.1e}"
+    assert ma <= lim, f"{what}: max abs error {ma:.3e} > {lim:.3e}"
+    return rf, ma
+
+
+class LazyExperts:
+    """Indexable view of a (E, a, b) torch weight tensor: w[e] -> fp32 numpy array,
+    converted one expert at a time (the oracle widens it to fp64)."""
+
+    def __init__(self, w: torch.Tensor):
+        self.w = w
+        self._cache = {}
+
+    def __len__(self):
+        return self.w.shape[0]
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self._cache:
+            if len(self._cache) > 16:
+                self._cache.clear()
+            self._cache[e] = self.w[e].float().cpu().numpy()
+        return self._cache[e]
+
+
+@pytest.fixture(scope="session")
+def cuda_dev():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from top_routing_grouped_gating_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    return dev
+
+
+def routing_margin_ok(logits32: np.ndarray, k: int, tol: np.ndarray) -> np.ndarray:
+    """Tokens whose top-k set cannot change under logit perturbations of size tol[t]
+    (gap between the k-th and (k+1)-th largest logit exceeds 2*tol, and the slot
+    order is not within 2*tol either)."""
+    srt = -np.sort(-logits32.astype(np.float64), axis=1)
+    gaps = srt[:, :-1] - srt[:, 1:]
+    if logits32.shape[1] > k:
+        need = gaps[:, :k]
+    else:
+        need = gaps[:, :k - 1]
+    return np.all(need > 2 * tol[:, None], axis=1)

@@ -24,3 +24,6 @@ def load_golden(name):
 @pytest.fixture
 def golden():
     return load_golden
+
+
+from tests._helpers import cuda_dev  # noqa: E402,F401  (session fixture for GPU tests)

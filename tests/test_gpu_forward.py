@@ -1,0 +1,110 @@
+"""End-to-end parity of moe_forward (one C-ABI call for the whole layer) against the
+CPU oracle on the seeded workloads, at their full sizes.
+
+Routing is checked bit-exactly by feeding both sides the oracle's fp32 logits
+(logits_override), so the comparison of outputs cannot be masked by near-tie
+routing flips of the fp32 router.  Where the oracle would take minutes at full
+size, every token is still computed on the GPU and a seeded sample of tokens is
+checked (tokens are independent in this layer).  A separate test runs the GPU
+router and compares the tokens whose routing margin is larger than the router's
+error bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import top_routing_grouped_gating_gb300 as moe
+from oracle import moe_oracle as O
+from tests._helpers import LazyExperts, assert_close_layer, routing_margin_ok, to_np
+from top_routing_grouped_gating_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+FULL_ORACLE_MAX_T = 64
+
+
+@pytest.fixture(scope="module")
+def layers(cuda_dev):
+    cache = {}
+
+    def get(name, **kw):
+        key = (name, tuple(sorted(kw.items())))
+        if key not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            cfg = W.with_shape(W.CONFIGS[name], **kw) if kw else W.CONFIGS[name]
+            inp = W.make_inputs(cfg, device="cuda")
+            layer = moe.MoELayer(inp["Wg"], inp["w13"], inp["down"], cfg.k)
+            cache[key] = (cfg, inp, layer)
+        return cache[key]
+    return get
+
+
+def _check_forward(cfg, inp, layer, sample=None):
+    x, Wg = inp["x"], inp["Wg"]
+    xn = to_np(x)
+    lg32 = O.router_logits_f32(xn, to_np(Wg))
+    out, ids, w = layer(x, logits_override=torch.from_numpy(lg32).to(x.device))
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 0
+    r_ids, r_w = O.gating_topk_softmax(lg32, cfg.k)
+    np.testing.assert_array_equal(to_np(ids), r_ids)
+    np.testing.assert_allclose(to_np(w), r_w, rtol=2e-6, atol=1e-7)
+    rows = np.arange(cfg.T) if sample is None else sample
+    ref = O.moe_forward(xn[rows], None, LazyExperts(inp["w13"]), LazyExperts(inp["down"]), cfg.k,
+                        logits32=lg32[rows], keep_intermediates=False)
+    return assert_close_layer(to_np(out)[rows], ref["out"], what=cfg.name)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_30b_a3b_decode", "qwen3_235b_a22b_decode"])
+def test_forward_full_oracle(layers, name):
+    cfg, inp, layer = layers(name)
+    _check_forward(cfg, inp, layer)
+
+
+@pytest.mark.parametrize("name,nsample", [("qwen3_30b_a3b_prefill_zipf", 96),
+                                          ("qwen3_235b_a22b_prefill", 48)])
+def test_forward_prefill_sampled(layers, name, nsample):
+    cfg, inp, layer = layers(name)
+    rng = np.random.default_rng(0)
+    sample = np.sort(rng.choice(cfg.T, nsample, replace=False))
+    sample[0], sample[-1] = 0, cfg.T - 1
+    _check_forward(cfg, inp, layer, sample=np.unique(sample))
+
+
+@pytest.mark.parametrize("T", [1, 3, 17, 100])
+def test_forward_ragged_token_counts(layers, T):
+    cfg, inp, layer = layers("qwen3_30b_a3b_decode", T=T)
+    _check_forward(cfg, inp, layer)
+
+
+def test_forward_single_expert_is_dense_mlp(layers):
+    cfg, inp, layer = layers("tiny", E=1, k=1, T=40)
+    _check_forward(cfg, inp, layer)
+
+
+def test_forward_with_gpu_router(layers):
+    cfg, inp, layer = layers("qwen3_30b_a3b_decode", T=64)
+    x, Wg = inp["x"], inp["Wg"]
+    out, ids, w = layer(x)
+    torch.cuda.synchronize()
+    xn = to_np(x).astype(np.float64)
+    Wn = to_np(Wg).astype(np.float64)
+    lg = O.router_logits_f32(xn, Wn)
+    tol = 1e-5 * (np.abs(xn) @ np.abs(Wn)).max(axis=1)
+    safe = routing_margin_ok(lg, cfg.k, tol)
+    assert safe.sum() >= cfg.T * 0.9
+    r_ids, _ = O.gating_topk_softmax(lg, cfg.k)
+    np.testing.assert_array_equal(to_np(ids)[safe], r_ids[safe])
+    rows = np.nonzero(safe)[0]
+    ref = O.moe_forward(to_np(x)[rows], None, LazyExperts(inp["w13"]), LazyExperts(inp["down"]), cfg.k,
+                        logits32=lg[rows], keep_intermediates=False)
+    assert_close_layer(to_np(out)[rows], ref["out"])
+
+
+def test_forward_is_deterministic(layers):
+    cfg, inp, layer = layers("qwen3_30b_a3b_prefill_zipf")
+    a = layer(inp["x"])[0].clone()
+    b = layer(inp["x"])[0]
+    assert torch.equal(a, b)
+    assert moe.get_device_status() == 0

@@ -1,0 +1,313 @@
+"""ctypes binding of ``libmoe_gb300.so`` (argument marshalling only).
+
+Every function here checks dtypes / devices / contiguity of torch tensors, passes
+their device pointers and the current CUDA stream to the C ABI declared in
+``include/moe_gb300.h``, and raises :class:`MoEError` on a non-zero status.  All
+arithmetic runs in the library's CUDA kernels; there is no fallback path, and a
+missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+_c_int, _c_size, _vp, _c_float = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+
+# name -> (restype, argtypes)
+_SIGS = {
+    "moe_abi_version": (_c_int, []),
+    "moe_status_string": (ctypes.c_char_p, [_c_int]),
+    "moe_get_device_status": (_c_int, [ctypes.POINTER(ctypes.c_int32), _vp]),
+    "moe_clear_device_status": (_c_int, [_vp]),
+    "moe_router_logits_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
+    "moe_router_logits": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_size, _vp]),
+    "moe_gating_topk_softmax": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_init_routing_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
+    "moe_init_routing": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _c_size, _vp]),
+    "moe_compute_expert_tokens": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_packed_weight_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "moe_pack_weights": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_grouped_matmul_workspace_size": (_c_size, []),
+    "moe_grouped_matmul_swiglu": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
+                                           _c_size, _vp]),
+    "moe_grouped_matmul": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_size,
+                                    _vp]),
+    "moe_finalize_routing": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp]),
+    "moe_forward_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "moe_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
+                             _vp, _vp, _c_size, _vp]),
+}
+
+DEV_BAD_EXPERT_ID = 0x1
+DEV_WAIT_TIMEOUT = 0x2
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = lib().moe_status_string(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load the in-tree library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing: build it with "
+                "`python -m top_routing_grouped_gating_gb300.build` (no CPU fallback exists)")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def exported_symbols():
+    return sorted(_SIGS)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise MoEError(fn, status)
+
+
+def _stream(dev: torch.device) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, dev: Optional[torch.device] = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dev is not None and t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, expected {dev}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _ws(nbytes: int, dev: torch.device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+
+
+# --------------------------------------------------------------------------- ops
+
+
+def router_logits(x: torch.Tensor, Wg: torch.Tensor) -> torch.Tensor:
+    _need(x, "x", torch.bfloat16)
+    _need(Wg, "Wg", torch.float32, x.device)
+    T, H = x.shape
+    E = Wg.shape[1]
+    L = lib()
+    with torch.cuda.device(x.device):
+        out = torch.empty(T, E, dtype=torch.float32, device=x.device)
+        nb = L.moe_router_logits_workspace_size(T, H, E)
+        ws = _ws(nb, x.device) if nb else None
+        _check("moe_router_logits", L.moe_router_logits(_ptr(x), _ptr(Wg), T, H, E, _ptr(out), _ptr(ws),
+                                                        nb, _stream(x.device)))
+    return out
+
+
+def gating_topk_softmax(logits: torch.Tensor, k: int, renormalize: bool = True):
+    _need(logits, "logits", torch.float32)
+    T, E = logits.shape
+    with torch.cuda.device(logits.device):
+        ids = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+        w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+        _check("moe_gating_topk_softmax",
+               lib().moe_gating_topk_softmax(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(ids),
+                                             _ptr(w), _stream(logits.device)))
+    return ids, w
+
+
+def init_routing(topk_ids: torch.Tensor, E: int, x: Optional[torch.Tensor] = None):
+    """Returns dict(expanded_row_idx, sorted_row_idx, expert_offsets, counts[, expanded_x])."""
+    _need(topk_ids, "topk_ids", torch.int32)
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    H = 0
+    if x is not None:
+        _need(x, "x", torch.bfloat16, dev)
+        H = x.shape[1]
+    P = T * k
+    L = lib()
+    with torch.cuda.device(dev):
+        eri = torch.empty(P, dtype=torch.int32, device=dev)
+        sri = torch.empty(P, dtype=torch.int32, device=dev)
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        cnt = torch.empty(E, dtype=torch.int32, device=dev)
+        xe = torch.empty(P, H, dtype=torch.bfloat16, device=dev) if x is not None else None
+        nb = L.moe_init_routing_workspace_size(T, E, k)
+        ws = _ws(nb, dev)
+        _check("moe_init_routing",
+               L.moe_init_routing(_ptr(x), _ptr(topk_ids), T, H, E, k, _ptr(xe), _ptr(eri), _ptr(sri),
+                                  _ptr(off), _ptr(cnt), _ptr(ws), ws.numel(), _stream(dev)))
+    res = dict(expanded_row_idx=eri, sorted_row_idx=sri, expert_offsets=off, counts=cnt)
+    if xe is not None:
+        res["expanded_x"] = xe
+    return res
+
+
+def compute_expert_tokens(topk_ids: torch.Tensor, E: int):
+    _need(topk_ids, "topk_ids", torch.int32)
+    dev = topk_ids.device
+    P = topk_ids.numel()
+    with torch.cuda.device(dev):
+        cnt = torch.empty(E, dtype=torch.int32, device=dev)
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        _check("moe_compute_expert_tokens",
+               lib().moe_compute_expert_tokens(_ptr(topk_ids), P, E, _ptr(cnt), _ptr(off), _stream(dev)))
+    return cnt, off
+
+
+def pack_weights(w13: torch.Tensor, down: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Logical w13 (E,H,2I) = [gate | up] and down (E,I,H), bf16 -> packed buffers."""
+    _need(w13, "w13", torch.bfloat16)
+    _need(down, "down", torch.bfloat16, w13.device)
+    E, H, I2 = w13.shape
+    I = I2 // 2
+    if down.shape != (E, I, H):
+        raise ValueError(f"down must be (E,I,H)=({E},{I},{H}), got {tuple(down.shape)}")
+    L = lib()
+    dev = w13.device
+    with torch.cuda.device(dev):
+        w13p = torch.empty(L.moe_packed_weight_bytes(E, H, I, 0) // 2, dtype=torch.bfloat16, device=dev)
+        downp = torch.empty(L.moe_packed_weight_bytes(E, H, I, 1) // 2, dtype=torch.bfloat16, device=dev)
+        _check("moe_pack_weights", L.moe_pack_weights(_ptr(w13), _ptr(down), E, H, I, _ptr(w13p),
+                                                      _ptr(downp), _stream(dev)))
+    return w13p, downp
+
+
+def grouped_matmul_swiglu(A: torch.Tensor, w13_packed: torch.Tensor, expert_offsets: torch.Tensor,
+                          E: int, I: int) -> torch.Tensor:
+    _need(A, "A", torch.bfloat16)
+    _need(expert_offsets, "expert_offsets", torch.int32, A.device)
+    _need(w13_packed, "w13_packed", torch.bfloat16, A.device)
+    P, K = A.shape
+    with torch.cuda.device(A.device):
+        h = torch.empty(P, I, dtype=torch.bfloat16, device=A.device)
+        _check("moe_grouped_matmul_swiglu",
+               lib().moe_grouped_matmul_swiglu(_ptr(A), _ptr(w13_packed), _ptr(expert_offsets), E, P, K, I,
+                                               _ptr(h), None, 0, _stream(A.device)))
+    return h
+
+
+def grouped_matmul(A: torch.Tensor, w_packed: torch.Tensor, expert_offsets: torch.Tensor, E: int,
+                   N: int) -> torch.Tensor:
+    _need(A, "A", torch.bfloat16)
+    _need(expert_offsets, "expert_offsets", torch.int32, A.device)
+    _need(w_packed, "w_packed", torch.bfloat16, A.device)
+    P, K = A.shape
+    with torch.cuda.device(A.device):
+        y = torch.empty(P, N, dtype=torch.bfloat16, device=A.device)
+        _check("moe_grouped_matmul",
+               lib().moe_grouped_matmul(_ptr(A), _ptr(w_packed), _ptr(expert_offsets), E, P, K, N, _ptr(y),
+                                        None, 0, _stream(A.device)))
+    return y
+
+
+def finalize_routing(y2: torch.Tensor, topk_w: torch.Tensor, expanded_row_idx: torch.Tensor) -> torch.Tensor:
+    _need(y2, "y2", torch.bfloat16)
+    _need(topk_w, "topk_w", torch.float32, y2.device)
+    _need(expanded_row_idx, "expanded_row_idx", torch.int32, y2.device)
+    T, k = topk_w.shape
+    H = y2.shape[1]
+    with torch.cuda.device(y2.device):
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=y2.device)
+        _check("moe_finalize_routing",
+               lib().moe_finalize_routing(_ptr(y2), _ptr(topk_w), _ptr(expanded_row_idx), T, k, H, _ptr(out),
+                                          _stream(y2.device)))
+    return out
+
+
+def forward_workspace_bytes(T: int, H: int, E: int, k: int, I: int) -> int:
+    return int(lib().moe_forward_workspace_size(T, H, E, k, I))
+
+
+def forward(x: torch.Tensor, Wg: Optional[torch.Tensor], w13_packed: torch.Tensor, down_packed: torch.Tensor,
+            E: int, k: int, I: int, logits_override: Optional[torch.Tensor] = None,
+            ws: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+            topk_ids: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None):
+    """One call of the whole layer.  Returns (out, topk_ids, topk_w)."""
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    T, H = x.shape
+    if Wg is not None:
+        _need(Wg, "Wg", torch.float32, dev)
+    if logits_override is not None:
+        _need(logits_override, "logits_override", torch.float32, dev)
+    L = lib()
+    with torch.cuda.device(dev):
+        nb = L.moe_forward_workspace_size(T, H, E, k, I)
+        if ws is None:
+            ws = _ws(nb, dev)
+        if out is None:
+            out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        if topk_ids is None:
+            topk_ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+        if topk_w is None:
+            topk_w = torch.empty(T, k, dtype=torch.float32, device=dev)
+        _check("moe_forward",
+               L.moe_forward(_ptr(x), _ptr(Wg), _ptr(logits_override), _ptr(w13_packed), _ptr(down_packed),
+                             T, H, E, k, I, _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel(),
+                             _stream(dev)))
+    return out, topk_ids, topk_w
+
+
+def get_device_status(device=None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    v = ctypes.c_int32(0)
+    with torch.cuda.device(dev):
+        _check("moe_get_device_status", lib().moe_get_device_status(ctypes.byref(v), _stream(dev)))
+    return int(v.value)
+
+
+def clear_device_status(device=None) -> None:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check("moe_clear_device_status", lib().moe_clear_device_status(_stream(dev)))
+
+
+class MoELayer:
+    """A Qwen3-MoE-style MoE layer with packed, resident weights and a reusable workspace."""
+
+    def __init__(self, Wg: torch.Tensor, w13: torch.Tensor, down: torch.Tensor, k: int):
+        self.E, self.H, I2 = w13.shape
+        self.I = I2 // 2
+        self.k = k
+        self.Wg = Wg.contiguous()
+        self.w13_packed, self.down_packed = pack_weights(w13.contiguous(), down.contiguous())
+        self._ws = None
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = forward_workspace_bytes(T, self.H, self.E, self.k, self.I)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = _ws(need, self.Wg.device)
+        return self._ws
+
+    def __call__(self, x: torch.Tensor, logits_override: Optional[torch.Tensor] = None, **kw):
+        return forward(x, self.Wg, self.w13_packed, self.down_packed, self.E, self.k, self.I,
+                       logits_override=logits_override, ws=self.workspace(x.shape[0]), **kw)

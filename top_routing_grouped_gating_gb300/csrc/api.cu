@@ -1,0 +1,410 @@
+// C-ABI entry points of the MoE-layer library: argument validation, per-device
+// facts (architecture, SM count, status word address), TMA descriptor encoding,
+// workspace layouts, and the sequence of launches for each operator.  The
+// operators follow the page "基于Atlas A3、950训练/推理集群的Qwen3-MoE模型低时延
+// 推理性能优化实践": gating top-k softmax (§快速选择专家), init_routing /
+// compute_expert_tokens / finalize_routing (§高效排序和token路由), grouped matmul
+// (§高性能专家计算) with SwiGLU (§计算分解).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/moe_gb300.h"
+#include "internal.h"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+// The device status word; each device holds its own copy.  Host code must not
+// use its name as an address: the device address comes from
+// cudaGetSymbolAddress, taken once per device.
+__device__ int g_device_status;
+
+struct DeviceFacts {
+  bool probed = false;
+  bool arch_ok = false;
+  int sm_count = 0;
+  int* status = nullptr;
+};
+std::mutex g_mu;
+DeviceFacts g_dev[64];
+
+moe_status current_device(DeviceFacts** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceFacts& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    d.arch_ok = (major == 10 && minor == 3);
+    d.sm_count = sms;
+    if (d.arch_ok) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return MOE_ERR_CUDA;
+      d.status = static_cast<int*>(p);
+    }
+    d.probed = true;
+  }
+  if (!d.arch_ok) return MOE_ERR_UNSUPPORTED_ARCH;
+  *out = &d;
+  return MOE_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+moe_status check_layer_shape(int T, int H, int E, int k, int I) {
+  if (T < 1 || H < 1 || E < 1 || k < 1 || I < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 128 != 0 || I % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (E > 256 || k > E || k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                      \
+  do {                                     \
+    const moe_status st_ = (expr);         \
+    if (st_ != MOE_OK) return st_;         \
+  } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+// Workspace of moe_forward, in call order.
+struct ForwardLayout {
+  size_t router, ids, w, routing, counts, offsets, eri, sri, done, xe, h, y2, total;
+};
+
+ForwardLayout forward_layout(int T, int H, int E, int k, int I) {
+  ForwardLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  const size_t P = (size_t)T * k;
+  const moe::RouterPlan rp = moe::router_plan(T, H, E);
+  L.router = take((size_t)rp.splits * T * E * sizeof(float));
+  L.ids = take(P * sizeof(int32_t));
+  L.w = take(P * sizeof(float));
+  L.routing = take(moe::routing_ws_bytes((int)P, E));
+  L.counts = take((size_t)E * sizeof(int32_t));
+  L.offsets = take((size_t)(E + 1) * sizeof(int32_t));
+  L.eri = take(P * sizeof(int32_t));
+  L.sri = take(P * sizeof(int32_t));
+  L.done = take((size_t)E * sizeof(int32_t));
+  L.xe = take(P * H * 2);
+  L.h = take(P * I * 2);
+  L.y2 = take(P * H * 2);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+}  // namespace
+
+namespace moe {
+
+int device_sm_count() {
+  DeviceFacts* d = nullptr;
+  if (current_device(&d) != MOE_OK) return 1;
+  return d->sm_count;
+}
+
+bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
+                         uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+int moe_abi_version(void) { return kAbiVersion; }
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_UNSUPPORTED_ARCH: return "unsupported device: compute capability 10.3 required";
+    case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+moe_status moe_get_device_status(int32_t* status_out, moe_stream_t stream) {
+  if (status_out == nullptr) return MOE_ERR_INVALID_ARG;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  int v = 0;
+  MOE_CUDA(cudaMemcpyAsync(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost, stream));
+  MOE_CUDA(cudaStreamSynchronize(stream));
+  *status_out = v;
+  return MOE_OK;
+}
+
+moe_status moe_clear_device_status(moe_stream_t stream) {
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(cudaMemsetAsync(d->status, 0, sizeof(int), stream));
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------ router --
+size_t moe_router_logits_workspace_size(int T, int H, int E) {
+  if (T < 1 || H < 1 || E < 1) return 0;
+  const moe::RouterPlan rp = moe::router_plan(T, H, E);
+  return rp.splits > 1 ? align256((size_t)rp.splits * T * E * sizeof(float)) : 0;
+}
+
+moe_status moe_router_logits(const moe_bf16* x, const float* Wg, int T, int H, int E,
+                             float* logits, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!x || !Wg || !logits || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || E > 256 || H < 32 || H % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  const moe::RouterPlan rp = moe::router_plan(T, H, E);
+  if (rp.splits > 1) {
+    if (ws == nullptr || ws_bytes < moe_router_logits_workspace_size(T, H, E) ||
+        (reinterpret_cast<uintptr_t>(ws) & 255u))
+      return MOE_ERR_WORKSPACE;
+    float* partial = static_cast<float*>(ws);
+    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, partial, stream));
+    MOE_CUDA(moe::launch_router_reduce(partial, rp.splits, T, E, logits, stream));
+  } else {
+    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, logits, stream));
+  }
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------ gating --
+moe_status moe_gating_topk_softmax(const float* logits, int T, int E, int k, int renormalize,
+                                   int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || E > 256 || k < 1 || k > E || k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_gating(logits, 1, T, E, k, renormalize, topk_ids, topk_w, d->status,
+                              stream));
+  return MOE_OK;
+}
+
+// ----------------------------------------------------------------- routing --
+size_t moe_init_routing_workspace_size(int T, int E, int k) {
+  if (T < 1 || E < 1 || k < 1) return 0;
+  const int P = T * k;
+  return align256(moe::routing_ws_bytes(P, E)) + align256((size_t)E * sizeof(int32_t));
+}
+
+moe_status moe_init_routing(const moe_bf16* x, const int32_t* topk_ids, int T, int H, int E, int k,
+                            moe_bf16* expanded_x, int32_t* expanded_row_idx,
+                            int32_t* sorted_row_idx, int32_t* expert_offsets, int32_t* counts,
+                            void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!topk_ids || !expanded_row_idx || !sorted_row_idx || !expert_offsets)
+    return MOE_ERR_INVALID_ARG;
+  if (expanded_x && (!x || !aligned16(x) || !aligned16(expanded_x))) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || E > 256 || k < 1 || k > 32 || (long long)T * k >= (1LL << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (expanded_x && (H < 8 || H % 8 != 0)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws == nullptr || ws_bytes < moe_init_routing_workspace_size(T, E, k) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_WORKSPACE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  const int P = T * k;
+  int32_t* cnt = counts ? counts : at<int32_t>(ws, align256(moe::routing_ws_bytes(P, E)));
+  MOE_CUDA(moe::launch_routing(topk_ids, P, E, cnt, expert_offsets, expanded_row_idx,
+                               sorted_row_idx, ws, nullptr, d->status, stream));
+  if (expanded_x)
+    MOE_CUDA(moe::launch_gather_rows(x, sorted_row_idx, expert_offsets, E, P, H, k, expanded_x,
+                                     stream));
+  return MOE_OK;
+}
+
+moe_status moe_compute_expert_tokens(const int32_t* topk_ids, int P, int E, int32_t* counts,
+                                     int32_t* expert_offsets, moe_stream_t stream) {
+  if (!topk_ids || !counts) return MOE_ERR_INVALID_ARG;
+  if (P < 1 || E < 1 || E > 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_expert_tokens(topk_ids, P, E, counts, expert_offsets, d->status, stream));
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------- weight packing --
+size_t moe_packed_weight_bytes(int E, int H, int I, int which) {
+  if (E < 1 || H < 1 || I < 1) return 0;
+  return (size_t)E * H * I * 2 * (which == 0 ? 2 : 1);
+}
+
+moe_status moe_pack_weights(const moe_bf16* w13, const moe_bf16* down, int E, int H, int I,
+                            void* w13_packed, void* down_packed, moe_stream_t stream) {
+  if ((w13 && !w13_packed) || (down && !down_packed)) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > 256 || H % 128 != 0 || I % 64 != 0 || H < 128 || I < 64)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  if (w13) MOE_CUDA(moe::launch_pack_w13(w13, E, H, I, static_cast<uint16_t*>(w13_packed), stream));
+  if (down)
+    MOE_CUDA(moe::launch_pack_down(down, E, H, I, static_cast<uint16_t*>(down_packed), stream));
+  return MOE_OK;
+}
+
+// ----------------------------------------------------------- grouped GEMMs --
+size_t moe_grouped_matmul_workspace_size(void) { return 0; }
+
+static moe_status grouped_common(const moe_bf16* A, const void* w, const int32_t* offsets, int E,
+                                 int P, int K, int N, moe_bf16* out, bool swiglu,
+                                 moe_stream_t stream) {
+  if (!A || !w || !offsets || !out || !aligned16(A) || !aligned16(w) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > 256 || P < 1 || K < 64 || K % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (swiglu ? (N < 64 || N % 64 != 0) : (N < 128 || N % 128 != 0))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  moe::GemmPhase ph{};
+  ph.A_weights = w;
+  ph.B_act = A;
+  ph.out = out;
+  ph.K = K;
+  ph.MW = swiglu ? 2 * N : N;
+  ph.n_out = N;
+  ph.swiglu = swiglu ? 1 : 0;
+  MOE_CUDA(moe::launch_grouped_gemm(swiglu ? &ph : nullptr, swiglu ? nullptr : &ph, offsets, E, P,
+                                    P, nullptr, d->status, stream));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_matmul_swiglu(const moe_bf16* A, const void* w13_packed,
+                                     const int32_t* expert_offsets, int E, int P, int K, int N,
+                                     moe_bf16* h, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  return grouped_common(A, w13_packed, expert_offsets, E, P, K, N, h, true, stream);
+}
+
+moe_status moe_grouped_matmul(const moe_bf16* A, const void* w_packed,
+                              const int32_t* expert_offsets, int E, int P, int K, int N,
+                              moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  return grouped_common(A, w_packed, expert_offsets, E, P, K, N, y, false, stream);
+}
+
+// ---------------------------------------------------------------- finalize --
+moe_status moe_finalize_routing(const moe_bf16* y2, const float* topk_w,
+                                const int32_t* expanded_row_idx, int T, int k, int H,
+                                moe_bf16* out, moe_stream_t stream) {
+  if (!y2 || !topk_w || !expanded_row_idx || !out || !aligned16(y2) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || k > 32 || H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_finalize(y2, topk_w, expanded_row_idx, T, k, H, out, stream));
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------- whole layer --
+size_t moe_forward_workspace_size(int T, int H, int E, int k, int I) {
+  if (check_layer_shape(T, H, E, k, I) != MOE_OK) return 0;
+  return forward_layout(T, H, E, k, I).total;
+}
+
+moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_override,
+                       const void* w13_packed, const void* down_packed, int T, int H, int E, int k,
+                       int I, moe_bf16* out, int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+  if (!x || !w13_packed || !down_packed || !out) return MOE_ERR_INVALID_ARG;
+  if (!logits_override && !Wg) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13_packed) || !aligned16(down_packed) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_layer_shape(T, H, E, k, I));
+  const ForwardLayout L = forward_layout(T, H, E, k, I);
+  if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_WORKSPACE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  const int P = T * k;
+  int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(ws, L.ids);
+  float* w = topk_w_out ? topk_w_out : at<float>(ws, L.w);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* eri = at<int32_t>(ws, L.eri);
+  int32_t* sri = at<int32_t>(ws, L.sri);
+  int* done = at<int>(ws, L.done);
+  uint16_t* xe = at<uint16_t>(ws, L.xe);
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  uint16_t* y2 = at<uint16_t>(ws, L.y2);
+
+  if (logits_override) {
+    MOE_CUDA(moe::launch_gating(logits_override, 1, T, E, k, 1, ids, w, d->status, stream));
+  } else {
+    const moe::RouterPlan rp = moe::router_plan(T, H, E);
+    float* part = at<float>(ws, L.router);
+    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, part, stream));
+    MOE_CUDA(moe::launch_gating(part, rp.splits, T, E, k, 1, ids, w, d->status, stream));
+  }
+  MOE_CUDA(moe::launch_routing(ids, P, E, at<int32_t>(ws, L.counts), offsets, eri, sri,
+                               at<void>(ws, L.routing), done, d->status, stream));
+  MOE_CUDA(moe::launch_gather_rows(x, sri, offsets, E, P, H, k, xe, stream));
+  moe::GemmPhase g1{}, g2{};
+  g1.A_weights = w13_packed;
+  g1.B_act = xe;
+  g1.out = h;
+  g1.K = H;
+  g1.MW = 2 * I;
+  g1.n_out = I;
+  g1.swiglu = 1;
+  g2.A_weights = down_packed;
+  g2.B_act = h;
+  g2.out = y2;
+  g2.K = I;
+  g2.MW = H;
+  g2.n_out = H;
+  g2.swiglu = 0;
+  MOE_CUDA(moe::launch_grouped_gemm(&g1, &g2, offsets, E, P, T, done, d->status, stream));
+  MOE_CUDA(moe::launch_finalize(y2, w, eri, T, k, H, out, stream));
+  return MOE_OK;
+}
+
+}  // extern "C"

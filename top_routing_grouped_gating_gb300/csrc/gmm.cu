@@ -1,0 +1,542 @@
+// Persistent grouped GEMM on the sm_103a tensor cores (tcgen05 + TMEM + TMA) for
+// the expert MLPs of the page "基于Atlas A3、950训练/推理集群的Qwen3-MoE模型低时延
+// 推理性能优化实践": §高性能专家计算 (grouped_matmul over all experts at once) with
+// §计算分解's SwiGLU fused into the epilogue of the gate/up projection.
+//
+// Orientation.  Every tile is  D[128 weight rows][N tokens] = W_tile . X_tile^T :
+// the packed weights are the MMA's A operand (M = 128 output features), the
+// expert's token rows are the B operand (N = 16..BN tokens, a multiple of 16 set
+// per tile from the expert's row count).  Decode-size experts (a few rows) then
+// cost one thin MMA per K step while the 128-row weight tiles stream from HBM;
+// prefill-size experts use N up to BN = 256 so each weight tile is reused by 256
+// tokens.
+//
+// Work unit = (phase, expert, 128-row weight block, token block).  Phase 0 is the
+// gate/up projection (weights packed so each 128-row block holds 64 gate rows and
+// the 64 matching up rows); phase 1 is the down projection.  Units are numbered
+// phase-major, expert-major, weight-block-major, token-block-minor and handed to
+// CTAs round-robin (grid = SM count, one CTA per SM).  When both phases run in one
+// launch, a phase-1 unit waits until every phase-0 unit of its expert has
+// published its rows of h (per-expert counter, release/acquire + async-proxy
+// fence); phase-0 units never wait, so the wait always ends.
+//
+// Warp roles (256 threads): warp 0 lane 0 = TMA producer; warp 1 lane 0 = MMA
+// issuer; warp 2 = TMEM allocator; warps 4-7 = epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. +31).  Shared memory holds a STAGES-deep ring of (A 128x64, B BNx64)
+// bf16 tiles in the 128-byte-swizzled K-major layout TMA writes; TMEM holds two
+// 128 x BN fp32 accumulators so the epilogue of one unit overlaps the MMAs of the
+// next.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kBM = 128;         // weight rows per tile (MMA M)
+constexpr int kBK = 64;          // K per stage: one 128-byte swizzle row of bf16
+constexpr int kBoxRows = 16;     // token rows per TMA box
+constexpr int kThreads = 256;
+constexpr int kMaxE = 256;
+constexpr int kABytes = kBM * kBK * 2;          // 16 KB
+constexpr int kBoxBytes = kBoxRows * kBK * 2;   // 2 KB
+constexpr int kEpiBytes = 32 * 64 * 4 + 32 * 64 * 2;  // SwiGLU exchange + h staging
+
+struct GemmArgs {
+  const int32_t* offsets;
+  int E;
+  int K[2];
+  int MW[2];
+  int ld[2];
+  int swiglu[2];
+  int active[2];
+  uint16_t* out[2];
+  int* done;      // per-expert count of finished phase-0 units, or null
+  int* status;
+};
+
+template <int BN, int STAGES>
+struct Layout {
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + STAGES * kABytes;
+  static constexpr int kEpi = kB + STAGES * kBBytes;
+  static constexpr int kBar = kEpi + kEpiBytes;              // 8-byte aligned
+  static constexpr int kNumBars = 2 * STAGES + 5;            // full, empty, tfull[2], tempty[2], fin
+  static constexpr int kMisc = kBar + kNumBars * 8;          // tmem addr, abort flag
+  static constexpr int kTables = kMisc + 16;                 // off, uoff0, uoff1 (kMaxE+1 each), scan tmp
+  static constexpr int kEnd = kTables + (3 * (kMaxE + 1) + 8) * 4;
+  static constexpr int kSmemBytes = kEnd + 1024;             // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct Unit {
+  int ph, e, mb, row0, rows;
+};
+
+struct Tables {
+  const int* off;
+  const int* uoff[2];
+  int E;
+};
+
+template <int BN>
+__device__ __forceinline__ Unit decode_unit(int u, const Tables& tb) {
+  Unit r;
+  const int total0 = tb.uoff[0][tb.E];
+  r.ph = (u < total0) ? 0 : 1;
+  if (r.ph) u -= total0;
+  const int* uo = tb.uoff[r.ph];
+  int lo = 0, hi = tb.E;  // uo[lo] <= u < uo[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (uo[mid] <= u) lo = mid;
+    else hi = mid;
+  }
+  r.e = lo;
+  const int local = u - uo[lo];
+  const int m = tb.off[lo + 1] - tb.off[lo];
+  const int nb = (m + BN - 1) / BN;
+  r.mb = local / nb;
+  const int b = local - r.mb * nb;
+  r.row0 = tb.off[lo] + b * BN;
+  r.rows = min(BN, tb.off[lo + 1] - r.row0);
+  return r;
+}
+
+__device__ __forceinline__ bool wait_counter(const int* p, int need, const volatile int* abort) {
+  if (ld_acquire_gpu(p) >= need) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= need) return true;
+    if ((i & 15u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
+                        const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmA1,
+                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+  using L = Layout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem + L::kA;
+  uint8_t* sB = smem + L::kB;
+  uint8_t* sEpi = smem + L::kEpi;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* fin = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  int* s_off = reinterpret_cast<int*>(smem + L::kTables);
+  int* s_uoff0 = s_off + (kMaxE + 1);
+  int* s_uoff1 = s_uoff0 + (kMaxE + 1);
+  int* s_tmp = s_uoff1 + (kMaxE + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = args.E;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(fin, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 2) {
+    tmem_alloc(s_tmem, 2 * BN);
+    tmem_relinquish();
+  }
+  for (int i = tid; i <= E; i += kThreads) s_off[i] = args.offsets[i];
+  __syncthreads();
+
+  // Units per expert and their exclusive prefix, per phase (E <= 256 = threads).
+  {
+    int u[2] = {0, 0};
+    if (tid < E) {
+      const int m = s_off[tid + 1] - s_off[tid];
+      const int nb = (m + BN - 1) / BN;
+      u[0] = args.active[0] ? nb * (args.MW[0] / kBM) : 0;
+      u[1] = args.active[1] ? nb * (args.MW[1] / kBM) : 0;
+    }
+    for (int p = 0; p < 2; ++p) {
+      int inc = u[p];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) s_tmp[warp] = inc;
+      __syncthreads();
+      int pre = 0, tot = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        if (w < warp) pre += s_tmp[w];
+        tot += s_tmp[w];
+      }
+      int* dst = p ? s_uoff1 : s_uoff0;
+      if (tid < E) dst[tid] = pre + inc - u[p];
+      if (tid == 0) dst[E] = tot;
+      __syncthreads();
+    }
+  }
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
+  Tables tb;
+  tb.off = s_off;
+  tb.uoff[0] = s_uoff0;
+  tb.uoff[1] = s_uoff1;
+  tb.E = E;
+  const int total = s_uoff0[E] + s_uoff1[E];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer --
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t par = 0;
+      uint32_t issued_mask = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Unit t = decode_unit<BN>(u, tb);
+        if (t.ph == 1 && args.done != nullptr) {
+          const int m = s_off[t.e + 1] - s_off[t.e];
+          const int need = ((m + BN - 1) / BN) * (args.MW[0] / kBM);
+          if (!wait_counter(args.done + t.e, need, s_abort)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        const CUtensorMap* ta = t.ph ? &tmA1 : &tmA0;
+        const CUtensorMap* tbm = t.ph ? &tmB1 : &tmB0;
+        const int nbox = (t.rows + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes = kABytes + nbox * kBoxBytes;
+        const int arow = t.e * args.MW[t.ph] + t.mb * kBM;
+        const int nk = args.K[t.ph] / kBK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(sA + stage * kABytes, ta, &full[stage], kb * kBK, arow, pol_w);
+          for (int j = 0; j < nbox; ++j)
+            tma_load_2d(sB + stage * L::kBBytes + j * kBoxBytes, tbm, &full[stage], kb * kBK,
+                        t.row0 + j * kBoxRows, pol_x);
+          issued_mask |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (par << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (ok) {
+        // producer tail: wait until the MMA unit has released every stage, so no
+        // commit-arrive is still in flight when the CTA exits
+        for (int i = 0; i < STAGES; ++i) {
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        // let copies already in flight land before the CTA's shared memory goes away
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued_mask >> s) & 1u) mbar_wait(&full[s], (issued_par >> s) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------- MMA issuer --
+      int stage = 0, acc = 0;
+      uint32_t par = 0, apar = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Unit t = decode_unit<BN>(u, tb);
+        const int n = (t.rows + 15) & ~15;
+        const uint32_t idesc = idesc_bf16_f32(kBM, n);
+        if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+        const int nk = args.K[t.ph] / kBK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], par, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_u32(sA + stage * kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * L::kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
+                        (kb | kk) ? 1u : 0u);
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) apar ^= 1u;
+      }
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        tc_commit(fin);  // drain this thread's outstanding MMAs before TMEM is freed
+        mbar_wait(fin, 0, nullptr);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue --
+    const int q = warp & 3;          // TMEM lane quarter
+    const int et = tid - 128;        // 0..127
+    int* s_flag = s_tmp;             // broadcast of the elected wait's result
+    int acc = 0;
+    uint32_t apar = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const Unit t = decode_unit<BN>(u, tb);
+      if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort) ? 1 : 0;
+      named_bar_sync(1, 128);
+      const int ok = s_flag[0];
+      named_bar_sync(1, 128);
+      if (!ok) {
+        if (et == 0) {
+          *s_abort = 1;
+          flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      uint16_t* out = args.out[t.ph];
+      const int ld = args.ld[t.ph];
+      if (args.swiglu[t.ph]) {
+        // lanes 0-63 of the tile are gate rows, 64-127 the matching up rows
+        float* xbuf = reinterpret_cast<float*>(sEpi);                   // [32 tok][64] fp32
+        uint16_t* hbuf = reinterpret_cast<uint16_t*>(sEpi + 32 * 64 * 4);  // [32 tok][64] bf16
+        for (int c0 = 0; c0 < t.rows; c0 += 32) {
+          float v[32];
+          tmem_ld_32x32b_x32(tbase + c0, v);
+          if (q >= 2) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xbuf[j * 64 + (q - 2) * 32 + lane] = v[j];
+          }
+          named_bar_sync(1, 128);
+          if (q < 2) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float g = v[j];
+              const float up = xbuf[j * 64 + q * 32 + lane];
+              const float h = g / (1.0f + __expf(-g)) * up;
+              hbuf[j * 64 + q * 32 + lane] = f2bf(h);
+            }
+          }
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int it = 0; it < 2; ++it) {
+            const int idx = et + it * 128;
+            const int j = idx >> 3, c = idx & 7;
+            if (c0 + j < t.rows) {
+              const uint4 val = *reinterpret_cast<const uint4*>(hbuf + j * 64 + c * 8);
+              *reinterpret_cast<uint4*>(out + (size_t)(t.row0 + c0 + j) * ld + t.mb * 64 + c * 8) =
+                  val;
+            }
+          }
+          named_bar_sync(1, 128);
+        }
+      } else {
+        uint16_t* tbw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 32;  // [32 tok][32] bf16
+        for (int c0 = 0; c0 < t.rows; c0 += 32) {
+          float v[32];
+          tmem_ld_32x32b_x32(tbase + c0, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tbw[j * 32 + lane] = f2bf(v[j]);
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int idx = lane + 32 * it;
+            const int j = idx >> 2, c = idx & 3;
+            if (c0 + j < t.rows) {
+              const uint4 val = *reinterpret_cast<const uint4*>(tbw + j * 32 + c * 8);
+              *reinterpret_cast<uint4*>(out + (size_t)(t.row0 + c0 + j) * ld + t.mb * kBM +
+                                        q * 32 + c * 8) = val;
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (t.ph == 0 && args.done != nullptr) {
+        __threadfence();
+        fence_proxy_async_global();
+        named_bar_sync(1, 128);
+        if (et == 0) red_release_add_gpu(args.done + t.e, 1);
+      }
+      acc ^= 1;
+      if (acc == 0) apar ^= 1u;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// Packed w13: per expert 2I rows of H; row block b (128 rows) = gate columns
+// 64b..64b+63 then up columns I+64b..I+64b+63.  Tiled 32x32 transpose.
+__global__ void pack_w13_kernel(const uint16_t* __restrict__ w13, int H, int I,
+                                uint16_t* __restrict__ out) {
+  __shared__ uint16_t tile[32][33];
+  const int h0 = blockIdx.x * 32, r0 = blockIdx.y * 32, e = blockIdx.z;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int blk = r0 / 128, within = r0 % 128;
+  const int col0 = within < 64 ? blk * 64 + within : I + blk * 64 + (within - 64);
+  const size_t n2 = 2 * (size_t)I;
+  for (int i = ty; i < 32; i += 8) tile[i][tx] = w13[((size_t)e * H + h0 + i) * n2 + col0 + tx];
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8)
+    out[((size_t)e * n2 + r0 + i) * H + h0 + tx] = tile[tx][i];
+}
+
+// Packed down: per expert H rows of I (down^T).
+__global__ void pack_down_kernel(const uint16_t* __restrict__ down, int H, int I,
+                                 uint16_t* __restrict__ out) {
+  __shared__ uint16_t tile[32][33];
+  const int i0 = blockIdx.x * 32, n0 = blockIdx.y * 32, e = blockIdx.z;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int i = ty; i < 32; i += 8) tile[i][tx] = down[((size_t)e * I + i0 + i) * H + n0 + tx];
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8)
+    out[((size_t)e * H + n0 + i) * I + i0 + tx] = tile[tx][i];
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_t* offsets, int E,
+                        int P, int* done, int* status, cudaStream_t s) {
+  using L = Layout<BN, STAGES>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+      err = cudaFuncSetAttribute(grouped_gemm_kernel<BN, STAGES>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+      if (err != cudaSuccess) return err;
+      attr_set[dev] = true;
+    }
+  }
+  GemmArgs a{};
+  a.offsets = offsets;
+  a.E = E;
+  a.done = (ph0 && ph1) ? done : nullptr;
+  a.status = status;
+  CUtensorMap tm[4];
+  const GemmPhase* phs[2] = {ph0, ph1};
+  for (int p = 0; p < 2; ++p) {
+    const GemmPhase* g = phs[p] ? phs[p] : (ph0 ? ph0 : ph1);
+    a.active[p] = phs[p] != nullptr;
+    a.K[p] = g->K;
+    a.MW[p] = g->MW;
+    a.ld[p] = g->n_out;
+    a.swiglu[p] = g->swiglu;
+    a.out[p] = g->out;
+    if (!encode_tmap_2d_bf16(&tm[2 * p], g->A_weights, (uint64_t)g->K, (uint64_t)E * g->MW, kBK,
+                             kBM))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap_2d_bf16(&tm[2 * p + 1], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK,
+                             kBoxRows))
+      return cudaErrorInvalidValue;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_sm_count(), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = a.done != nullptr ? 1 : 0;  // co-residency for the phase dependency
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<BN, STAGES>, tm[0], tm[1], tm[2], tm[3], a);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
+                                const int32_t* offsets, int E, int P, int max_rows_hint,
+                                int* done_counter, int* status, cudaStream_t s) {
+  (void)max_rows_hint;
+  // Thin token tiles when the mean expert load is small (decode), wide ones else.
+  if ((long long)P <= 16LL * E)
+    return launch_impl<32, 10>(ph0, ph1, offsets, E, P, done_counter, status, s);
+  return launch_impl<256, 4>(ph0, ph1, offsets, E, P, done_counter, status, s);
+}
+
+cudaError_t launch_pack_w13(const uint16_t* w13, int E, int H, int I, uint16_t* out,
+                            cudaStream_t s) {
+  dim3 grid(H / 32, 2 * I / 32, E), block(32, 8);
+  pack_w13_kernel<<<grid, block, 0, s>>>(w13, H, I, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_down(const uint16_t* down, int E, int H, int I, uint16_t* out,
+                             cudaStream_t s) {
+  dim3 grid(I / 32, H / 32, E), block(32, 8);
+  pack_down_kernel<<<grid, block, 0, s>>>(down, H, I, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

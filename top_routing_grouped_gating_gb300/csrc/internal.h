@@ -1,0 +1,74 @@
+// Internal launchers shared between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---- router / gating (router_gating.cu)
+struct RouterPlan {
+  int splits;      // split-K factor over H
+  int t_tiles;     // ceil(T / 32)
+  int e_tiles;     // ceil(E / 128)
+};
+RouterPlan router_plan(int T, int H, int E);
+// partial[s][T][E] when splits > 1, else writes out directly.
+cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
+                          const RouterPlan& plan, float* partial_or_out, cudaStream_t s);
+cudaError_t launch_router_reduce(const float* partial, int splits, int T, int E, float* logits,
+                                 cudaStream_t s);
+// Gating reads sum_{s<splits} src[s*T*E + t*E + e] (splits == 1: plain logits).
+cudaError_t launch_gating(const float* src, int splits, int T, int E, int k, int renormalize,
+                          int32_t* ids, float* w, int* status, cudaStream_t s);
+
+// ---- routing (routing.cu)
+struct RoutingPlan {
+  bool single_cta;
+  int chunks;        // multi-CTA path: number of pair chunks
+  int chunk_pairs;   // pairs per chunk
+};
+RoutingPlan routing_plan(int P, int E);
+size_t routing_ws_bytes(int P, int E);
+// ids (P); writes counts (may be null), offsets (E+1), eri (P), sri (P).
+// zero_counter (E ints, may be null) is cleared for the fused GEMM dependency.
+cudaError_t launch_routing(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* eri, int32_t* sri, void* ws, int* zero_counter, int* status,
+                           cudaStream_t s);
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sri, const int32_t* offsets,
+                               int E, int P, int H, int k, uint16_t* expanded_x, cudaStream_t s);
+cudaError_t launch_expert_tokens(const int32_t* ids, int P, int E, int32_t* counts,
+                                 int32_t* offsets, int* status, cudaStream_t s);
+cudaError_t launch_finalize(const uint16_t* y2, const float* w, const int32_t* eri, int T, int k,
+                            int H, uint16_t* out, cudaStream_t s);
+
+// ---- grouped GEMM (gmm.cu)
+struct GemmPhase {
+  const void* A_weights;   // packed weights, rows = E * MW, cols = K
+  const uint16_t* B_act;   // activations (P, K)
+  uint16_t* out;           // (P, n_out)
+  int K;                   // reduction length
+  int MW;                  // weight rows per expert (2I for gate/up, H for down)
+  int n_out;               // output columns (I for gate/up, H for down)
+  int swiglu;              // 1: SwiGLU epilogue on interleaved gate/up rows
+};
+// phases[0] and/or phases[1] (null A_weights = phase absent).  When both are
+// present they run in one persistent launch with a per-expert dependency on
+// done_counter (E ints, zeroed beforehand).
+cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
+                                const int32_t* offsets, int E, int P, int max_rows_hint,
+                                int* done_counter, int* status, cudaStream_t s);
+cudaError_t launch_pack_w13(const uint16_t* w13, int E, int H, int I, uint16_t* out,
+                            cudaStream_t s);
+cudaError_t launch_pack_down(const uint16_t* down, int E, int H, int I, uint16_t* out,
+                             cudaStream_t s);
+
+// ---- device facts (api.cu)
+int device_sm_count();
+bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
+                         uint32_t box_inner, uint32_t box_rows);
+
+}  // namespace moe

@@ -1,0 +1,214 @@
+// Router scores and top-k softmax gating.
+//
+// Router: logits = x (T,H bf16) . Wg (H,E fp32) on CUDA cores in fp32 FMA -- the
+// page "基于Atlas A3、950训练/推理集群的Qwen3-MoE模型低时延推理性能优化实践"
+// (§融合RMSNorm Cast) keeps the gate computation in FP32.  Tiles of 32 tokens x
+// 128 experts; the H axis is split across CTAs when there are few tiles (decode),
+// and the partial sums are added later in a fixed order, so results are
+// bit-reproducible.
+//
+// Gating (§快速选择专家): one warp per token.  Lane l holds experts l, l+32, ...;
+// k rounds of a warp-wide arg-max under (logit desc, expert id asc) pick the
+// slots; weights are softmax over the chosen logits (renormalised) or the
+// full-softmax probabilities.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRT = 32;    // tokens per router tile
+constexpr int kRE = 128;   // experts per router tile
+constexpr int kRK = 32;    // H rows per smem step
+
+__global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict__ x,
+                                                     const float* __restrict__ Wg, int T, int H,
+                                                     int E, int h_per_split,
+                                                     float* __restrict__ out) {
+  __shared__ float xs[kRT][kRK + 1];
+  __shared__ float ws[kRK][kRE];
+  const int tid = threadIdx.x;
+  const int tx = tid & 31;          // experts e0 + tx + 32*i
+  const int ty = tid >> 5;          // tokens t0 + 4*ty + j
+  const int t0 = blockIdx.x * kRT;
+  const int e0 = blockIdx.y * kRE;
+  const int split = blockIdx.z;
+  const int hb = split * h_per_split;
+  float acc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
+
+  for (int h0 = hb; h0 < hb + h_per_split; h0 += kRK) {
+    {  // x tile: 32 tokens x 32 h (bf16 -> fp32); 4 elements per thread
+      const int tt = tid >> 3, hh = (tid & 7) * 4;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t0 + tt < T) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)(t0 + tt) * H + h0 + hh);
+        v[0] = bf16_lo(raw.x);
+        v[1] = bf16_hi(raw.x);
+        v[2] = bf16_lo(raw.y);
+        v[3] = bf16_hi(raw.y);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xs[tt][hh + q] = v[q];
+    }
+#pragma unroll
+    for (int r = 0; r < (kRK * kRE) / 256; ++r) {  // Wg tile: 32 h x 128 experts
+      const int idx = tid + 256 * r;
+      const int hh = idx / kRE, ee = idx % kRE;
+      ws[hh][ee] = (e0 + ee < E) ? Wg[(size_t)(h0 + hh) * E + e0 + ee] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < kRK; ++kk) {
+      float xv[4], wv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xv[j] = xs[4 * ty + j][kk];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) wv[i] = ws[kk][tx + 32 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[j][i] = fmaf(xv[j], wv[i], acc[j][i]);
+    }
+    __syncthreads();
+  }
+  float* dst = out + (size_t)split * T * E;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int t = t0 + 4 * ty + j;
+    if (t >= T) continue;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + tx + 32 * i;
+      if (e < E) dst[(size_t)t * E + e] = acc[j][i];
+    }
+  }
+}
+
+__global__ void router_reduce_kernel(const float* __restrict__ partial, int splits, size_t n,
+                                     float* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float s = partial[i];
+    for (int p = 1; p < splits; ++p) s += partial[(size_t)p * n + i];
+    out[i] = s;
+  }
+}
+
+// (a beats b) under logit descending, expert id ascending.
+__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+__global__ void __launch_bounds__(256) gating_kernel(const float* __restrict__ src, int splits,
+                                                     int T, int E, int k, int renormalize,
+                                                     int32_t* __restrict__ ids,
+                                                     float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  const size_t n = (size_t)T * E;
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      float s = src[(size_t)t * E + e];
+      for (int p = 1; p < splits; ++p) s += src[(size_t)p * n + (size_t)t * E + e];
+      v[i] = s;
+    } else {
+      v[i] = -INFINITY;
+    }
+  }
+  uint32_t taken = 0;
+  float my_v = -INFINITY;
+  int my_i = 0;
+  for (int s = 0; s < k; ++s) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && beats(v[i], e, bv, bi)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (beats(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == s) {
+      my_v = bv;
+      my_i = bi;
+    }
+  }
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);  // slot 0 holds the maximum
+  float num = (lane < k) ? expf(my_v - m) : 0.f;
+  float den;
+  if (renormalize) {
+    den = num;
+  } else {
+    den = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < E) den += expf(v[i] - m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  if (lane < k) {
+    ids[(size_t)t * k + lane] = my_i;
+    w[(size_t)t * k + lane] = num / den;
+  }
+}
+
+}  // namespace
+
+RouterPlan router_plan(int T, int H, int E) {
+  RouterPlan p;
+  p.t_tiles = (T + kRT - 1) / kRT;
+  p.e_tiles = (E + kRE - 1) / kRE;
+  const int tiles = p.t_tiles * p.e_tiles;
+  int s = 1;
+  // split H until there are ~128 CTAs, keeping each split a multiple of kRK rows
+  while (s < 16 && tiles * s * 2 <= 128 && (H / kRK) % (s * 2) == 0) s *= 2;
+  p.splits = s;
+  return p;
+}
+
+cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
+                          const RouterPlan& plan, float* out, cudaStream_t s) {
+  dim3 grid(plan.t_tiles, plan.e_tiles, plan.splits);
+  router_kernel<<<grid, 256, 0, s>>>(x, Wg, T, H, E, H / plan.splits, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_reduce(const float* partial, int splits, int T, int E, float* logits,
+                                 cudaStream_t s) {
+  const size_t n = (size_t)T * E;
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  router_reduce_kernel<<<blocks, 256, 0, s>>>(partial, splits, n, logits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gating(const float* src, int splits, int T, int E, int k, int renormalize,
+                          int32_t* ids, float* w, int* status, cudaStream_t s) {
+  (void)status;
+  const int blocks = (T + 7) / 8;
+  gating_kernel<<<blocks, 256, 0, s>>>(src, splits, T, E, k, renormalize, ids, w);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,321 @@
+// init_routing, compute_expert_tokens and finalize_routing
+// (page "基于Atlas A3、950训练/推理集群的Qwen3-MoE模型低时延推理性能优化实践",
+// §高效排序和token路由).
+//
+// init_routing is a stable counting sort of the P = T*k token-expert pairs by
+// expert id.  Pairs are taken in chunks of consecutive j; a chunk's rows for
+// expert e start at offsets[e] + (pairs of e in earlier chunks).  Inside a chunk,
+// pairs are ranked in rounds of blockDim consecutive j: __match_any_sync gives
+// the rank among equal ids inside a warp, and per-warp counts in shared memory
+// give the rank across the round's warps.  Every position is therefore the
+// unique stable one and the result is deterministic.
+//
+// Small P (decode) runs histogram, scan and scatter in one CTA; large P uses a
+// per-chunk histogram kernel, a one-CTA scan and a per-chunk scatter kernel.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kSingleCtaMaxPairs = 4096;
+constexpr int kChunkPairs = 2048;
+constexpr int kMaxExperts = 256;
+
+// Exclusive scan of one value per thread for threads [0, 256); every thread of
+// the block must call it.  s_tmp: 8 ints.  Returns the exclusive prefix; *total
+// receives the sum of all 256 values.
+__device__ int block_excl_scan_256(int v, int* s_tmp, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int x = tid < kMaxExperts ? v : 0;
+  int inc = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += y;
+  }
+  if (warp < 8 && lane == 31) s_tmp[warp] = inc;
+  __syncthreads();
+  int pre = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int c = s_tmp[w];
+    if (w < warp) pre += c;
+    tot += c;
+  }
+  __syncthreads();
+  *total = tot;
+  return pre + inc - x;
+}
+
+// Scatter pairs [j_begin, j_end) in order.  s_base[e] = first free row of e for
+// this range (advanced as rounds complete); s_wcnt = (warps x E) zeros.
+__device__ void scatter_range(const int32_t* __restrict__ ids, int j_begin, int j_end, int E,
+                              int* s_base, int* s_wcnt, int32_t* __restrict__ eri,
+                              int32_t* __restrict__ sri) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  for (int j0 = j_begin; j0 < j_end; j0 += blockDim.x) {
+    const int j = j0 + tid;
+    int e = -1;                       // -1: no pair in this slot
+    if (j < j_end) {
+      e = ids[j];
+      if (e < 0 || e >= E) e = -2;    // -2: invalid id, pair dropped
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) s_wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += s_wcnt[w * E + e];
+      const int p = s_base[e] + before + rank;
+      eri[j] = p;
+      sri[p] = j;
+    } else if (e == -2) {
+      eri[j] = -1;
+    }
+    __syncthreads();
+    for (int x = tid; x < E; x += blockDim.x) {
+      int s = 0;
+      for (int w = 0; w < nwarps; ++w) {
+        s += s_wcnt[w * E + x];
+        s_wcnt[w * E + x] = 0;
+      }
+      s_base[x] += s;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kRouteThreads) routing_single_cta_kernel(
+    const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ eri, int32_t* __restrict__ sri,
+    int* __restrict__ zero_counter, int* status) {
+  __shared__ int s_hist[kMaxExperts];
+  __shared__ int s_base[kMaxExperts];
+  __shared__ int s_tmp[8];
+  __shared__ int s_wcnt[(kRouteThreads / 32) * kMaxExperts];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kMaxExperts; i += blockDim.x) s_hist[i] = 0;
+  for (int i = tid; i < (kRouteThreads / 32) * E; i += blockDim.x) s_wcnt[i] = 0;
+  if (zero_counter != nullptr)
+    for (int i = tid; i < E; i += blockDim.x) zero_counter[i] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int j = tid; j < P; j += blockDim.x) {
+    const int e = ids[j];
+    if (e >= 0 && e < E) atomicAdd(&s_hist[e], 1);
+    else bad = true;
+  }
+  if (bad) flag_status(status, MOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+  int total = 0;
+  const int c = (tid < E) ? s_hist[tid] : 0;
+  const int off = block_excl_scan_256(c, s_tmp, &total);
+  if (tid < E) {
+    s_base[tid] = off;
+    offsets[tid] = off;
+    if (counts != nullptr) counts[tid] = c;
+  }
+  if (tid == 0) offsets[E] = total;
+  __syncthreads();
+  scatter_range(ids, 0, P, E, s_base, s_wcnt, eri, sri);
+}
+
+__global__ void __launch_bounds__(kRouteThreads) routing_hist_kernel(
+    const int32_t* __restrict__ ids, int P, int E, int chunk_pairs, int32_t* __restrict__ chunk_hist,
+    int* status) {
+  __shared__ int s_hist[kMaxExperts];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < E; i += blockDim.x) s_hist[i] = 0;
+  __syncthreads();
+  const int j0 = blockIdx.x * chunk_pairs;
+  const int j1 = min(P, j0 + chunk_pairs);
+  bool bad = false;
+  for (int j = j0 + tid; j < j1; j += blockDim.x) {
+    const int e = ids[j];
+    if (e >= 0 && e < E) atomicAdd(&s_hist[e], 1);
+    else bad = true;
+  }
+  if (bad) flag_status(status, MOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+  for (int i = tid; i < E; i += blockDim.x) chunk_hist[(size_t)blockIdx.x * E + i] = s_hist[i];
+}
+
+// chunk_hist[c][e] (counts) -> chunk_hist[c][e] (first row of e for chunk c).
+__global__ void __launch_bounds__(256) routing_scan_kernel(int32_t* __restrict__ chunk_hist,
+                                                           int chunks, int E,
+                                                           int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ offsets,
+                                                           int* __restrict__ zero_counter) {
+  __shared__ int s_tmp[8];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int c = 0; c < chunks; ++c) {
+      const int h = chunk_hist[(size_t)c * E + e];
+      chunk_hist[(size_t)c * E + e] = run;
+      run += h;
+    }
+  }
+  int total = 0;
+  const int off = block_excl_scan_256(e < E ? run : 0, s_tmp, &total);
+  if (e < E) {
+    if (counts != nullptr) counts[e] = run;
+    offsets[e] = off;
+    if (zero_counter != nullptr) zero_counter[e] = 0;
+    for (int c = 0; c < chunks; ++c) chunk_hist[(size_t)c * E + e] += off;
+  }
+  if (e == 0) offsets[E] = total;
+}
+
+__global__ void __launch_bounds__(kRouteThreads) routing_scatter_kernel(
+    const int32_t* __restrict__ ids, int P, int E, int chunk_pairs,
+    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ eri, int32_t* __restrict__ sri) {
+  __shared__ int s_base[kMaxExperts];
+  __shared__ int s_wcnt[(kRouteThreads / 32) * kMaxExperts];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < E; i += blockDim.x) s_base[i] = chunk_base[(size_t)blockIdx.x * E + i];
+  for (int i = tid; i < (kRouteThreads / 32) * E; i += blockDim.x) s_wcnt[i] = 0;
+  __syncthreads();
+  const int j0 = blockIdx.x * chunk_pairs;
+  scatter_range(ids, j0, min(P, j0 + chunk_pairs), E, s_base, s_wcnt, eri, sri);
+}
+
+// expanded_x[p] = x[sri[p] / k] for p < offsets[E]; one warp per row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ sri,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int E, int P, int H, int k,
+                                                          uint16_t* __restrict__ xe) {
+  const int lane = threadIdx.x & 31;
+  const int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (p >= P || p >= offsets[E]) return;
+  const int t = sri[p] / k;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  uint4* dst = reinterpret_cast<uint4*>(xe + (size_t)p * H);
+  for (int v = lane; v < H / 8; v += 32) dst[v] = src[v];
+}
+
+__global__ void __launch_bounds__(kRouteThreads) expert_tokens_kernel(
+    const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int* status) {
+  __shared__ int s_hist[kMaxExperts];
+  __shared__ int s_tmp[8];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kMaxExperts; i += blockDim.x) s_hist[i] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int j = tid; j < P; j += blockDim.x) {
+    const int e = ids[j];
+    if (e >= 0 && e < E) atomicAdd(&s_hist[e], 1);
+    else bad = true;
+  }
+  if (bad) flag_status(status, MOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+  int total = 0;
+  const int c = (tid < E) ? s_hist[tid] : 0;
+  const int off = block_excl_scan_256(c, s_tmp, &total);
+  if (tid < E) {
+    counts[tid] = c;
+    if (offsets != nullptr) offsets[tid] = off;
+  }
+  if (tid == 0 && offsets != nullptr) offsets[E] = total;
+}
+
+// out[t] = sum_s w[t,s] * y2[eri[t*k+s]] in fp32, slot order; one CTA per token.
+__global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restrict__ y2,
+                                                       const float* __restrict__ w,
+                                                       const int32_t* __restrict__ eri, int k,
+                                                       int H, uint16_t* __restrict__ out) {
+  __shared__ int s_row[32];
+  __shared__ float s_w[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    s_row[threadIdx.x] = eri[(size_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  for (int v = threadIdx.x; v < H / 8; v += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int s = 0; s < k; ++s) {
+      const int p = s_row[s];
+      if (p < 0) continue;
+      const float ws = s_w[s];
+      const uint4 q = reinterpret_cast<const uint4*>(y2 + (size_t)p * H)[v];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(ws, bf16_lo(u[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(ws, bf16_hi(u[i]), acc[2 * i + 1]);
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(out + (size_t)t * H)[v] = o;
+  }
+}
+
+}  // namespace
+
+RoutingPlan routing_plan(int P, int E) {
+  (void)E;
+  RoutingPlan r;
+  r.single_cta = P <= kSingleCtaMaxPairs;
+  r.chunk_pairs = kChunkPairs;
+  r.chunks = r.single_cta ? 1 : (P + kChunkPairs - 1) / kChunkPairs;
+  return r;
+}
+
+size_t routing_ws_bytes(int P, int E) {
+  const RoutingPlan r = routing_plan(P, E);
+  return r.single_cta ? 0 : (size_t)r.chunks * E * sizeof(int32_t);
+}
+
+cudaError_t launch_routing(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* eri, int32_t* sri, void* ws, int* zero_counter, int* status,
+                           cudaStream_t s) {
+  const RoutingPlan r = routing_plan(P, E);
+  if (r.single_cta) {
+    routing_single_cta_kernel<<<1, kRouteThreads, 0, s>>>(ids, P, E, counts, offsets, eri, sri,
+                                                          zero_counter, status);
+    return cudaGetLastError();
+  }
+  int32_t* chunk_hist = static_cast<int32_t*>(ws);
+  routing_hist_kernel<<<r.chunks, kRouteThreads, 0, s>>>(ids, P, E, r.chunk_pairs, chunk_hist,
+                                                         status);
+  routing_scan_kernel<<<1, 256, 0, s>>>(chunk_hist, r.chunks, E, counts, offsets, zero_counter);
+  routing_scatter_kernel<<<r.chunks, kRouteThreads, 0, s>>>(ids, P, E, r.chunk_pairs, chunk_hist,
+                                                            eri, sri);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sri, const int32_t* offsets,
+                               int E, int P, int H, int k, uint16_t* xe, cudaStream_t s) {
+  const int blocks = (P + 7) / 8;
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(x, sri, offsets, E, P, H, k, xe);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expert_tokens(const int32_t* ids, int P, int E, int32_t* counts,
+                                 int32_t* offsets, int* status, cudaStream_t s) {
+  expert_tokens_kernel<<<1, kRouteThreads, 0, s>>>(ids, P, E, counts, offsets, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const uint16_t* y2, const float* w, const int32_t* eri, int T, int k,
+                            int H, uint16_t* out, cudaStream_t s) {
+  const int threads = (H / 8) >= 256 ? 256 : ((H / 8 + 31) / 32) * 32;
+  finalize_kernel<<<T, threads, 0, s>>>(y2, w, eri, k, H, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
