@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE-layer forward on GB300 (one JSON line on stdout, rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+A step is one ``moe_forward`` call (router -> gating -> init_routing -> grouped GEMM
++ SwiGLU -> grouped GEMM -> finalize) over one batch of T tokens of the workload,
+with inputs and packed weights resident in HBM.  The default workload is the
+Qwen3-30B-A3B-shaped decode layer (T=32, H=2048, E=128, k=8, I=768): its active
+expert weights (~1 GB) are far larger than L2, so no L2 flush is needed between
+steps.  Timing uses CUDA events on the launching stream, bracketed by a barrier
+and a device synchronize, max over ranks.
+
+Multi-GPU: tokens are independent, so N GPUs run N replicas of the layer on their
+own batches with no collective on the data path (weak scaling); torch.distributed
+is used only for the barrier and the max-over-ranks of the elapsed time.
+
+``--impl reference`` times the CPU fp64 oracle (the test oracle under ``oracle/``,
+unmodified) on the host cores, on a bounded sample of tokens per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 GB300; % of HBM (decode) or tensor-core (prefill) peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_30b_a3b_decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the cpu_baseline sample")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- helpers ---
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def file_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the grouped-GEMM kernel from the committed ncu summary,
+    or None when there is none or the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path, encoding="utf-8").read()
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", txt)
+    if not m_b or not m_h:
+        return None
+    src = os.path.join(ROOT, "top_routing_grouped_gating_gb300", "csrc", "gmm.cu")
+    if m_h.group(1) != file_sha(src):
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    def __init__(self, dev_index: int):
+        import torch
+        self.proc = None
+        self.lines = []
+        sel = []
+        try:
+            props = torch.cuda.get_device_properties(dev_index)
+            uuid = str(getattr(props, "uuid", "") or "")
+            if uuid:
+                sel = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "50"] + sel
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def algorithmic_gemm_bytes(cfg, active: int) -> int:
+    """Bytes one grouped-GEMM launch must move: the active experts' w13 and down
+    weights, the expert-sorted activations in, h out and back in, y2 out."""
+    P = cfg.T * cfg.k
+    weights = active * 3 * cfg.H * cfg.I * 2
+    acts = P * cfg.H * 2 + 2 * P * cfg.I * 2 + P * cfg.H * 2
+    return weights + acts
+
+
+def gemm_flops(cfg) -> float:
+    return 2.0 * cfg.T * cfg.k * 3 * cfg.H * cfg.I
+
+
+def launches_per_step(cfg, router: bool = True) -> int:
+    P = cfg.T * cfg.k
+    routing = 1 if P <= 4096 else 3
+    return (1 if router else 0) + 1 + routing + 1 + 1 + 1
+
+
+# ------------------------------------------------------------ CPU oracle arm --
+
+
+def oracle_arrays(inp):
+    """Host fp64 copies of the weights (untimed: the oracle's inputs at rest)."""
+    import numpy as np
+    E = inp["w13"].shape[0]
+    w13 = [inp["w13"][e].double().cpu().numpy() for e in range(E)]
+    down = [inp["down"][e].double().cpu().numpy() for e in range(E)]
+    x = inp["x"].double().cpu().numpy()
+    Wg = inp["Wg"].double().cpu().numpy()
+    return x, Wg, w13, down
+
+
+def oracle_step(O, arrays, k, rows):
+    x, Wg, w13, down = arrays
+    O.moe_forward(x[rows], Wg, w13, down, k, keep_intermediates=False)
+
+
+def time_oracle(O, arrays, k, T, target_s):
+    """Tokens/s of the oracle on consecutive token samples until ~target_s of CPU time."""
+    n = 0
+    t0 = time.perf_counter()
+    start = 0
+    while time.perf_counter() - t0 < target_s:
+        rows = [(start + i) % T for i in range(min(T, 4))]
+        oracle_step(O, arrays, k, rows)
+        n += len(rows)
+        start += len(rows)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+def run_reference(args, cfg):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+    from oracle import moe_oracle as O
+    from top_routing_grouped_gating_gb300 import workloads as W
+
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"   # same values as the GPU arm
+    inp = W.make_inputs(cfg, device=gen_dev)
+    arrays = oracle_arrays(inp)
+    del inp
+    # size each step's token sample so the whole K+W run stays within a few minutes
+    t0 = time.perf_counter()
+    oracle_step(O, arrays, cfg.k, [0])
+    per_tok = max(time.perf_counter() - t0, 1e-4)
+    budget = 150.0 / max(args.steps + args.warmup, 1)
+    ntok = int(max(1, min(cfg.T, budget // per_tok)))
+    for i in range(args.warmup):
+        oracle_step(O, arrays, cfg.k, [(i * ntok + j) % cfg.T for j in range(ntok)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_step(O, arrays, cfg.k, [(i * ntok + j) % cfg.T for j in range(ntok)])
+    dt = time.perf_counter() - t0
+    value = ntok * args.steps / dt
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{ntok} token(s) of the workload per step, numpy fp64 oracle, "
+                                   f"weights pre-widened to fp64 in host memory"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(cfg):
+    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+            "router": cfg.router, "seed": cfg.seed, "parallelism": "replicas (token batches), no collective",
+            "l2": "inputs larger than L2: the active experts' weights streamed per step exceed the 129 MB L2"}
+
+
+# ------------------------------------------------------------------- ours ---
+
+
+def run_ours(args, cfg):
+    import numpy as np
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from top_routing_grouped_gating_gb300 import build as B
+    B.build()
+    import top_routing_grouped_gating_gb300 as moe
+    from top_routing_grouped_gating_gb300 import workloads as W
+
+    inp = W.make_inputs(cfg, device=f"cuda:{local}")
+    layer = moe.MoELayer(inp["Wg"], inp["w13"], inp["down"], cfg.k)
+    x = inp["x"]
+    stream = torch.cuda.current_stream(dev)
+    out, ids, w = layer(x)
+    torch.cuda.synchronize(dev)
+    bufs = dict(out=out, topk_ids=ids, topk_w=w)
+    counts = torch.bincount(ids.flatten().long(), minlength=cfg.E)
+    active = int((counts > 0).sum())
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if ws == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- warm-up
+    for _ in range(max(args.warmup, 3)):
+        layer(x, **bufs)
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region (device-resident inputs), grouped-GEMM events on every step
+    K = args.steps
+    gb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ge = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(K):
+        moe.set_gemm_events(gb[i], ge[i])
+        layer(x, **bufs)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    moe.set_gemm_events(None, None)
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end))
+    gemm_ms = statistics.mean(gb[i].elapsed_time(ge[i]) for i in range(K))
+    status = moe.get_device_status(dev)
+
+    # ---- end-to-end: pinned host input -> device -> layer -> pinned host output
+    x_host = x.cpu().pin_memory()
+    o_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        o, _, _ = layer(x_dev, **bufs)
+        o_host.copy_(o, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e_start.record(stream)
+    for _ in range(K):
+        x_dev.copy_(x_host, non_blocking=True)
+        o, _, _ = layer(x_dev, **bufs)
+        o_host.copy_(o, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end))
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    hbm, bf16, peak_kind = measured_peaks()
+    value = cfg.T * K * ws / (ms_total / 1e3)
+    decode = cfg.T * cfg.k <= 16 * cfg.E
+    gbytes = algorithmic_gemm_bytes(cfg, active)
+    if decode:
+        achieved = gbytes / (gemm_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s"}
+    else:
+        achieved = gemm_flops(cfg) / (gemm_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                "frac": achieved / bf16,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops)" if peak_kind == "measured"
+                else "fallback 1.9 PFLOP/s"}
+    tr = profiled_traffic(cfg.name)
+    roof.update({"traffic": tr, "kernel": "grouped_gemm_kernel (both projections, one launch)",
+                 "kernel_ms": gemm_ms, "algorithmic_bytes": gbytes, "active_experts": active})
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(cfg),
+        "roofline": roof,
+        "e2e": {"value": cfg.T * K * ws / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": cfg.T * cfg.H * 2, "d2h_bytes_per_step": cfg.T * cfg.H * 2},
+        "gpu_launches": launches_per_step(cfg) * K,
+        "clocks": clocks,
+        "device_status": status,
+    }
+
+    if not args.no_cpu_baseline:
+        from oracle import moe_oracle as O
+        arrays = oracle_arrays({k_: v.cpu() for k_, v in inp.items()})
+        v_cpu, ntok, dt = time_oracle(O, arrays, cfg.k, cfg.T, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"{ntok} tokens of the workload in batches of 4 over {dt:.1f} s, "
+                                          f"numpy fp64 oracle, weights pre-widened to fp64 in host memory"}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from top_routing_grouped_gating_gb300 import workloads as W
+    if args.workload not in W.CONFIGS:
+        raise SystemExit(f"unknown workload {args.workload}; one of {sorted(W.CONFIGS)}")
+    cfg = W.CONFIGS[args.workload]
+    if cfg.mx:
+        raise SystemExit("the MXFP8 workload is not benchmarked by this script yet")
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

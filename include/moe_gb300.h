@@ -195,6 +195,15 @@ MOE_API moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* 
                        int I, moe_bf16* out, int32_t* topk_ids_out, float* topk_w_out, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
 
+/* -------------------------------------------------------------- profiling --
+ * Measurement aid, not part of the page's operator set: when set (non-NULL), every
+ * later moe_forward call made by this host thread records `ev_begin` on its stream
+ * just before the grouped-GEMM launch and `ev_end` just after it, so a caller can
+ * time that kernel alone with cudaEventElapsedTime.  Both are cudaEvent_t handles
+ * owned by the caller; pass NULL, NULL to stop.
+ */
+MOE_API moe_status moe_set_gemm_events(void* ev_begin, void* ev_end);
+
 #ifdef __cplusplus
 }
 #endif

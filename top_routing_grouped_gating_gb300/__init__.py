@@ -25,5 +25,6 @@ from ._binding import (  # noqa: F401
     library_path,
     pack_weights,
     router_logits,
+    set_gemm_events,
 )
 from .workloads import CONFIGS, MoEConfig, make_inputs  # noqa: F401

@@ -42,6 +42,7 @@ _SIGS = {
     "moe_forward_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "moe_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
                              _vp, _vp, _c_size, _vp]),
+    "moe_set_gemm_events": (_c_int, [_vp, _vp]),
 }
 
 DEV_BAD_EXPERT_ID = 0x1
@@ -275,6 +276,14 @@ def forward(x: torch.Tensor, Wg: Optional[torch.Tensor], w13_packed: torch.Tenso
                              T, H, E, k, I, _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel(),
                              _stream(dev)))
     return out, topk_ids, topk_w
+
+
+def set_gemm_events(ev_begin: Optional[torch.cuda.Event], ev_end: Optional[torch.cuda.Event]) -> None:
+    """Record these CUDA events around the grouped-GEMM launch of later forward calls
+    (this host thread).  None, None switches it off."""
+    b = None if ev_begin is None else ev_begin.cuda_event
+    e = None if ev_end is None else ev_end.cuda_event
+    _check("moe_set_gemm_events", lib().moe_set_gemm_events(b, e))
 
 
 def get_device_status(device=None) -> int:

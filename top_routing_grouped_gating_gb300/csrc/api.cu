@@ -126,6 +126,9 @@ ForwardLayout forward_layout(int T, int H, int E, int k, int I) {
   return L;
 }
 
+thread_local cudaEvent_t t_gemm_ev_begin = nullptr;
+thread_local cudaEvent_t t_gemm_ev_end = nullptr;
+
 template <typename T>
 T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
@@ -402,8 +405,17 @@ moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_o
   g2.MW = H;
   g2.n_out = H;
   g2.swiglu = 0;
+  if (t_gemm_ev_begin) MOE_CUDA(cudaEventRecord(t_gemm_ev_begin, stream));
   MOE_CUDA(moe::launch_grouped_gemm(&g1, &g2, offsets, E, P, T, done, d->status, stream));
+  if (t_gemm_ev_end) MOE_CUDA(cudaEventRecord(t_gemm_ev_end, stream));
   MOE_CUDA(moe::launch_finalize(y2, w, eri, T, k, H, out, stream));
+  return MOE_OK;
+}
+
+moe_status moe_set_gemm_events(void* ev_begin, void* ev_end) {
+  if ((ev_begin == nullptr) != (ev_end == nullptr)) return MOE_ERR_INVALID_ARG;
+  t_gemm_ev_begin = static_cast<cudaEvent_t>(ev_begin);
+  t_gemm_ev_end = static_cast<cudaEvent_t>(ev_end);
   return MOE_OK;
 }
 
