@@ -314,6 +314,10 @@ def run_ours(args, cfg):
     torch.cuda.synchronize(dev)
     t_start.record(stream)
     for i in range(K):
+        # torch only reports elapsed_time for events it recorded itself; record both
+        # here first, the library then re-records them around the grouped GEMM
+        gb[i].record(stream)
+        ge[i].record(stream)
         moe.set_gemm_events(gb[i], ge[i])
         layer(x, **bufs)
     t_end.record(stream)
