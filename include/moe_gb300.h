@@ -195,6 +195,28 @@ MOE_API moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* 
                        int I, moe_bf16* out, int32_t* topk_ids_out, float* topk_w_out, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
 
+/* ------------------------------------------------ allocation-free routing --
+ * No counterpart in the pages: an extra entry point for callers that cannot
+ * allocate device memory -- code living inside a host framework that owns all
+ * device memory and offers no allocator to it, or a serving loop that must not
+ * allocate once it is running.  It does what moe_init_routing does, with the
+ * same arguments minus the workspace; its scratch (about 33 KB) is a fixed array
+ * in the library's own device memory, present on every GPU that loads the
+ * library until the process exits.
+ *  - T*k must be <= MOE_NOALLOC_MAX_PAIRS, else MOE_ERR_UNSUPPORTED_SHAPE.
+ *  - It calls no allocator.  Its first call on a device (with that device
+ *    current) looks up the scratch address; make that first call before any
+ *    stream capture on that device.
+ *  - All calls on a device share the scratch: calls that may overlap on the GPU
+ *    (unordered streams) race and must be serialised by the caller.
+ */
+#define MOE_NOALLOC_MAX_PAIRS 65536
+MOE_API moe_status moe_init_routing_noalloc(const moe_bf16* x, const int32_t* topk_ids, int T, int H,
+                                            int E, int k, moe_bf16* expanded_x,
+                                            int32_t* expanded_row_idx, int32_t* sorted_row_idx,
+                                            int32_t* expert_offsets, int32_t* counts,
+                                            moe_stream_t stream);
+
 /* -------------------------------------------------------------- profiling --
  * Measurement aid, not part of the page's operator set: when set (non-NULL), every
  * later moe_forward call made by this host thread records `ev_begin` on its stream

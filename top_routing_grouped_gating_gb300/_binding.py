@@ -43,6 +43,8 @@ _SIGS = {
     "moe_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
                              _vp, _vp, _c_size, _vp]),
     "moe_set_gemm_events": (_c_int, [_vp, _vp]),
+    "moe_init_routing_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp,
+                                          _vp]),
 }
 
 DEV_BAD_EXPERT_ID = 0x1

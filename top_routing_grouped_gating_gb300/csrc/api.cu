@@ -144,6 +144,12 @@ int device_sm_count() {
   return d->sm_count;
 }
 
+int* device_status_ptr() {
+  DeviceFacts* d = nullptr;
+  if (current_device(&d) != MOE_OK) return nullptr;
+  return d->status;
+}
+
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                          uint32_t box_inner, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();

@@ -68,6 +68,7 @@ cudaError_t launch_pack_down(const uint16_t* down, int E, int H, int I, uint16_t
 
 // ---- device facts (api.cu)
 int device_sm_count();
+int* device_status_ptr();  // the current device's status word, or null
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                          uint32_t box_inner, uint32_t box_rows);
 
