@@ -108,3 +108,18 @@ def test_forward_is_deterministic(layers):
     b = layer(inp["x"])[0]
     assert torch.equal(a, b)
     assert moe.get_device_status() == 0
+
+
+def test_graphed_layer_matches_direct_calls(layers):
+    cfg, inp, layer = layers("qwen3_30b_a3b_decode")
+    g = layer.capture(cfg.T)
+    x = inp["x"]
+    ref = layer(x)[0].clone()
+    out = g(x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    x2 = torch.flip(x, dims=[0]).contiguous()
+    out2 = g(x2).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(out2, layer(x2)[0])
+    assert moe.get_device_status() == 0

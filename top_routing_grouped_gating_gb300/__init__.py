@@ -8,6 +8,7 @@ package does not need a GPU, calling an op does (there is no CPU fallback).
 from ._binding import (  # noqa: F401
     DEV_BAD_EXPERT_ID,
     DEV_WAIT_TIMEOUT,
+    GraphedMoELayer,
     MoEError,
     MoELayer,
     clear_device_status,

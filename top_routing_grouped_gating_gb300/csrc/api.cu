@@ -97,7 +97,7 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 
 // Workspace of moe_forward, in call order.
 struct ForwardLayout {
-  size_t router, ids, w, routing, counts, offsets, eri, sri, done, xe, h, y2, total;
+  size_t router, ids, w, routing, counts, offsets, eri, sri, done, counter, xe, h, y2, total;
 };
 
 ForwardLayout forward_layout(int T, int H, int E, int k, int I) {
@@ -119,6 +119,7 @@ ForwardLayout forward_layout(int T, int H, int E, int k, int I) {
   L.eri = take(P * sizeof(int32_t));
   L.sri = take(P * sizeof(int32_t));
   L.done = take((size_t)E * sizeof(int32_t));
+  L.counter = take(sizeof(int32_t));
   L.xe = take(P * H * 2);
   L.h = take(P * I * 2);
   L.y2 = take(P * H * 2);
@@ -218,10 +219,10 @@ moe_status moe_router_logits(const moe_bf16* x, const float* Wg, int T, int H, i
         (reinterpret_cast<uintptr_t>(ws) & 255u))
       return MOE_ERR_WORKSPACE;
     float* partial = static_cast<float*>(ws);
-    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, partial, stream));
+    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, partial, nullptr, stream));
     MOE_CUDA(moe::launch_router_reduce(partial, rp.splits, T, E, logits, stream));
   } else {
-    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, logits, stream));
+    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, logits, nullptr, stream));
   }
   return MOE_OK;
 }
@@ -233,8 +234,8 @@ moe_status moe_gating_topk_softmax(const float* logits, int T, int E, int k, int
   if (T < 1 || E < 1 || E > 256 || k < 1 || k > E || k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   DeviceFacts* d = nullptr;
   MOE_TRY(current_device(&d));
-  MOE_CUDA(moe::launch_gating(logits, 1, T, E, k, renormalize, topk_ids, topk_w, d->status,
-                              stream));
+  MOE_CUDA(moe::launch_gating(logits, 1, T, E, k, renormalize, topk_ids, topk_w, nullptr,
+                              d->status, stream));
   return MOE_OK;
 }
 
@@ -385,16 +386,30 @@ moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_o
   uint16_t* h = at<uint16_t>(ws, L.h);
   uint16_t* y2 = at<uint16_t>(ws, L.y2);
 
+  // Small P: init_routing runs inside the gating launch (its last CTA routes all
+  // pairs); the counter it uses is zeroed by the router launch, or here.
+  const bool fused_routing = moe::routing_plan(P, E).single_cta;
+  moe::GatingRouting fr{};
+  fr.counter = at<int>(ws, L.counter);
+  fr.counts = at<int32_t>(ws, L.counts);
+  fr.offsets = offsets;
+  fr.eri = eri;
+  fr.sri = sri;
+  fr.done = done;
+  const moe::GatingRouting* fuse = fused_routing ? &fr : nullptr;
   if (logits_override) {
-    MOE_CUDA(moe::launch_gating(logits_override, 1, T, E, k, 1, ids, w, d->status, stream));
+    if (fused_routing) MOE_CUDA(cudaMemsetAsync(fr.counter, 0, sizeof(int), stream));
+    MOE_CUDA(moe::launch_gating(logits_override, 1, T, E, k, 1, ids, w, fuse, d->status, stream));
   } else {
     const moe::RouterPlan rp = moe::router_plan(T, H, E);
     float* part = at<float>(ws, L.router);
-    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, part, stream));
-    MOE_CUDA(moe::launch_gating(part, rp.splits, T, E, k, 1, ids, w, d->status, stream));
+    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, part, fused_routing ? fr.counter : nullptr,
+                                stream));
+    MOE_CUDA(moe::launch_gating(part, rp.splits, T, E, k, 1, ids, w, fuse, d->status, stream));
   }
-  MOE_CUDA(moe::launch_routing(ids, P, E, at<int32_t>(ws, L.counts), offsets, eri, sri,
-                               at<void>(ws, L.routing), done, d->status, stream));
+  if (!fused_routing)
+    MOE_CUDA(moe::launch_routing(ids, P, E, fr.counts, offsets, eri, sri,
+                                 at<void>(ws, L.routing), done, d->status, stream));
   MOE_CUDA(moe::launch_gather_rows(x, sri, offsets, E, P, H, k, xe, stream));
   moe::GemmPhase g1{}, g2{};
   g1.A_weights = w13_packed;

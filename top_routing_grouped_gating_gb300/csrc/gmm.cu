@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = args.E;
+  pdl_trigger();  // the finalize launch may start and wait for this grid to finish
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {

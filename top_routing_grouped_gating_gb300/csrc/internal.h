@@ -11,19 +11,33 @@ namespace moe {
 
 // ---- router / gating (router_gating.cu)
 struct RouterPlan {
+  bool small;      // decode-size tiles (32 tokens x 32 experts x 128 rows of H)
   int splits;      // split-K factor over H
   int t_tiles;     // ceil(T / 32)
-  int e_tiles;     // ceil(E / 128)
+  int e_tiles;     // expert tiles
 };
 RouterPlan router_plan(int T, int H, int E);
-// partial[s][T][E] when splits > 1, else writes out directly.
+// partial[s][T][E] when splits > 1, else writes out directly.  zero_word (may be
+// null) is set to 0 by the launch (the fused gating/routing counter).
 cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
-                          const RouterPlan& plan, float* partial_or_out, cudaStream_t s);
+                          const RouterPlan& plan, float* partial_or_out, int* zero_word,
+                          cudaStream_t s);
 cudaError_t launch_router_reduce(const float* partial, int splits, int T, int E, float* logits,
                                  cudaStream_t s);
+// Optional init_routing fused into the gating launch (one-CTA routing, P <= 4096):
+// the last gating CTA routes all pairs.  counter must be 0 at launch.
+struct GatingRouting {
+  int* counter;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* eri;
+  int32_t* sri;
+  int* done;     // E ints cleared for the grouped GEMM's dependency
+};
 // Gating reads sum_{s<splits} src[s*T*E + t*E + e] (splits == 1: plain logits).
 cudaError_t launch_gating(const float* src, int splits, int T, int E, int k, int renormalize,
-                          int32_t* ids, float* w, int* status, cudaStream_t s);
+                          int32_t* ids, float* w, const GatingRouting* fuse, int* status,
+                          cudaStream_t s);
 
 // ---- routing (routing.cu)
 struct RoutingPlan {

@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "routing_dev.cuh"
 
 namespace moe {
 
@@ -27,8 +28,13 @@ constexpr int kRK = 32;    // H rows per smem step
 __global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict__ x,
                                                      const float* __restrict__ Wg, int T, int H,
                                                      int E, int h_per_split,
-                                                     float* __restrict__ out) {
+                                                     float* __restrict__ out, int* zero_word) {
   __shared__ float xs[kRT][kRK + 1];
+  pdl_wait();
+  pdl_trigger();
+  if (zero_word != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
+      threadIdx.x == 0)
+    *zero_word = 0;
   __shared__ float ws[kRK][kRE];
   const int tid = threadIdx.x;
   const int tx = tid & 31;          // experts e0 + tx + 32*i
@@ -91,6 +97,69 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict_
   }
 }
 
+// Decode-size router: tiles of 32 tokens x 32 experts over a 128-row slice of H,
+// the whole slice loaded into shared memory before any arithmetic, so each CTA
+// pays one round of load latency.  Partial sums go to partial[split][T][E].
+constexpr int kSmallRows = 128;
+constexpr int kSmallExp = 32;
+
+__global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __restrict__ x,
+                                                           const float* __restrict__ Wg, int T,
+                                                           int H, int E,
+                                                           float* __restrict__ partial,
+                                                           int* zero_word) {
+  __shared__ float ws[kSmallRows][kSmallExp];
+  pdl_wait();
+  pdl_trigger();
+  if (zero_word != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
+      threadIdx.x == 0)
+    *zero_word = 0;
+  __shared__ float xs[kRT][kSmallRows + 1];
+  const int tid = threadIdx.x;
+  const int tx = tid & 31;          // expert e0 + tx
+  const int ty = tid >> 5;          // tokens t0 + 4*ty + j
+  const int e0 = blockIdx.x * kSmallExp;
+  const int split = blockIdx.y;
+  const int t0 = blockIdx.z * kRT;
+  const int hb = split * kSmallRows;
+#pragma unroll
+  for (int r = 0; r < (kSmallRows * kSmallExp) / 256; ++r) {
+    const int idx = tid + 256 * r;
+    const int hh = idx >> 5, ee = idx & 31;
+    ws[hh][ee] = (e0 + ee < E) ? Wg[(size_t)(hb + hh) * E + e0 + ee] : 0.f;
+  }
+#pragma unroll
+  for (int r = 0; r < (kRT * kSmallRows) / (256 * 8); ++r) {
+    const int idx = tid + 256 * r;
+    const int tt = idx >> 4, h8 = (idx & 15) * 8;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (t0 + tt < T) raw = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + hb + h8);
+    const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      xs[tt][h8 + 2 * q] = bf16_lo(u[q]);
+      xs[tt][h8 + 2 * q + 1] = bf16_hi(u[q]);
+    }
+  }
+  __syncthreads();
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int h = 0; h < kSmallRows; ++h) {
+    const float wv = ws[h][tx];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = fmaf(xs[4 * ty + j][h], wv, acc[j]);
+  }
+  const int e = e0 + tx;
+  if (e < E) {
+    float* dst = partial + (size_t)split * T * E;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = t0 + 4 * ty + j;
+      if (t < T) dst[(size_t)t * E + e] = acc[j];
+    }
+  }
+}
+
 __global__ void router_reduce_kernel(const float* __restrict__ partial, int splits, size_t n,
                                      float* __restrict__ out) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
@@ -106,25 +175,21 @@ __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-__global__ void __launch_bounds__(256) gating_kernel(const float* __restrict__ src, int splits,
-                                                     int T, int E, int k, int renormalize,
-                                                     int32_t* __restrict__ ids,
-                                                     float* __restrict__ w) {
-  const int lane = threadIdx.x & 31;
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (t >= T) return;
+__device__ __forceinline__ void gating_token(const float* __restrict__ src, int splits, int t,
+                                             int T, int E, int k, int renormalize,
+                                             int32_t* __restrict__ ids, float* __restrict__ w,
+                                             int lane) {
   const size_t n = (size_t)T * E;
   float v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      float s = src[(size_t)t * E + e];
-      for (int p = 1; p < splits; ++p) s += src[(size_t)p * n + (size_t)t * E + e];
-      v[i] = s;
-    } else {
-      v[i] = -INFINITY;
-    }
+  for (int i = 0; i < 8; ++i) v[i] = (lane + 32 * i < E) ? 0.f : -INFINITY;
+  // sum the split-K partials in split order; independent loads kept in flight
+#pragma unroll 4
+  for (int p = 0; p < splits; ++p) {
+    const float* row = src + (size_t)p * n + (size_t)t * E;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < E) v[i] += __ldcg(row + lane + 32 * i);
   }
   uint32_t taken = 0;
   float my_v = -INFINITY;
@@ -174,11 +239,44 @@ __global__ void __launch_bounds__(256) gating_kernel(const float* __restrict__ s
   }
 }
 
+__global__ void __launch_bounds__(256) gating_kernel(const float* __restrict__ src, int splits,
+                                                     int T, int E, int k, int renormalize,
+                                                     int32_t* __restrict__ ids,
+                                                     float* __restrict__ w, GatingRouting fuse,
+                                                     int* status) {
+  __shared__ RoutingSmem<8> rsm;
+  __shared__ int s_last;
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t < T) {
+    gating_token(src, splits, t, T, E, k, renormalize, ids, w, lane);
+  }
+  if (fuse.counter == nullptr) return;
+  // Fused init_routing: the last CTA to finish its tokens routes all P pairs.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(fuse.counter, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  routing_single_cta(ids, T * k, E, fuse.counts, fuse.offsets, fuse.eri, fuse.sri, fuse.done,
+                     status, rsm);
+  if (threadIdx.x == 0) *fuse.counter = 0;  // ready for the next call
+}
+
 }  // namespace
 
 RouterPlan router_plan(int T, int H, int E) {
   RouterPlan p;
   p.t_tiles = (T + kRT - 1) / kRT;
+  p.small = (p.t_tiles <= 2 && H % kSmallRows == 0);
+  if (p.small) {
+    p.e_tiles = (E + kSmallExp - 1) / kSmallExp;
+    p.splits = H / kSmallRows;
+    return p;
+  }
   p.e_tiles = (E + kRE - 1) / kRE;
   const int tiles = p.t_tiles * p.e_tiles;
   int s = 1;
@@ -189,9 +287,15 @@ RouterPlan router_plan(int T, int H, int E) {
 }
 
 cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
-                          const RouterPlan& plan, float* out, cudaStream_t s) {
-  dim3 grid(plan.t_tiles, plan.e_tiles, plan.splits);
-  router_kernel<<<grid, 256, 0, s>>>(x, Wg, T, H, E, H / plan.splits, out);
+                          const RouterPlan& plan, float* out, int* zero_word, cudaStream_t s) {
+  if (plan.small) {
+    dim3 grid(plan.e_tiles, plan.splits, plan.t_tiles);
+    return launch_pdl(router_small_kernel, grid, dim3(256), 0, s, x, Wg, T, H, E, out, zero_word);
+  } else {
+    dim3 grid(plan.t_tiles, plan.e_tiles, plan.splits);
+    return launch_pdl(router_kernel, grid, dim3(256), 0, s, x, Wg, T, H, E, H / plan.splits, out,
+                      zero_word);
+  }
   return cudaGetLastError();
 }
 
@@ -204,11 +308,13 @@ cudaError_t launch_router_reduce(const float* partial, int splits, int T, int E,
 }
 
 cudaError_t launch_gating(const float* src, int splits, int T, int E, int k, int renormalize,
-                          int32_t* ids, float* w, int* status, cudaStream_t s) {
-  (void)status;
+                          int32_t* ids, float* w, const GatingRouting* fuse, int* status,
+                          cudaStream_t s) {
   const int blocks = (T + 7) / 8;
-  gating_kernel<<<blocks, 256, 0, s>>>(src, splits, T, E, k, renormalize, ids, w);
-  return cudaGetLastError();
+  GatingRouting f{};
+  if (fuse != nullptr) f = *fuse;
+  return launch_pdl(gating_kernel, dim3(blocks), dim3(256), 0, s, src, splits, T, E, k,
+                    renormalize, ids, w, f, status);
 }
 
 }  // namespace moe

@@ -14,6 +14,7 @@
 // per-chunk histogram kernel, a one-CTA scan and a per-chunk scatter kernel.
 #include "common.cuh"
 #include "internal.h"
+#include "routing_dev.cuh"
 
 namespace moe {
 
@@ -22,107 +23,13 @@ namespace {
 constexpr int kRouteThreads = 1024;
 constexpr int kSingleCtaMaxPairs = 4096;
 constexpr int kChunkPairs = 2048;
-constexpr int kMaxExperts = 256;
-
-// Exclusive scan of one value per thread for threads [0, 256); every thread of
-// the block must call it.  s_tmp: 8 ints.  Returns the exclusive prefix; *total
-// receives the sum of all 256 values.
-__device__ int block_excl_scan_256(int v, int* s_tmp, int* total) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int x = tid < kMaxExperts ? v : 0;
-  int inc = x;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, inc, off);
-    if (lane >= off) inc += y;
-  }
-  if (warp < 8 && lane == 31) s_tmp[warp] = inc;
-  __syncthreads();
-  int pre = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    const int c = s_tmp[w];
-    if (w < warp) pre += c;
-    tot += c;
-  }
-  __syncthreads();
-  *total = tot;
-  return pre + inc - x;
-}
-
-// Scatter pairs [j_begin, j_end) in order.  s_base[e] = first free row of e for
-// this range (advanced as rounds complete); s_wcnt = (warps x E) zeros.
-__device__ void scatter_range(const int32_t* __restrict__ ids, int j_begin, int j_end, int E,
-                              int* s_base, int* s_wcnt, int32_t* __restrict__ eri,
-                              int32_t* __restrict__ sri) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
-  for (int j0 = j_begin; j0 < j_end; j0 += blockDim.x) {
-    const int j = j0 + tid;
-    int e = -1;                       // -1: no pair in this slot
-    if (j < j_end) {
-      e = ids[j];
-      if (e < 0 || e >= E) e = -2;    // -2: invalid id, pair dropped
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (e >= 0 && rank == 0) s_wcnt[warp * E + e] = __popc(peers);
-    __syncthreads();
-    if (e >= 0) {
-      int before = 0;
-      for (int w = 0; w < warp; ++w) before += s_wcnt[w * E + e];
-      const int p = s_base[e] + before + rank;
-      eri[j] = p;
-      sri[p] = j;
-    } else if (e == -2) {
-      eri[j] = -1;
-    }
-    __syncthreads();
-    for (int x = tid; x < E; x += blockDim.x) {
-      int s = 0;
-      for (int w = 0; w < nwarps; ++w) {
-        s += s_wcnt[w * E + x];
-        s_wcnt[w * E + x] = 0;
-      }
-      s_base[x] += s;
-    }
-    __syncthreads();
-  }
-}
 
 __global__ void __launch_bounds__(kRouteThreads) routing_single_cta_kernel(
     const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ eri, int32_t* __restrict__ sri,
     int* __restrict__ zero_counter, int* status) {
-  __shared__ int s_hist[kMaxExperts];
-  __shared__ int s_base[kMaxExperts];
-  __shared__ int s_tmp[8];
-  __shared__ int s_wcnt[(kRouteThreads / 32) * kMaxExperts];
-  const int tid = threadIdx.x;
-  for (int i = tid; i < kMaxExperts; i += blockDim.x) s_hist[i] = 0;
-  for (int i = tid; i < (kRouteThreads / 32) * E; i += blockDim.x) s_wcnt[i] = 0;
-  if (zero_counter != nullptr)
-    for (int i = tid; i < E; i += blockDim.x) zero_counter[i] = 0;
-  __syncthreads();
-  bool bad = false;
-  for (int j = tid; j < P; j += blockDim.x) {
-    const int e = ids[j];
-    if (e >= 0 && e < E) atomicAdd(&s_hist[e], 1);
-    else bad = true;
-  }
-  if (bad) flag_status(status, MOE_DEV_BAD_EXPERT_ID);
-  __syncthreads();
-  int total = 0;
-  const int c = (tid < E) ? s_hist[tid] : 0;
-  const int off = block_excl_scan_256(c, s_tmp, &total);
-  if (tid < E) {
-    s_base[tid] = off;
-    offsets[tid] = off;
-    if (counts != nullptr) counts[tid] = c;
-  }
-  if (tid == 0) offsets[E] = total;
-  __syncthreads();
-  scatter_range(ids, 0, P, E, s_base, s_wcnt, eri, sri);
+  __shared__ RoutingSmem<kRouteThreads / 32> sm;
+  routing_single_cta(ids, P, E, counts, offsets, eri, sri, zero_counter, status, sm);
 }
 
 __global__ void __launch_bounds__(kRouteThreads) routing_hist_kernel(
@@ -191,6 +98,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ offsets,
                                                           int E, int P, int H, int k,
                                                           uint16_t* __restrict__ xe) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (p >= P || p >= offsets[E]) return;
@@ -233,6 +142,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
                                                        int H, uint16_t* __restrict__ out) {
   __shared__ int s_row[32];
   __shared__ float s_w[32];
+  pdl_wait();
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
     s_row[threadIdx.x] = eri[(size_t)t * k + threadIdx.x];
@@ -301,8 +211,8 @@ cudaError_t launch_routing(const int32_t* ids, int P, int E, int32_t* counts, in
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sri, const int32_t* offsets,
                                int E, int P, int H, int k, uint16_t* xe, cudaStream_t s) {
   const int blocks = (P + 7) / 8;
-  gather_rows_kernel<<<blocks, 256, 0, s>>>(x, sri, offsets, E, P, H, k, xe);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, x, sri, offsets, E, P, H, k,
+                    xe);
 }
 
 cudaError_t launch_expert_tokens(const int32_t* ids, int P, int E, int32_t* counts,
@@ -314,8 +224,7 @@ cudaError_t launch_expert_tokens(const int32_t* ids, int P, int E, int32_t* coun
 cudaError_t launch_finalize(const uint16_t* y2, const float* w, const int32_t* eri, int T, int k,
                             int H, uint16_t* out, cudaStream_t s) {
   const int threads = (H / 8) >= 256 ? 256 : ((H / 8 + 31) / 32) * 32;
-  finalize_kernel<<<T, threads, 0, s>>>(y2, w, eri, k, H, out);
-  return cudaGetLastError();
+  return launch_pdl(finalize_kernel, dim3(T), dim3(threads), 0, s, y2, w, eri, k, H, out);
 }
 
 }  // namespace moe
