@@ -195,6 +195,58 @@ MOE_API moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* 
                        int I, moe_bf16* out, int32_t* topk_ids_out, float* topk_w_out, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
 
+/* ------------------------------------------------------------------ MXFP8 --
+ * §融合RMSNorm MX量化: residual add, RMSNorm and MXFP8 dynamic quantisation in one
+ * pass.  MX format (OCP Microscaling v1.0; the page names only "MXFP8", round mode
+ * "rint" and float8_e4m3fn): blocks of 32 consecutive elements share an E8M0 scale
+ * 2^X with X = floor(log2(max|v|)) - 8 clamped to [-127,127] (all-zero block:
+ * X = -127); elements are e4m3(v / 2^X), nearest-even, saturating at +-448.
+ * Scale byte = X + 127.
+ *
+ * moe_add_rmsnorm_mxquant:  s = x + r (fp32);  residual_out = bf16(s);
+ *   y = s * rsqrt(mean(s^2) + eps) * w (fp32);  y32_out = y;  q, scale = MX(y) along H.
+ *   x, r (T,H) bf16 (r may be NULL: no residual, the page's first-layer variant);
+ *   w (H) bf16; residual_out (T,H) bf16 or NULL; y32_out (T,H) fp32 or NULL;
+ *   q (T,H) e4m3 bytes; scale (T,H/32) bytes.  H % 256 == 0.
+ */
+MOE_API moe_status moe_add_rmsnorm_mxquant(const moe_bf16* x, const moe_bf16* r, const moe_bf16* w,
+                                           float eps, int T, int H, moe_bf16* residual_out,
+                                           float* y32_out, uint8_t* q, uint8_t* scale,
+                                           moe_stream_t stream);
+
+/* Dynamic MX quantisation of an fp32 (rows, n) matrix along its rows (the page's
+ * npu_dynamic_mx_quant, §计算分解 AllGather方案).  n % 32 == 0; q (rows,n) bytes;
+ * scale (rows, n/32) bytes.  y 16-byte aligned. */
+MOE_API moe_status moe_mx_quantize(const float* y, int rows, int n, uint8_t* q, uint8_t* scale,
+                                   moe_stream_t stream);
+
+/* MX pre-quantisation of the expert weights along their reduction axis (H for w13,
+ * I for down), load-time.  Codes are K-major in the same row order as
+ * moe_pack_weights; scales are stored as 512-byte atoms per (expert, 128-row
+ * block, 128-element K step): byte (r%32)*16 + (r/32)*4 + b holds the scale of row r,
+ * K block b.  Requires H % 128 == 0 and I % 128 == 0.
+ *   which: 0 w13 codes (E*2I*H bytes), 1 w13 scales (E*2I*H/32), 2 down codes
+ *   (E*H*I), 3 down scales (E*H*I/32). */
+MOE_API size_t moe_packed_weight_bytes_mx(int E, int H, int I, int which);
+MOE_API moe_status moe_pack_weights_mx(const moe_bf16* w13, const moe_bf16* down, int E, int H,
+                                       int I, void* w13_q, void* w13_sf, void* down_q,
+                                       void* down_sf, moe_stream_t stream);
+
+/* The MXFP8 layer in one call: add+RMSNorm+MX quant -> router on the fp32 normalised
+ * activations (§融合RMSNorm Cast) -> gating -> init_routing -> block-scaled grouped
+ * GEMM over w13 + SwiGLU, h MX-quantised along I -> block-scaled grouped GEMM over
+ * down -> finalize.  Arguments as moe_forward plus r, norm_w, eps and residual_out
+ * (T,H bf16 or NULL), with the packed MX weights.  H % 256 == 0, I % 128 == 0.
+ *   ws >= moe_forward_mx_workspace_size(T,H,E,k,I) bytes. */
+MOE_API size_t moe_forward_mx_workspace_size(int T, int H, int E, int k, int I);
+MOE_API moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w,
+                                  float eps, const float* Wg, const float* logits_override,
+                                  const void* w13_q, const void* w13_sf, const void* down_q,
+                                  const void* down_sf, int T, int H, int E, int k, int I,
+                                  moe_bf16* out, moe_bf16* residual_out, int32_t* topk_ids_out,
+                                  float* topk_w_out, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
 /* ------------------------------------------------ allocation-free routing --
  * No counterpart in the pages: an extra entry point for callers that cannot
  * allocate device memory -- code living inside a host framework that owns all

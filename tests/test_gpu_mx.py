@@ -1,0 +1,153 @@
+"""MXFP8 path on the GPU against the CPU oracle (via the C ABI).
+
+Bit-exact where both sides quantise identical inputs (the standalone quantiser on
+seeded fp32 data, the weight pre-quantisation of bf16 weights).  Where the GPU
+quantises its own fp32 RMSNorm output, the codes are compared through their
+dequantised values, since the oracle's fp64 normalisation can sit on the other
+side of a rounding boundary.  The layer output must stay within relative
+Frobenius error 4e-2 of the oracle run on dequantised inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import top_routing_grouped_gating_gb300 as moe
+from oracle import moe_oracle as O
+from tests._helpers import REL_FRO_MX, LazyExperts, rel_fro, to_np
+from top_routing_grouped_gating_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def tricky_fp32(rows, n, seed):
+    """Seeded fp32 data with MX edge cases: zero blocks, powers of two, e4m3
+    rounding midpoints, saturating values, tiny and negative-zero entries."""
+    rng = np.random.default_rng(seed)
+    y = rng.standard_normal((rows, n)) * np.exp2(rng.integers(-30, 30, size=(rows, 1)))
+    yb = y.reshape(rows, n // 32, 32)
+    yb[0, 0] = 0.0
+    yb[0, 1] = -0.0
+    yb[1, 0] = np.exp2(np.arange(32) - 16.0)
+    codes = np.arange(1, 126)
+    mids = (O.e4m3_decode(codes) + O.e4m3_decode(codes + 1)) / 2
+    yb[2, :, :] = rng.choice(mids, size=yb[2].shape) * rng.choice([-1, 1], size=yb[2].shape)
+    yb[2, :, 0] = 448.0 * 1.1           # block max: saturating neighbours
+    yb[3, 0, :] = 500.0                 # whole block saturates
+    yb[3, 1, :] = 1e-42                 # fp32 subnormals
+    yb[3, 1, 3] = -0.0
+    return y.reshape(rows, n).astype(np.float32)
+
+
+def test_mx_quantize_bit_exact(cuda_dev):
+    y = tricky_fp32(64, 512, seed=1)
+    q, sc = moe.mx_quantize(torch.from_numpy(y).to(cuda_dev))
+    rq, rsc = O.mx_quantize(y.astype(np.float64))
+    np.testing.assert_array_equal(to_np(sc), rsc)
+    np.testing.assert_array_equal(to_np(q), rq)
+
+
+def test_add_rmsnorm_mxquant(cuda_dev):
+    cfg = W.with_shape(W.CONFIGS["mxfp8_prefill"], T=64)
+    inp = W.make_inputs(cfg, weights=True, device="cpu")
+    x, r, w = inp["x"], inp["r"], inp["norm_w"]
+    res, y32, q, sc = moe.add_rmsnorm_mxquant(x.to(cuda_dev), r.to(cuda_dev), w.to(cuda_dev), cfg.eps)
+    s, y = O.add_rmsnorm(to_np(x), to_np(r), to_np(w), cfg.eps)
+    ref_res = torch.from_numpy(s).to(torch.bfloat16)
+    assert torch.equal(res.cpu().view(torch.int16), ref_res.view(torch.int16))
+    # fp32 normalisation: a few roundings (sum of squares over H, rsqrt, two products)
+    np.testing.assert_allclose(to_np(y32), y, rtol=2e-5, atol=1e-6)
+    rq, rsc = O.mx_quantize(y)
+    deq = O.mx_dequantize(to_np(q).astype(np.uint8), to_np(sc).astype(np.uint8))
+    rdeq = O.mx_dequantize(rq, rsc)
+    diff = deq != rdeq
+    assert diff.mean() < 2e-3
+    # any disagreement is one e4m3 step of that block (a rounding-boundary straddle)
+    step = np.exp2(np.repeat(to_np(sc).astype(np.float64), 32, axis=1) - 127) * 2.0 ** -2
+    assert np.all(np.abs(deq - rdeq)[diff] <= np.maximum(np.abs(rdeq[diff]) * 2.0 ** -3, step[diff]))
+    # residual-free variant
+    _, y0, _, _ = moe.add_rmsnorm_mxquant(x.to(cuda_dev), None, w.to(cuda_dev), cfg.eps)
+    _, y0r = O.add_rmsnorm(to_np(x), None, to_np(w), cfg.eps)
+    np.testing.assert_allclose(to_np(y0), y0r, rtol=2e-5, atol=1e-6)
+
+
+def _unpack_w13(q, sf, E, H, I):
+    """Packed MX w13 -> per expert (codes (H, 2I) logical, scales (H/32, 2I))."""
+    q = q.reshape(E, 2 * I, H)
+    sf = sf.reshape(E, 2 * I // 128, H // 128, 512)
+    r = np.arange(2 * I)
+    blk, wi = r // 128, r % 128
+    col = np.where(wi < 64, blk * 64 + wi, I + blk * 64 + (wi - 64))
+    codes = np.empty((E, H, 2 * I), np.uint8)
+    scales = np.empty((E, H // 32, 2 * I), np.uint8)
+    b = np.arange(H // 32)
+    for e in range(E):
+        codes[e][:, col] = q[e].T
+        off = (r[:, None] % 32) * 16 + ((r[:, None] % 128) // 32) * 4 + (b[None, :] % 4)
+        scales[e][:, col] = sf[e][r[:, None] // 128, b[None, :] // 4, off].T
+    return codes, scales
+
+
+def test_pack_weights_mx_bit_exact(cuda_dev):
+    E, H, I = 4, 256, 128
+    g = torch.Generator().manual_seed(7)
+    w13 = (torch.randn(E, H, 2 * I, generator=g) * 0.05).to(torch.bfloat16)
+    down = (torch.randn(E, I, H, generator=g) * 0.05).to(torch.bfloat16)
+    w13[0, :32, 5] = 0                       # an all-zero block
+    w13_q, w13_sf, down_q, down_sf = moe.pack_weights_mx(w13.to(cuda_dev), down.to(cuda_dev))
+    codes, scales = _unpack_w13(to_np(w13_q), to_np(w13_sf), E, H, I)
+    for e in range(E):
+        rq, rsc = O.mx_quantize(to_np(w13[e]).astype(np.float64).T)   # along H, per column
+        np.testing.assert_array_equal(codes[e].T, rq)
+        np.testing.assert_array_equal(scales[e].T, rsc)
+    dq = to_np(down_q).reshape(E, H, I)
+    dsf = to_np(down_sf).reshape(E, H // 128, I // 128, 512)
+    n = np.arange(H)[:, None]
+    b = np.arange(I // 32)[None, :]
+    for e in range(E):
+        rq, rsc = O.mx_quantize(to_np(down[e]).astype(np.float64).T)  # along I, per column n
+        np.testing.assert_array_equal(dq[e], rq)
+        got_sc = dsf[e][n // 128, b // 4, (n % 32) * 16 + ((n % 128) // 32) * 4 + b % 4]
+        np.testing.assert_array_equal(got_sc, rsc)
+
+
+def _mx_layer(cfg, device="cuda"):
+    inp = W.make_inputs(cfg, device=device)
+    layer = moe.MoELayerMX(inp["Wg"], inp["w13"], inp["down"], inp["norm_w"], cfg.k, cfg.eps)
+    return inp, layer
+
+
+def _check_mx_forward(cfg, inp, layer, sample=None):
+    x, r = inp["x"], inp["r"]
+    xn, rn, wn = to_np(x), to_np(r), to_np(inp["norm_w"])
+    _, y = O.add_rmsnorm(xn, rn, wn, cfg.eps)
+    lg32 = O.router_logits_f32(y, to_np(inp["Wg"]))
+    out, res, ids, w = layer(x, r, logits_override=torch.from_numpy(lg32).to(x.device))
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 0
+    r_ids, r_w = O.gating_topk_softmax(lg32, cfg.k)
+    np.testing.assert_array_equal(to_np(ids), r_ids)
+    rows = np.arange(cfg.T) if sample is None else sample
+    ref = O.moe_forward_mx(xn[rows], rn[rows], wn, cfg.eps, None, LazyExperts(inp["w13"]),
+                           LazyExperts(inp["down"]), cfg.k, logits32=lg32[rows])
+    got = to_np(out)[rows]
+    assert np.all(np.isfinite(got))
+    rf = rel_fro(got, ref["out"])
+    assert rf <= REL_FRO_MX, f"relative Frobenius error {rf:.3e}"
+    return rf
+
+
+@pytest.mark.parametrize("T,E,k,H,I", [(64, 8, 2, 256, 128), (300, 4, 2, 256, 256), (1, 8, 8, 512, 128)])
+def test_forward_mx_small(cuda_dev, T, E, k, H, I):
+    cfg = W.with_shape(W.CONFIGS["mxfp8_prefill"], T=T, E=E, k=k, H=H, I=I)
+    inp, layer = _mx_layer(cfg)
+    _check_mx_forward(cfg, inp, layer)
+
+
+def test_forward_mx_full_size_sampled(cuda_dev):
+    cfg = W.CONFIGS["mxfp8_prefill"]
+    inp, layer = _mx_layer(cfg)
+    sample = np.array([0, 1777, cfg.T - 1])
+    _check_mx_forward(cfg, inp, layer, sample=sample)
+    a = layer(inp["x"], inp["r"])[0].clone()
+    b = layer(inp["x"], inp["r"])[0]
+    assert torch.equal(a, b)

@@ -11,6 +11,10 @@ from ._binding import (  # noqa: F401
     GraphedMoELayer,
     MoEError,
     MoELayer,
+    MoELayerMX,
+    add_rmsnorm_mxquant,
+    mx_quantize,
+    pack_weights_mx,
     clear_device_status,
     compute_expert_tokens,
     exported_symbols,

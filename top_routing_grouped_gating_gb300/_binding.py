@@ -43,6 +43,13 @@ _SIGS = {
     "moe_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
                              _vp, _vp, _c_size, _vp]),
     "moe_set_gemm_events": (_c_int, [_vp, _vp]),
+    "moe_add_rmsnorm_mxquant": (_c_int, [_vp, _vp, _vp, _c_float, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp]),
+    "moe_mx_quantize": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_packed_weight_bytes_mx": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "moe_pack_weights_mx": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp]),
+    "moe_forward_mx_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "moe_forward_mx": (_c_int, [_vp, _vp, _vp, _c_float, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                _c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_init_routing_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp,
                                           _vp]),
 }
@@ -326,6 +333,108 @@ class MoELayer:
     def capture(self, T: int, logits_override: bool = False) -> "GraphedMoELayer":
         """A CUDA-graph replayable forward of this layer for T tokens."""
         return GraphedMoELayer(self, T, logits_override)
+
+
+# ----------------------------------------------------------------------- MXFP8
+
+
+def add_rmsnorm_mxquant(x: torch.Tensor, r: Optional[torch.Tensor], w: torch.Tensor, eps: float = 1e-6):
+    """Returns (residual bf16, y32 fp32, q uint8 e4m3 codes, scale uint8 E8M0)."""
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    if r is not None:
+        _need(r, "r", torch.bfloat16, dev)
+    _need(w, "w", torch.bfloat16, dev)
+    T, H = x.shape
+    with torch.cuda.device(dev):
+        res = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        y32 = torch.empty(T, H, dtype=torch.float32, device=dev)
+        q = torch.empty(T, H, dtype=torch.uint8, device=dev)
+        sc = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+        _check("moe_add_rmsnorm_mxquant",
+               lib().moe_add_rmsnorm_mxquant(_ptr(x), _ptr(r), _ptr(w), float(eps), T, H, _ptr(res), _ptr(y32),
+                                             _ptr(q), _ptr(sc), _stream(dev)))
+    return res, y32, q, sc
+
+
+def mx_quantize(y: torch.Tensor):
+    """MX-quantise an fp32 (rows, n) matrix along its rows -> (codes, scales)."""
+    _need(y, "y", torch.float32)
+    rows, n = y.shape
+    dev = y.device
+    with torch.cuda.device(dev):
+        q = torch.empty(rows, n, dtype=torch.uint8, device=dev)
+        sc = torch.empty(rows, n // 32, dtype=torch.uint8, device=dev)
+        _check("moe_mx_quantize", lib().moe_mx_quantize(_ptr(y), rows, n, _ptr(q), _ptr(sc), _stream(dev)))
+    return q, sc
+
+
+def pack_weights_mx(w13: torch.Tensor, down: torch.Tensor):
+    """Logical bf16 w13 (E,H,2I), down (E,I,H) -> (w13_q, w13_sf, down_q, down_sf) uint8 buffers."""
+    _need(w13, "w13", torch.bfloat16)
+    _need(down, "down", torch.bfloat16, w13.device)
+    E, H, I2 = w13.shape
+    I = I2 // 2
+    L = lib()
+    dev = w13.device
+    with torch.cuda.device(dev):
+        bufs = [torch.empty(L.moe_packed_weight_bytes_mx(E, H, I, i), dtype=torch.uint8, device=dev)
+                for i in range(4)]
+        _check("moe_pack_weights_mx", L.moe_pack_weights_mx(_ptr(w13), _ptr(down), E, H, I, *[_ptr(b) for b in bufs],
+                                                            _stream(dev)))
+    return tuple(bufs)
+
+
+class MoELayerMX:
+    """MXFP8 MoE layer: fused add+RMSNorm+MX quant in front, block-scaled grouped GEMMs."""
+
+    def __init__(self, Wg: torch.Tensor, w13: torch.Tensor, down: torch.Tensor, norm_w: torch.Tensor, k: int,
+                 eps: float = 1e-6):
+        self.E, self.H, I2 = w13.shape
+        self.I = I2 // 2
+        self.k = k
+        self.eps = float(eps)
+        self.Wg = Wg.contiguous()
+        self.norm_w = norm_w.contiguous()
+        self.w13_q, self.w13_sf, self.down_q, self.down_sf = pack_weights_mx(w13.contiguous(), down.contiguous())
+        self._ws = None
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = int(lib().moe_forward_mx_workspace_size(T, self.H, self.E, self.k, self.I))
+        if need == 0:
+            raise ValueError("unsupported MXFP8 layer shape")
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = _ws(need, self.Wg.device)
+        return self._ws
+
+    def __call__(self, x: torch.Tensor, r: Optional[torch.Tensor] = None,
+                 logits_override: Optional[torch.Tensor] = None, out=None, residual_out=None, topk_ids=None,
+                 topk_w=None):
+        """Returns (out, residual, topk_ids, topk_w)."""
+        _need(x, "x", torch.bfloat16)
+        dev = x.device
+        T, H = x.shape
+        if r is not None:
+            _need(r, "r", torch.bfloat16, dev)
+        if logits_override is not None:
+            _need(logits_override, "logits_override", torch.float32, dev)
+        ws = self.workspace(T)
+        with torch.cuda.device(dev):
+            if out is None:
+                out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            if residual_out is None:
+                residual_out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            if topk_ids is None:
+                topk_ids = torch.empty(T, self.k, dtype=torch.int32, device=dev)
+            if topk_w is None:
+                topk_w = torch.empty(T, self.k, dtype=torch.float32, device=dev)
+            _check("moe_forward_mx",
+                   lib().moe_forward_mx(_ptr(x), _ptr(r), _ptr(self.norm_w), self.eps, _ptr(self.Wg),
+                                        _ptr(logits_override), _ptr(self.w13_q), _ptr(self.w13_sf),
+                                        _ptr(self.down_q), _ptr(self.down_sf), T, H, self.E, self.k, self.I,
+                                        _ptr(out), _ptr(residual_out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws),
+                                        ws.numel(), _stream(dev)))
+        return out, residual_out, topk_ids, topk_w
 
 
 class GraphedMoELayer:

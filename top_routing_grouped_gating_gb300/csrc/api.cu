@@ -151,17 +151,24 @@ int* device_status_ptr() {
   return d->status;
 }
 
-bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
-                         uint32_t box_inner, uint32_t box_rows) {
+bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                    const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                    uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint64_t strides[1] = {inner * elem_bytes};
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(tm, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
+                         uint32_t box_inner, uint32_t box_rows) {
+  return encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, rows, box_inner,
+                        box_rows);
 }
 
 }  // namespace moe
@@ -430,6 +437,204 @@ moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_o
   MOE_CUDA(moe::launch_grouped_gemm(&g1, &g2, offsets, E, P, T, done, d->status, stream));
   if (t_gemm_ev_end) MOE_CUDA(cudaEventRecord(t_gemm_ev_end, stream));
   MOE_CUDA(moe::launch_finalize(y2, w, eri, T, k, H, out, stream));
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------- MXFP8 --
+moe_status moe_add_rmsnorm_mxquant(const moe_bf16* x, const moe_bf16* r, const moe_bf16* w,
+                                   float eps, int T, int H, moe_bf16* residual_out,
+                                   float* y32_out, uint8_t* q, uint8_t* scale,
+                                   moe_stream_t stream) {
+  if (!x || !w || !q || !scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (r && !aligned16(r)) || !aligned16(w) ||
+      (residual_out && !aligned16(residual_out)) || (y32_out && !aligned16(y32_out)) ||
+      (reinterpret_cast<uintptr_t>(q) & 7u))
+    return MOE_ERR_INVALID_ARG;
+  if (T < 1 || H < 256 || H % 256 != 0 || H > 32768) return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_add_rmsnorm_mxquant(x, r, w, eps, T, H, residual_out, y32_out, q, scale,
+                                           stream));
+  return MOE_OK;
+}
+
+moe_status moe_mx_quantize(const float* y, int rows, int n, uint8_t* q, uint8_t* scale,
+                           moe_stream_t stream) {
+  if (!y || !q || !scale || !aligned16(y) || (reinterpret_cast<uintptr_t>(q) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  if (rows < 1 || n < 32 || n % 32 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_mx_quantize(y, rows, n, q, scale, stream));
+  return MOE_OK;
+}
+
+size_t moe_packed_weight_bytes_mx(int E, int H, int I, int which) {
+  if (E < 1 || H < 1 || I < 1) return 0;
+  const size_t w = (size_t)E * H * I;
+  switch (which) {
+    case 0: return 2 * w;
+    case 1: return 2 * w / 32;
+    case 2: return w;
+    case 3: return w / 32;
+    default: return 0;
+  }
+}
+
+moe_status moe_pack_weights_mx(const moe_bf16* w13, const moe_bf16* down, int E, int H, int I,
+                               void* w13_q, void* w13_sf, void* down_q, void* down_sf,
+                               moe_stream_t stream) {
+  if ((w13 && (!w13_q || !w13_sf)) || (down && (!down_q || !down_sf))) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > 256 || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_pack_mx(w13, down, E, H, I, static_cast<uint8_t*>(w13_q),
+                               static_cast<uint8_t*>(w13_sf), static_cast<uint8_t*>(down_q),
+                               static_cast<uint8_t*>(down_sf), stream));
+  return MOE_OK;
+}
+
+namespace {
+
+struct ForwardMxLayout {
+  size_t y32, xq, xs, router, ids, w, routing, counts, offsets, eri, sri, done, counter, xe,
+      xe_sf, eri_pad, hq, h_sf, y2, total;
+  int pad_rows;
+};
+
+ForwardMxLayout forward_mx_layout(int T, int H, int E, int k, int I) {
+  ForwardMxLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  const size_t P = (size_t)T * k;
+  const size_t R = ((P + 127) / 128) * 128 + 128 * (size_t)E;  // rows after 128-row padding
+  L.pad_rows = (int)R;
+  const moe::RouterPlan rp = moe::router_plan(T, H, E);
+  L.y32 = take((size_t)T * H * 4);
+  L.xq = take((size_t)T * H);
+  L.xs = take((size_t)T * H / 32);
+  L.router = take((size_t)rp.splits * T * E * sizeof(float));
+  L.ids = take(P * 4);
+  L.w = take(P * 4);
+  L.routing = take(moe::routing_ws_bytes((int)P, E));
+  L.counts = take((size_t)E * 4);
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.eri = take(P * 4);
+  L.sri = take(P * 4);
+  L.done = take((size_t)E * 4);
+  L.counter = take(4);
+  L.xe = take(R * H);
+  L.xe_sf = take(R * H / 32);
+  L.eri_pad = take(P * 4);
+  L.hq = take(R * I);
+  L.h_sf = take(R * I / 32);
+  L.y2 = take(R * H * 2);
+  L.total = o;
+  return L;
+}
+
+moe_status check_mx_shape(int T, int H, int E, int k, int I) {
+  MOE_TRY(check_layer_shape(T, H, E, k, I));
+  if (H % 256 != 0 || I % 128 != 0 || H > 32768) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)T * k + 128LL * E + 128 >= (1LL << 31) / 4) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+}  // namespace
+
+size_t moe_forward_mx_workspace_size(int T, int H, int E, int k, int I) {
+  if (check_mx_shape(T, H, E, k, I) != MOE_OK) return 0;
+  return forward_mx_layout(T, H, E, k, I).total;
+}
+
+moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w, float eps,
+                          const float* Wg, const float* logits_override, const void* w13_q,
+                          const void* w13_sf, const void* down_q, const void* down_sf, int T,
+                          int H, int E, int k, int I, moe_bf16* out, moe_bf16* residual_out,
+                          int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  if (!x || !norm_w || !w13_q || !w13_sf || !down_q || !down_sf || !out)
+    return MOE_ERR_INVALID_ARG;
+  if (!logits_override && !Wg) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (r && !aligned16(r)) || !aligned16(norm_w) || !aligned16(w13_q) ||
+      !aligned16(w13_sf) || !aligned16(down_q) || !aligned16(down_sf) || !aligned16(out) ||
+      (residual_out && !aligned16(residual_out)))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_mx_shape(T, H, E, k, I));
+  const ForwardMxLayout L = forward_mx_layout(T, H, E, k, I);
+  if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_WORKSPACE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  const int P = T * k;
+  float* y32 = at<float>(ws, L.y32);
+  uint8_t* xq = at<uint8_t>(ws, L.xq);
+  uint8_t* xs = at<uint8_t>(ws, L.xs);
+  int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(ws, L.ids);
+  float* w = topk_w_out ? topk_w_out : at<float>(ws, L.w);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* eri = at<int32_t>(ws, L.eri);
+  int32_t* sri = at<int32_t>(ws, L.sri);
+  int* done = at<int>(ws, L.done);
+  MOE_CUDA(moe::launch_add_rmsnorm_mxquant(x, r, norm_w, eps, T, H, residual_out, y32, xq, xs,
+                                           stream));
+  const bool fused_routing = moe::routing_plan(P, E).single_cta;
+  moe::GatingRouting fr{};
+  fr.counter = at<int>(ws, L.counter);
+  fr.counts = at<int32_t>(ws, L.counts);
+  fr.offsets = offsets;
+  fr.eri = eri;
+  fr.sri = sri;
+  fr.done = done;
+  const moe::GatingRouting* fuse = fused_routing ? &fr : nullptr;
+  if (logits_override) {
+    if (fused_routing) MOE_CUDA(cudaMemsetAsync(fr.counter, 0, sizeof(int), stream));
+    MOE_CUDA(moe::launch_gating(logits_override, 1, T, E, k, 1, ids, w, fuse, d->status, stream));
+  } else {
+    const moe::RouterPlan rp = moe::router_plan(T, H, E);
+    float* part = at<float>(ws, L.router);
+    MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, E, rp, part,
+                                    fused_routing ? fr.counter : nullptr, stream));
+    MOE_CUDA(moe::launch_gating(part, rp.splits, T, E, k, 1, ids, w, fuse, d->status, stream));
+  }
+  if (!fused_routing)
+    MOE_CUDA(moe::launch_routing(ids, P, E, fr.counts, offsets, eri, sri,
+                                 at<void>(ws, L.routing), done, d->status, stream));
+  uint8_t* xe = at<uint8_t>(ws, L.xe);
+  uint8_t* xe_sf = at<uint8_t>(ws, L.xe_sf);
+  int32_t* eri_pad = at<int32_t>(ws, L.eri_pad);
+  MOE_CUDA(moe::launch_mx_expand(xq, xs, ids, eri, offsets, E, P, H, k, xe, xe_sf, eri_pad,
+                                 stream));
+  uint8_t* hq = at<uint8_t>(ws, L.hq);
+  uint8_t* h_sf = at<uint8_t>(ws, L.h_sf);
+  uint16_t* y2 = at<uint16_t>(ws, L.y2);
+  moe::GemmPhaseMx g1{}, g2{};
+  g1.A_q = w13_q;
+  g1.A_sf = static_cast<const uint8_t*>(w13_sf);
+  g1.B_q = xe;
+  g1.B_sf = xe_sf;
+  g1.out_q = hq;
+  g1.out_sf = h_sf;
+  g1.K = H;
+  g1.MW = 2 * I;
+  g1.n_out = I;
+  g2.A_q = down_q;
+  g2.A_sf = static_cast<const uint8_t*>(down_sf);
+  g2.B_q = hq;
+  g2.B_sf = h_sf;
+  g2.out_bf16 = y2;
+  g2.K = I;
+  g2.MW = H;
+  g2.n_out = H;
+  if (t_gemm_ev_begin) MOE_CUDA(cudaEventRecord(t_gemm_ev_begin, stream));
+  MOE_CUDA(moe::launch_grouped_gemm_mx(&g1, &g2, offsets, E, L.pad_rows, done, d->status, stream));
+  if (t_gemm_ev_end) MOE_CUDA(cudaEventRecord(t_gemm_ev_end, stream));
+  MOE_CUDA(moe::launch_finalize(y2, w, eri_pad, T, k, H, out, stream));
   return MOE_OK;
 }
 

@@ -117,6 +117,16 @@ MOE_DEVINL void tma_load_2d(void* smem_dst, const CUtensorMap* tm, uint64_t* bar
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
+MOE_DEVINL void bulk_load_1d(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                             uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 MOE_DEVINL void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -173,6 +183,49 @@ MOE_DEVINL uint64_t smem_desc_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1) << 46;                   // descriptor version (sm_100 family)
   d |= static_cast<uint64_t>(2) << 61;                   // swizzle mode: 128-byte
   return d;
+}
+
+// Shared-memory descriptor of a K-major tile without swizzle: 8-row x 16-byte core
+// matrices, `sbo` bytes apart along M/N (used for the 32 x 16-byte scale atoms).
+MOE_DEVINL uint64_t smem_desc_noswz(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Copy a 32-row x 128-bit shared-memory tile into TMEM columns [taddr, taddr+4),
+// replicated into all four 32-lane quarters (the scale-factor atom layout).
+MOE_DEVINL void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Block-scaled MMA: D (+)= (A . 2^SFA) x (B . 2^SFB)^T, A and B e4m3, scales E8M0
+// per 32 K-elements read from TMEM, fp32 accumulate.  K = 32 per instruction.
+MOE_DEVINL void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: A and B e4m3, both
+// K-major, E8M0 scales; sf ids pick the byte of each 32-bit scale word.
+__host__ __device__ constexpr uint32_t idesc_mxf8_f32(int M, int N, uint32_t sfa_id,
+                                                      uint32_t sfb_id) {
+  return (sfb_id << 4)                               // B scale-factor byte
+         | (0u << 7) | (0u << 10)                    // A, B format: e4m3
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scale format: E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)     // M / 16
+         | (sfa_id << 29);                           // A scale-factor byte
 }
 
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M x N.

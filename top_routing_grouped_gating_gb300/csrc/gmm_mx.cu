@@ -1,0 +1,542 @@
+// Block-scaled MXFP8 grouped GEMM (tcgen05.mma kind::mxf8f6f4, E8M0 scales per 32
+// K-elements in TMEM) for the MXFP8 expert MLPs of the page "基于Atlas A3、950训练/
+// 推理集群的Qwen3-MoE模型低时延推理性能优化实践" (§融合RMSNorm MX量化 feeds MXFP8
+// activations to the grouped matmul; §高性能专家计算; SwiGLU from §计算分解).
+//
+// Same orientation, unit order, warp roles and phase dependency as the bf16 grouped
+// GEMM (gmm.cu): D[128 weight rows][<=128 tokens] per unit, weights as the A
+// operand.  Differences:
+//  - operands are e4m3 bytes, so one 128-byte swizzle row holds 128 K-elements and
+//    a pipeline stage covers K = 128 = four MMAs of K = 32;
+//  - each stage also carries the 512-byte scale atoms of its A and B tiles (128
+//    rows x 4 blocks each, loaded with 1-D bulk copies); the MMA thread copies them
+//    into a per-stage TMEM slot with tcgen05.cp before the stage's four MMAs, and
+//    MMA kk uses byte kk of each scale word;
+//  - the expert-sorted activations are padded so each expert starts on a 128-row
+//    boundary (one token block = one scale atom per K step);
+//  - the gate/up epilogue applies SwiGLU and MX-quantises h along I (a warp's 32
+//    lanes hold one 32-feature block of one token), writing e4m3 codes and scale
+//    atoms that the down projection then reads.
+#include <cuda_fp8.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBK = 128;                          // fp8 elements per stage (128 bytes)
+constexpr int kBoxRows = 16;
+constexpr int kThreads = 256;
+constexpr int kMaxE = 256;
+constexpr int kStages = 6;
+constexpr int kABytes = kBM * kBK;                // 16 KB
+constexpr int kBBytes = kBN * kBK;                // 16 KB
+constexpr int kBoxBytes = kBoxRows * kBK;         // 2 KB
+constexpr int kSfBytes = 512;                     // one scale atom
+constexpr int kEpiBytes = 32 * 64 * 4 + 32 * 64 * 2 + 32 * 64;
+constexpr int kAccCols = kBN;                     // per accumulator
+constexpr int kSfCol = 2 * kAccCols;              // first scale-factor TMEM column
+constexpr int kTmemCols = 512;
+
+struct L {
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + kStages * kABytes;
+  static constexpr int kSf = kB + kStages * kBBytes;              // per stage: SFA, SFB
+  static constexpr int kEpi = kSf + kStages * 2 * kSfBytes;
+  static constexpr int kBar = kEpi + kEpiBytes;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kTables = kMisc + 16;
+  static constexpr int kEnd = kTables + (4 * (kMaxE + 1) + 8) * 4;
+  static constexpr int kSmemBytes = kEnd + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct MxArgs {
+  const int32_t* offsets;
+  int E;
+  int K[2];
+  int MW[2];
+  int ld[2];
+  int active[2];
+  const uint8_t* a_sf[2];   // weight scale atoms [E][MW/128][K/128][512]
+  const uint8_t* b_sf[2];   // activation scale atoms [Ppad/128][K/128][512]
+  uint8_t* hq;              // phase-0 output codes (Ppad, ld0)
+  uint8_t* h_sf;            // phase-0 output scale atoms [Ppad/128][ld0/128][512]
+  uint16_t* y;              // phase-1 output (Ppad, ld1) bf16
+  int* done;
+  int* status;
+};
+
+struct Unit {
+  int ph, e, mb, nb, row0, rows;   // row0: padded row of the token block
+};
+
+struct Tables {
+  const int* off;
+  const int* poff;
+  const int* uoff[2];
+  int E;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const Tables& tb) {
+  Unit r;
+  const int total0 = tb.uoff[0][tb.E];
+  r.ph = (u < total0) ? 0 : 1;
+  if (r.ph) u -= total0;
+  const int* uo = tb.uoff[r.ph];
+  int lo = 0, hi = tb.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (uo[mid] <= u) lo = mid;
+    else hi = mid;
+  }
+  r.e = lo;
+  const int local = u - uo[lo];
+  const int m = tb.off[lo + 1] - tb.off[lo];
+  const int nb = (m + kBN - 1) / kBN;
+  r.mb = local / nb;
+  r.nb = local - r.mb * nb;
+  r.row0 = tb.poff[lo] + r.nb * kBN;
+  r.rows = min(kBN, m - r.nb * kBN);
+  return r;
+}
+
+__device__ __forceinline__ bool wait_counter(const int* p, int need, const volatile int* abort) {
+  if (ld_acquire_gpu(p) >= need) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= need) return true;
+    if ((i & 15u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
+  if (ef == 0) return -127;
+  const int X = ef - 127 - 8;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
+__device__ __forceinline__ uint8_t mx_code(float v, int X) {
+  const int nx = -X;
+  const int a = nx > 126 ? 126 : nx;
+  const float f = v * __uint_as_float(static_cast<uint32_t>(a + 127) << 23) *
+                  __uint_as_float(static_cast<uint32_t>(nx - a + 127) << 23);
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA0,
+                           const __grid_constant__ CUtensorMap tmB0,
+                           const __grid_constant__ CUtensorMap tmA1,
+                           const __grid_constant__ CUtensorMap tmB1, const MxArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem + L::kA;
+  uint8_t* sB = smem + L::kB;
+  uint8_t* sSF = smem + L::kSf;
+  uint8_t* sEpi = smem + L::kEpi;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* fin = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  int* s_off = reinterpret_cast<int*>(smem + L::kTables);
+  int* s_poff = s_off + (kMaxE + 1);
+  int* s_uoff0 = s_poff + (kMaxE + 1);
+  int* s_uoff1 = s_uoff0 + (kMaxE + 1);
+  int* s_tmp = s_uoff1 + (kMaxE + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = args.E;
+  pdl_trigger();
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(fin, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 2) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  for (int i = tid; i <= E; i += kThreads) s_off[i] = args.offsets[i];
+  __syncthreads();
+
+  // units per expert (per phase) and the 128-row padded offsets, by block scans
+  {
+    int v[3] = {0, 0, 0};
+    if (tid < E) {
+      const int m = s_off[tid + 1] - s_off[tid];
+      const int nb = (m + kBN - 1) / kBN;
+      v[0] = args.active[0] ? nb * (args.MW[0] / kBM) : 0;
+      v[1] = args.active[1] ? nb * (args.MW[1] / kBM) : 0;
+      v[2] = nb * kBN;
+    }
+    int* dsts[3] = {s_uoff0, s_uoff1, s_poff};
+    for (int p = 0; p < 3; ++p) {
+      int inc = v[p];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) s_tmp[warp] = inc;
+      __syncthreads();
+      int pre = 0, tot = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        if (w < warp) pre += s_tmp[w];
+        tot += s_tmp[w];
+      }
+      if (tid < E) dsts[p][tid] = pre + inc - v[p];
+      if (tid == 0) dsts[p][E] = tot;
+      __syncthreads();
+    }
+  }
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
+  Tables tb;
+  tb.off = s_off;
+  tb.poff = s_poff;
+  tb.uoff[0] = s_uoff0;
+  tb.uoff[1] = s_uoff1;
+  tb.E = E;
+  const int total = s_uoff0[E] + s_uoff1[E];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer --
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t par = 0;
+      uint32_t issued_mask = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Unit t = decode_unit(u, tb);
+        if (t.ph == 1 && args.done != nullptr) {
+          const int m = s_off[t.e + 1] - s_off[t.e];
+          const int need = ((m + kBN - 1) / kBN) * (args.MW[0] / kBM);
+          if (!wait_counter(args.done + t.e, need, s_abort)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        const CUtensorMap* ta = t.ph ? &tmA1 : &tmA0;
+        const CUtensorMap* tbm = t.ph ? &tmB1 : &tmB0;
+        const int K = args.K[t.ph];
+        const int nk = K / kBK;
+        const int nbox = (t.rows + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes = kABytes + nbox * kBoxBytes + 2 * kSfBytes;
+        const int arow = t.e * args.MW[t.ph] + t.mb * kBM;
+        const uint8_t* asf =
+            args.a_sf[t.ph] + ((size_t)(t.e * (args.MW[t.ph] / kBM) + t.mb) * nk) * kSfBytes;
+        const uint8_t* bsf = args.b_sf[t.ph] + ((size_t)(t.row0 / kBN) * nk) * kSfBytes;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(sA + stage * kABytes, ta, &full[stage], kb * kBK, arow, pol_w);
+          for (int j = 0; j < nbox; ++j)
+            tma_load_2d(sB + stage * kBBytes + j * kBoxBytes, tbm, &full[stage], kb * kBK,
+                        t.row0 + j * kBoxRows, pol_x);
+          uint8_t* sf = sSF + stage * 2 * kSfBytes;
+          bulk_load_1d(sf, asf + (size_t)kb * kSfBytes, kSfBytes, &full[stage], pol_w);
+          bulk_load_1d(sf + kSfBytes, bsf + (size_t)kb * kSfBytes, kSfBytes, &full[stage], pol_x);
+          issued_mask |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (par << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (ok) {
+        for (int i = 0; i < kStages; ++i) {
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        for (int s = 0; s < kStages; ++s)
+          if ((issued_mask >> s) & 1u) mbar_wait(&full[s], (issued_par >> s) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------- MMA issuer --
+      int stage = 0, acc = 0;
+      uint32_t par = 0, apar = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Unit t = decode_unit(u, tb);
+        const int n = (t.rows + 15) & ~15;
+        if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+        const int nk = args.K[t.ph] / kBK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], par, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * 8);
+          const uint32_t sfb_t = sfa_t + 4;
+          const uint32_t sf_s = smem_u32(sSF + stage * 2 * kSfBytes);
+          tc_cp_32x128b_warpx4(sfa_t, smem_desc_noswz(sf_s, 128));
+          tc_cp_32x128b_warpx4(sfb_t, smem_desc_noswz(sf_s + kSfBytes, 128));
+          const uint32_t a0 = smem_u32(sA + stage * kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            tc_mma_mxf8(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32),
+                        idesc_mxf8_f32(kBM, n, kk, kk), sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) apar ^= 1u;
+      }
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        tc_commit(fin);
+        mbar_wait(fin, 0, nullptr);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue --
+    const int q = warp & 3;
+    const int et = tid - 128;
+    int* s_flag = s_tmp;
+    int acc = 0;
+    uint32_t apar = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const Unit t = decode_unit(u, tb);
+      if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort) ? 1 : 0;
+      named_bar_sync(1, 128);
+      const int ok = s_flag[0];
+      named_bar_sync(1, 128);
+      if (!ok) {
+        if (et == 0) {
+          *s_abort = 1;
+          flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * kAccCols);
+      if (t.ph == 0) {
+        // SwiGLU, then MX quantisation of h along I: lanes of a gate warp hold the
+        // 32 consecutive features of one scale block.
+        float* xbuf = reinterpret_cast<float*>(sEpi);                      // [32 tok][64] fp32
+        uint8_t* cbuf = sEpi + 32 * 64 * 4 + 32 * 64 * 2;                  // [32 tok][64] codes
+        const int ld = args.ld[0];
+        const int ksteps = ld / 128;
+        const int ks = t.mb / 2;                 // 128-feature step of the down projection
+        const int kbq = (t.mb & 1) * 2 + q;      // this warp's 32-feature block in that step
+        for (int c0 = 0; c0 < t.rows; c0 += 32) {
+          float v[32];
+          tmem_ld_32x32b_x32(tbase + c0, v);
+          if (q >= 2) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xbuf[j * 64 + (q - 2) * 32 + lane] = v[j];
+          }
+          named_bar_sync(1, 128);
+          if (q < 2) {
+            int myX = -127;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float g = v[j];
+              const float up = xbuf[j * 64 + q * 32 + lane];
+              const float h = g / (1.0f + __expf(-g)) * up;
+              float amax = fabsf(h);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+              const int X = mx_exponent(amax);
+              if (lane == j) myX = X;
+              cbuf[j * 64 + q * 32 + lane] = mx_code(h, X);
+            }
+            const int prow = t.row0 + c0 + lane;
+            if (c0 + lane < t.rows) {
+              uint8_t* atom = args.h_sf + ((size_t)(prow / 128) * ksteps + ks) * kSfBytes;
+              atom[(prow & 31) * 16 + ((prow >> 5) & 3) * 4 + kbq] =
+                  static_cast<uint8_t>(myX + 127);
+            }
+          }
+          named_bar_sync(1, 128);
+          {
+            const int j = et >> 2, c = et & 3;   // 32 rows x 4 vectors of 16 codes
+            if (c0 + j < t.rows) {
+              const uint4 val = *reinterpret_cast<const uint4*>(cbuf + j * 64 + c * 16);
+              *reinterpret_cast<uint4*>(args.hq + (size_t)(t.row0 + c0 + j) * ld + t.mb * 64 +
+                                        c * 16) = val;
+            }
+          }
+          named_bar_sync(1, 128);
+        }
+      } else {
+        uint16_t* tbw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 32;
+        const int ld = args.ld[1];
+        for (int c0 = 0; c0 < t.rows; c0 += 32) {
+          float v[32];
+          tmem_ld_32x32b_x32(tbase + c0, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tbw[j * 32 + lane] = f2bf(v[j]);
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int idx = lane + 32 * it;
+            const int j = idx >> 2, c = idx & 3;
+            if (c0 + j < t.rows) {
+              const uint4 val = *reinterpret_cast<const uint4*>(tbw + j * 32 + c * 8);
+              *reinterpret_cast<uint4*>(args.y + (size_t)(t.row0 + c0 + j) * ld + t.mb * kBM +
+                                        q * 32 + c * 8) = val;
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (t.ph == 0 && args.done != nullptr) {
+        __threadfence();
+        fence_proxy_async_global();
+        named_bar_sync(1, 128);
+        if (et == 0) red_release_add_gpu(args.done + t.e, 1);
+      }
+      acc ^= 1;
+      if (acc == 0) apar ^= 1u;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+bool encode_tmap_2d_u8(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
+                       uint32_t box_inner, uint32_t box_rows) {
+  return encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, inner, rows, box_inner,
+                        box_rows);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1,
+                                   const int32_t* offsets, int E, int P_pad_rows, int* done,
+                                   int* status, cudaStream_t s) {
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+      err = cudaFuncSetAttribute(grouped_gemm_mx_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+      if (err != cudaSuccess) return err;
+      attr_set[dev] = true;
+    }
+  }
+  MxArgs a{};
+  a.offsets = offsets;
+  a.E = E;
+  a.done = (ph0 && ph1) ? done : nullptr;
+  a.status = status;
+  CUtensorMap tm[4];
+  const GemmPhaseMx* phs[2] = {ph0, ph1};
+  for (int p = 0; p < 2; ++p) {
+    const GemmPhaseMx* g = phs[p] ? phs[p] : (ph0 ? ph0 : ph1);
+    a.active[p] = phs[p] != nullptr;
+    a.K[p] = g->K;
+    a.MW[p] = g->MW;
+    a.ld[p] = g->n_out;
+    a.a_sf[p] = g->A_sf;
+    a.b_sf[p] = g->B_sf;
+    if (!encode_tmap_2d_u8(&tm[2 * p], g->A_q, (uint64_t)g->K, (uint64_t)E * g->MW, kBK, kBM))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap_2d_u8(&tm[2 * p + 1], g->B_q, (uint64_t)g->K, (uint64_t)P_pad_rows, kBK,
+                           kBoxRows))
+      return cudaErrorInvalidValue;
+  }
+  if (ph0) {
+    a.hq = ph0->out_q;
+    a.h_sf = ph0->out_sf;
+  }
+  if (ph1) a.y = ph1->out_bf16;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_sm_count(), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = a.done != nullptr ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_kernel, tm[0], tm[1], tm[2], tm[3], a);
+}
+
+}  // namespace moe

@@ -22,6 +22,10 @@ RouterPlan router_plan(int T, int H, int E);
 cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
                           const RouterPlan& plan, float* partial_or_out, int* zero_word,
                           cudaStream_t s);
+// Same with fp32 activations (the MXFP8 path routes on the fp32 normalised input).
+cudaError_t launch_router_f32(const float* x, const float* Wg, int T, int H, int E,
+                              const RouterPlan& plan, float* partial_or_out, int* zero_word,
+                              cudaStream_t s);
 cudaError_t launch_router_reduce(const float* partial, int splits, int T, int E, float* logits,
                                  cudaStream_t s);
 // Optional init_routing fused into the gating launch (one-CTA routing, P <= 4096):
@@ -80,9 +84,39 @@ cudaError_t launch_pack_w13(const uint16_t* w13, int E, int H, int I, uint16_t* 
 cudaError_t launch_pack_down(const uint16_t* down, int E, int H, int I, uint16_t* out,
                              cudaStream_t s);
 
+// ---- MXFP8 (mx.cu, gmm_mx.cu)
+cudaError_t launch_add_rmsnorm_mxquant(const uint16_t* x, const uint16_t* r, const uint16_t* w,
+                                       float eps, int T, int H, uint16_t* residual_out,
+                                       float* y32_out, uint8_t* q, uint8_t* scale, cudaStream_t s);
+cudaError_t launch_mx_quantize(const float* y, int rows, int n, uint8_t* q, uint8_t* scale,
+                               cudaStream_t s);
+cudaError_t launch_pack_mx(const uint16_t* w13, const uint16_t* down, int E, int H, int I,
+                           uint8_t* w13q, uint8_t* w13sf, uint8_t* downq, uint8_t* downsf,
+                           cudaStream_t s);
+cudaError_t launch_mx_expand(const uint8_t* xq, const uint8_t* xs, const int32_t* ids,
+                             const int32_t* eri, const int32_t* offsets, int E, int P, int H,
+                             int k, uint8_t* xe, uint8_t* xe_sf, int32_t* eri_pad,
+                             cudaStream_t s);
+struct GemmPhaseMx {
+  const void* A_q;          // packed e4m3 weights, rows = E * MW, K bytes each
+  const uint8_t* A_sf;      // weight scale atoms
+  const uint8_t* B_q;       // padded expert-sorted activation codes (rows, K)
+  const uint8_t* B_sf;      // their scale atoms
+  uint8_t* out_q;           // phase 0: h codes (rows, n_out)
+  uint8_t* out_sf;          // phase 0: h scale atoms
+  uint16_t* out_bf16;       // phase 1: y (rows, n_out)
+  int K, MW, n_out;
+};
+cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1,
+                                   const int32_t* offsets, int E, int P_pad_rows, int* done,
+                                   int* status, cudaStream_t s);
+
 // ---- device facts (api.cu)
 int device_sm_count();
 int* device_status_ptr();  // the current device's status word, or null
+bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                    const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                    uint32_t box_rows);
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                          uint32_t box_inner, uint32_t box_rows);
 

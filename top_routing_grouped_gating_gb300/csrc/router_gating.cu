@@ -25,7 +25,8 @@ constexpr int kRT = 32;    // tokens per router tile
 constexpr int kRE = 128;   // experts per router tile
 constexpr int kRK = 32;    // H rows per smem step
 
-__global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict__ x,
+template <typename XT>
+__global__ void __launch_bounds__(256) router_kernel(const XT* __restrict__ x,
                                                      const float* __restrict__ Wg, int T, int H,
                                                      int E, int h_per_split,
                                                      float* __restrict__ out, int* zero_word) {
@@ -54,11 +55,19 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict_
       const int tt = tid >> 3, hh = (tid & 7) * 4;
       float v[4] = {0.f, 0.f, 0.f, 0.f};
       if (t0 + tt < T) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)(t0 + tt) * H + h0 + hh);
-        v[0] = bf16_lo(raw.x);
-        v[1] = bf16_hi(raw.x);
-        v[2] = bf16_lo(raw.y);
-        v[3] = bf16_hi(raw.y);
+        if constexpr (sizeof(XT) == 4) {
+          const float4 f = *reinterpret_cast<const float4*>(x + (size_t)(t0 + tt) * H + h0 + hh);
+          v[0] = f.x;
+          v[1] = f.y;
+          v[2] = f.z;
+          v[3] = f.w;
+        } else {
+          const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)(t0 + tt) * H + h0 + hh);
+          v[0] = bf16_lo(raw.x);
+          v[1] = bf16_hi(raw.x);
+          v[2] = bf16_lo(raw.y);
+          v[3] = bf16_hi(raw.y);
+        }
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) xs[tt][hh + q] = v[q];
@@ -103,7 +112,8 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict_
 constexpr int kSmallRows = 128;
 constexpr int kSmallExp = 32;
 
-__global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __restrict__ x,
+template <typename XT>
+__global__ void __launch_bounds__(256) router_small_kernel(const XT* __restrict__ x,
                                                            const float* __restrict__ Wg, int T,
                                                            int H, int E,
                                                            float* __restrict__ partial,
@@ -128,17 +138,31 @@ __global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __res
     const int hh = idx >> 5, ee = idx & 31;
     ws[hh][ee] = (e0 + ee < E) ? Wg[(size_t)(hb + hh) * E + e0 + ee] : 0.f;
   }
+  if constexpr (sizeof(XT) == 4) {
 #pragma unroll
-  for (int r = 0; r < (kRT * kSmallRows) / (256 * 8); ++r) {
-    const int idx = tid + 256 * r;
-    const int tt = idx >> 4, h8 = (idx & 15) * 8;
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (t0 + tt < T) raw = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + hb + h8);
-    const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int r = 0; r < (kRT * kSmallRows) / (256 * 4); ++r) {
+      const int idx = tid + 256 * r;
+      const int tt = idx >> 5, h4 = (idx & 31) * 4;
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t0 + tt < T) f = *reinterpret_cast<const float4*>(x + (size_t)(t0 + tt) * H + hb + h4);
+      xs[tt][h4] = f.x;
+      xs[tt][h4 + 1] = f.y;
+      xs[tt][h4 + 2] = f.z;
+      xs[tt][h4 + 3] = f.w;
+    }
+  } else {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      xs[tt][h8 + 2 * q] = bf16_lo(u[q]);
-      xs[tt][h8 + 2 * q + 1] = bf16_hi(u[q]);
+    for (int r = 0; r < (kRT * kSmallRows) / (256 * 8); ++r) {
+      const int idx = tid + 256 * r;
+      const int tt = idx >> 4, h8 = (idx & 15) * 8;
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (t0 + tt < T) raw = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + hb + h8);
+      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xs[tt][h8 + 2 * q] = bf16_lo(u[q]);
+        xs[tt][h8 + 2 * q + 1] = bf16_hi(u[q]);
+      }
     }
   }
   __syncthreads();
@@ -286,17 +310,28 @@ RouterPlan router_plan(int T, int H, int E) {
   return p;
 }
 
-cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
-                          const RouterPlan& plan, float* out, int* zero_word, cudaStream_t s) {
+template <typename XT>
+cudaError_t launch_router_t(const XT* x, const float* Wg, int T, int H, int E,
+                            const RouterPlan& plan, float* out, int* zero_word, cudaStream_t s) {
   if (plan.small) {
     dim3 grid(plan.e_tiles, plan.splits, plan.t_tiles);
-    return launch_pdl(router_small_kernel, grid, dim3(256), 0, s, x, Wg, T, H, E, out, zero_word);
-  } else {
-    dim3 grid(plan.t_tiles, plan.e_tiles, plan.splits);
-    return launch_pdl(router_kernel, grid, dim3(256), 0, s, x, Wg, T, H, E, H / plan.splits, out,
+    return launch_pdl(router_small_kernel<XT>, grid, dim3(256), 0, s, x, Wg, T, H, E, out,
                       zero_word);
   }
-  return cudaGetLastError();
+  dim3 grid(plan.t_tiles, plan.e_tiles, plan.splits);
+  return launch_pdl(router_kernel<XT>, grid, dim3(256), 0, s, x, Wg, T, H, E, H / plan.splits,
+                    out, zero_word);
+}
+
+cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
+                          const RouterPlan& plan, float* out, int* zero_word, cudaStream_t s) {
+  return launch_router_t(x, Wg, T, H, E, plan, out, zero_word, s);
+}
+
+cudaError_t launch_router_f32(const float* x, const float* Wg, int T, int H, int E,
+                              const RouterPlan& plan, float* out, int* zero_word,
+                              cudaStream_t s) {
+  return launch_router_t(x, Wg, T, H, E, plan, out, zero_word, s);
 }
 
 cudaError_t launch_router_reduce(const float* partial, int splits, int T, int E, float* logits,
