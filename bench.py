@@ -171,38 +171,44 @@ def gemm_flops(cfg) -> float:
 
 
 def launches_per_step(cfg, router: bool = True) -> int:
+    """Kernels one moe_forward call launches: router, gating (routing fused into it
+    when P <= 4096, else histogram + scan + scatter), row expansion, grouped GEMM,
+    finalize; the MXFP8 layer adds the fused add+RMSNorm+quant kernel."""
     P = cfg.T * cfg.k
-    routing = 1 if P <= 4096 else 3
-    return (1 if router else 0) + 1 + routing + 1 + 1 + 1
+    routing = 0 if P <= 4096 else 3
+    return (1 if cfg.mx else 0) + (1 if router else 0) + 1 + routing + 1 + 1 + 1
 
 
 # ------------------------------------------------------------ CPU oracle arm --
 
 
 def oracle_arrays(inp):
-    """Host fp64 copies of the weights (untimed: the oracle's inputs at rest)."""
-    import numpy as np
+    """Host fp64 copies of the inputs (untimed: the oracle's inputs at rest)."""
     E = inp["w13"].shape[0]
-    w13 = [inp["w13"][e].double().cpu().numpy() for e in range(E)]
-    down = [inp["down"][e].double().cpu().numpy() for e in range(E)]
-    x = inp["x"].double().cpu().numpy()
-    Wg = inp["Wg"].double().cpu().numpy()
-    return x, Wg, w13, down
+    arr = {"w13": [inp["w13"][e].double().cpu().numpy() for e in range(E)],
+           "down": [inp["down"][e].double().cpu().numpy() for e in range(E)]}
+    for key in ("x", "Wg", "r", "norm_w"):
+        if key in inp:
+            arr[key] = inp[key].double().cpu().numpy()
+    return arr
 
 
-def oracle_step(O, arrays, k, rows):
-    x, Wg, w13, down = arrays
-    O.moe_forward(x[rows], Wg, w13, down, k, keep_intermediates=False)
+def oracle_step(O, arrays, cfg, rows):
+    a = arrays
+    if cfg.mx:
+        O.moe_forward_mx(a["x"][rows], a["r"][rows], a["norm_w"], cfg.eps, a["Wg"], a["w13"], a["down"], cfg.k)
+    else:
+        O.moe_forward(a["x"][rows], a["Wg"], a["w13"], a["down"], cfg.k, keep_intermediates=False)
 
 
-def time_oracle(O, arrays, k, T, target_s):
+def time_oracle(O, arrays, cfg, target_s):
     """Tokens/s of the oracle on consecutive token samples until ~target_s of CPU time."""
     n = 0
     t0 = time.perf_counter()
     start = 0
     while time.perf_counter() - t0 < target_s:
-        rows = [(start + i) % T for i in range(min(T, 4))]
-        oracle_step(O, arrays, k, rows)
+        rows = [(start + i) % cfg.T for i in range(min(cfg.T, 4))]
+        oracle_step(O, arrays, cfg, rows)
         n += len(rows)
         start += len(rows)
     dt = time.perf_counter() - t0
@@ -224,15 +230,15 @@ def run_reference(args, cfg):
     del inp
     # size each step's token sample so the whole K+W run stays within a few minutes
     t0 = time.perf_counter()
-    oracle_step(O, arrays, cfg.k, [0])
+    oracle_step(O, arrays, cfg, [0])
     per_tok = max(time.perf_counter() - t0, 1e-4)
     budget = 150.0 / max(args.steps + args.warmup, 1)
     ntok = int(max(1, min(cfg.T, budget // per_tok)))
     for i in range(args.warmup):
-        oracle_step(O, arrays, cfg.k, [(i * ntok + j) % cfg.T for j in range(ntok)])
+        oracle_step(O, arrays, cfg, [(i * ntok + j) % cfg.T for j in range(ntok)])
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle_step(O, arrays, cfg.k, [(i * ntok + j) % cfg.T for j in range(ntok)])
+        oracle_step(O, arrays, cfg, [(i * ntok + j) % cfg.T for j in range(ntok)])
     dt = time.perf_counter() - t0
     value = ntok * args.steps / dt
     cores = blas_threads()
@@ -278,12 +284,24 @@ def run_ours(args, cfg):
     from top_routing_grouped_gating_gb300 import workloads as W
 
     inp = W.make_inputs(cfg, device=f"cuda:{local}")
-    layer = moe.MoELayer(inp["Wg"], inp["w13"], inp["down"], cfg.k)
     x = inp["x"]
     stream = torch.cuda.current_stream(dev)
-    out, ids, w = layer(x)
+    if cfg.mx:
+        layer = moe.MoELayerMX(inp["Wg"], inp["w13"], inp["down"], inp["norm_w"], cfg.k, cfg.eps)
+        r = inp["r"]
+        out, res, ids, w = layer(x, r)
+        bufs = dict(out=out, residual_out=res, topk_ids=ids, topk_w=w)
+
+        def step(xx, rr=r):
+            return layer(xx, rr, **bufs)[0]
+    else:
+        layer = moe.MoELayer(inp["Wg"], inp["w13"], inp["down"], cfg.k)
+        out, ids, w = layer(x)
+        bufs = dict(out=out, topk_ids=ids, topk_w=w)
+
+        def step(xx, rr=None):
+            return layer(xx, **bufs)[0]
     torch.cuda.synchronize(dev)
-    bufs = dict(out=out, topk_ids=ids, topk_w=w)
     counts = torch.bincount(ids.flatten().long(), minlength=cfg.E)
     active = int((counts > 0).sum())
 
@@ -300,13 +318,17 @@ def run_ours(args, cfg):
 
     # ---- warm-up
     for _ in range(max(args.warmup, 3)):
-        layer(x, **bufs)
+        step(x)
     torch.cuda.synchronize(dev)
 
     # ---- timed region (device-resident inputs), grouped-GEMM events on every step
     K = args.steps
-    gb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ge = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    # grouped-GEMM events on every GEMM_EVERY-th step of the timed region (an event
+    # pair between two kernels costs their programmatic launch overlap)
+    GEMM_EVERY = 8
+    timed = list(range(0, K, GEMM_EVERY))
+    gb = {i: torch.cuda.Event(enable_timing=True) for i in timed}
+    ge = {i: torch.cuda.Event(enable_timing=True) for i in timed}
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
@@ -314,38 +336,47 @@ def run_ours(args, cfg):
     torch.cuda.synchronize(dev)
     t_start.record(stream)
     for i in range(K):
-        # torch only reports elapsed_time for events it recorded itself; record both
-        # here first, the library then re-records them around the grouped GEMM
-        gb[i].record(stream)
-        ge[i].record(stream)
-        moe.set_gemm_events(gb[i], ge[i])
-        layer(x, **bufs)
+        if i in gb:
+            # torch only reports elapsed_time for events it recorded itself; record
+            # both here first, the library then re-records them around the GEMM
+            gb[i].record(stream)
+            ge[i].record(stream)
+            moe.set_gemm_events(gb[i], ge[i])
+        step(x)
+        if i in gb:
+            moe.set_gemm_events(None, None)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clocks = sampler.stop()
     moe.set_gemm_events(None, None)
     ms_total = max_over_ranks(t_start.elapsed_time(t_end))
-    gemm_ms = statistics.mean(gb[i].elapsed_time(ge[i]) for i in range(K))
+    gemm_ms = statistics.mean(gb[i].elapsed_time(ge[i]) for i in timed)
     status = moe.get_device_status(dev)
 
     # ---- end-to-end: pinned host input -> device -> layer -> pinned host output
     x_host = x.cpu().pin_memory()
+    r_host = inp["r"].cpu().pin_memory() if cfg.mx else None
     o_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
-    for _ in range(3):
+    r_dev = torch.empty_like(x) if cfg.mx else None
+
+    def e2e_step():
         x_dev.copy_(x_host, non_blocking=True)
-        o, _, _ = layer(x_dev, **bufs)
+        if cfg.mx:
+            r_dev.copy_(r_host, non_blocking=True)
+        o = step(x_dev, r_dev)
         o_host.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
     torch.cuda.synchronize(dev)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
     e_start.record(stream)
     for _ in range(K):
-        x_dev.copy_(x_host, non_blocking=True)
-        o, _, _ = layer(x_dev, **bufs)
-        o_host.copy_(o, non_blocking=True)
+        e2e_step()
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -360,6 +391,8 @@ def run_ours(args, cfg):
     value = cfg.T * K * ws / (ms_total / 1e3)
     decode = cfg.T * cfg.k <= 16 * cfg.E
     gbytes = algorithmic_gemm_bytes(cfg, active)
+    if cfg.mx:
+        bf16 = bf16 * 2.0   # MXFP8 dense peak: measured bf16 x the nominal fp8/bf16 ratio (4.5/2.25)
     if decode:
         achieved = gbytes / (gemm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
@@ -367,10 +400,11 @@ def run_ours(args, cfg):
                 else "fallback 6.8 TB/s"}
     else:
         achieved = gemm_flops(cfg) / (gemm_ms / 1e3) / 1e12
+        src = "bf16_tflops x 2 (nominal MXFP8/bf16 ratio)" if cfg.mx else "bf16_tflops"
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
                 "frac": achieved / bf16,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops)" if peak_kind == "measured"
-                else "fallback 1.9 PFLOP/s"}
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json {src})" if peak_kind == "measured"
+                else "fallback 1.9 PFLOP/s" + (" x 2" if cfg.mx else "")}
     tr = profiled_traffic(cfg.name)
     roof.update({"traffic": tr, "kernel": "grouped_gemm_kernel (both projections, one launch)",
                  "kernel_ms": gemm_ms, "algorithmic_bytes": gbytes, "active_experts": active})
@@ -378,10 +412,11 @@ def run_ours(args, cfg):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(cfg),
-        "roofline": roof,
+        "vs_baseline": None, "dtype": "mxfp8 (e4m3 + e8m0/32)" if cfg.mx else "bf16", "data": "synthetic",
+        "config": workload_config(cfg), "roofline": roof,
         "e2e": {"value": cfg.T * K * ws / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": cfg.T * cfg.H * 2, "d2h_bytes_per_step": cfg.T * cfg.H * 2},
+                "h2d_bytes_per_step": cfg.T * cfg.H * 2 * (2 if cfg.mx else 1),
+                "d2h_bytes_per_step": cfg.T * cfg.H * 2},
         "gpu_launches": launches_per_step(cfg) * K,
         "clocks": clocks,
         "device_status": status,
@@ -390,7 +425,7 @@ def run_ours(args, cfg):
     if not args.no_cpu_baseline:
         from oracle import moe_oracle as O
         arrays = oracle_arrays({k_: v.cpu() for k_, v in inp.items()})
-        v_cpu, ntok, dt = time_oracle(O, arrays, cfg.k, cfg.T, args.cpu_seconds)
+        v_cpu, ntok, dt = time_oracle(O, arrays, cfg, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                                 "sample": f"{ntok} tokens of the workload in batches of 4 over {dt:.1f} s, "
                                           f"numpy fp64 oracle, weights pre-widened to fp64 in host memory"}
@@ -406,8 +441,6 @@ def main(argv=None):
     if args.workload not in W.CONFIGS:
         raise SystemExit(f"unknown workload {args.workload}; one of {sorted(W.CONFIGS)}")
     cfg = W.CONFIGS[args.workload]
-    if cfg.mx:
-        raise SystemExit("the MXFP8 workload is not benchmarked by this script yet")
     if args.impl == "reference":
         return run_reference(args, cfg)
     return run_ours(args, cfg)

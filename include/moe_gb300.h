@@ -134,8 +134,9 @@ MOE_API moe_status moe_compute_expert_tokens(const int32_t* topk_ids, int P, int
  *        SwiGLU op chunks the merged product in two and gates the first half)
  *   down (E,I,H)  bf16
  *   w13_packed  >= moe_packed_weight_bytes(E,H,I,0) bytes: per expert 2I rows of H
- *        (row block b of 128 rows = gate columns 64b..64b+63, then the matching up
- *        columns)
+ *        (row block b of 128 rows covers features 64b..64b+63; in each 32-row
+ *        quarter q, rows 0-15 are gate columns 64b+16q.. and rows 16-31 the matching
+ *        up columns)
  *   down_packed >= moe_packed_weight_bytes(E,H,I,1) bytes: per expert H rows of I
  * Either input may be NULL to skip it.
  */

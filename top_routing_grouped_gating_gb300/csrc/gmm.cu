@@ -12,8 +12,9 @@
 // tokens.
 //
 // Work unit = (phase, expert, 128-row weight block, token block).  Phase 0 is the
-// gate/up projection (weights packed so each 128-row block holds 64 gate rows and
-// the 64 matching up rows); phase 1 is the down projection.  Units are numbered
+// gate/up projection (weights packed so each 32-row quarter of a 128-row block
+// holds 16 gate rows and the 16 matching up rows, paired by a warp shuffle in the
+// epilogue); phase 1 is the down projection.  Units are numbered
 // phase-major, expert-major, weight-block-major, token-block-minor and handed to
 // CTAs round-robin (grid = SM count, one CTA per SM).  When both phases run in one
 // launch, a phase-1 unit waits until every phase-0 unit of its expert has
@@ -37,12 +38,10 @@ namespace {
 
 constexpr int kBM = 128;         // weight rows per tile (MMA M)
 constexpr int kBK = 64;          // K per stage: one 128-byte swizzle row of bf16
-constexpr int kBoxRows = 16;     // token rows per TMA box
 constexpr int kThreads = 256;
 constexpr int kMaxE = 256;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
-constexpr int kBoxBytes = kBoxRows * kBK * 2;   // 2 KB
-constexpr int kEpiBytes = 32 * 64 * 4 + 32 * 64 * 2;  // SwiGLU exchange + h staging
+constexpr int kEpiBytes = 4 * 32 * 32 * 2;  // per epilogue warp: 32 tokens x 32 bf16
 
 struct GemmArgs {
   const int32_t* offsets;
@@ -57,9 +56,10 @@ struct GemmArgs {
   int* status;
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int BOX>
 struct Layout {
   static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kBoxBytes = BOX * kBK * 2;
   static constexpr int kA = 0;
   static constexpr int kB = kA + STAGES * kABytes;
   static constexpr int kEpi = kB + STAGES * kBBytes;
@@ -124,13 +124,13 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int BOX>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, BOX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -239,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const CUtensorMap* ta = t.ph ? &tmA1 : &tmA0;
         const CUtensorMap* tbm = t.ph ? &tmB1 : &tmB0;
-        const int nbox = (t.rows + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = kABytes + nbox * kBoxBytes;
+        const int nbox = (t.rows + BOX - 1) / BOX;
+        const uint32_t bytes = kABytes + nbox * L::kBoxBytes;
         const int arow = t.e * args.MW[t.ph] + t.mb * kBM;
         const int nk = args.K[t.ph] / kBK;
         for (int kb = 0; kb < nk; ++kb) {
@@ -251,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sA + stage * kABytes, ta, &full[stage], kb * kBK, arow, pol_w);
           for (int j = 0; j < nbox; ++j)
-            tma_load_2d(sB + stage * L::kBBytes + j * kBoxBytes, tbm, &full[stage], kb * kBK,
-                        t.row0 + j * kBoxRows, pol_x);
+            tma_load_2d(sB + stage * L::kBBytes + j * L::kBoxBytes, tbm, &full[stage], kb * kBK,
+                        t.row0 + j * BOX, pol_x);
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (par << stage);
           if (++stage == STAGES) {
@@ -356,38 +356,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint16_t* out = args.out[t.ph];
       const int ld = args.ld[t.ph];
       if (args.swiglu[t.ph]) {
-        // lanes 0-63 of the tile are gate rows, 64-127 the matching up rows
-        float* xbuf = reinterpret_cast<float*>(sEpi);                   // [32 tok][64] fp32
-        uint16_t* hbuf = reinterpret_cast<uint16_t*>(sEpi + 32 * 64 * 4);  // [32 tok][64] bf16
+        // Each 32-lane TMEM quarter holds 16 gate rows (lanes 0-15) and the 16
+        // matching up rows (lanes 16-31).  One shuffle across the half-warps pairs
+        // them: lanes 0-15 finish tokens 0-15 of the chunk, lanes 16-31 tokens 16-31,
+        // for feature t.mb*64 + q*16 + (lane % 16).
+        uint16_t* hw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 16;  // [32 tok][16] bf16
+        const bool lo = lane < 16;
+        const int f = lane & 15;
         for (int c0 = 0; c0 < t.rows; c0 += 32) {
           float v[32];
           tmem_ld_32x32b_x32(tbase + c0, v);
-          if (q >= 2) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) xbuf[j * 64 + (q - 2) * 32 + lane] = v[j];
+          for (int j = 0; j < 16; ++j) {
+            const float send = lo ? v[16 + j] : v[j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            const float g = lo ? v[j] : recv;
+            const float up = lo ? recv : v[16 + j];
+            const float h = g / (1.0f + __expf(-g)) * up;
+            hw[(lo ? j : 16 + j) * 16 + f] = f2bf(h);
           }
-          named_bar_sync(1, 128);
-          if (q < 2) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float g = v[j];
-              const float up = xbuf[j * 64 + q * 32 + lane];
-              const float h = g / (1.0f + __expf(-g)) * up;
-              hbuf[j * 64 + q * 32 + lane] = f2bf(h);
-            }
+          __syncwarp();
+          if (c0 + lane < t.rows) {
+            const uint4* src = reinterpret_cast<const uint4*>(hw + lane * 16);
+            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)(t.row0 + c0 + lane) * ld +
+                                                  t.mb * 64 + q * 16);
+            dst[0] = src[0];
+            dst[1] = src[1];
           }
-          named_bar_sync(1, 128);
-#pragma unroll
-          for (int it = 0; it < 2; ++it) {
-            const int idx = et + it * 128;
-            const int j = idx >> 3, c = idx & 7;
-            if (c0 + j < t.rows) {
-              const uint4 val = *reinterpret_cast<const uint4*>(hbuf + j * 64 + c * 8);
-              *reinterpret_cast<uint4*>(out + (size_t)(t.row0 + c0 + j) * ld + t.mb * 64 + c * 8) =
-                  val;
-            }
-          }
-          named_bar_sync(1, 128);
+          __syncwarp();
         }
       } else {
         uint16_t* tbw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 32;  // [32 tok][32] bf16
@@ -432,17 +428,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Packed w13: per expert 2I rows of H; row block b (128 rows) = gate columns
-// 64b..64b+63 then up columns I+64b..I+64b+63.  Tiled 32x32 transpose.
+// Packed w13: per expert 2I rows of H.  Row block b (128 rows) covers features
+// 64b..64b+63; its quarter q (rows 32q..32q+31) holds gate columns 64b+16q+i in
+// rows 32q+i and the matching up columns I+64b+16q+i in rows 32q+16+i (i < 16), so
+// one TMEM lane quarter of the accumulator holds both halves of 16 features.
+// Tiled 32x32 transpose.
 __global__ void pack_w13_kernel(const uint16_t* __restrict__ w13, int H, int I,
                                 uint16_t* __restrict__ out) {
   __shared__ uint16_t tile[32][33];
   const int h0 = blockIdx.x * 32, r0 = blockIdx.y * 32, e = blockIdx.z;
   const int tx = threadIdx.x, ty = threadIdx.y;
-  const int blk = r0 / 128, within = r0 % 128;
-  const int col0 = within < 64 ? blk * 64 + within : I + blk * 64 + (within - 64);
+  const int blk = r0 / 128, q = (r0 % 128) / 32;
+  const int col = tx < 16 ? blk * 64 + q * 16 + tx : I + blk * 64 + q * 16 + (tx - 16);
   const size_t n2 = 2 * (size_t)I;
-  for (int i = ty; i < 32; i += 8) tile[i][tx] = w13[((size_t)e * H + h0 + i) * n2 + col0 + tx];
+  for (int i = ty; i < 32; i += 8) tile[i][tx] = w13[((size_t)e * H + h0 + i) * n2 + col];
   __syncthreads();
   for (int i = ty; i < 32; i += 8)
     out[((size_t)e * n2 + r0 + i) * H + h0 + tx] = tile[tx][i];
@@ -460,10 +459,10 @@ __global__ void pack_down_kernel(const uint16_t* __restrict__ down, int H, int I
     out[((size_t)e * H + n0 + i) * I + i0 + tx] = tile[tx][i];
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int BOX>
 cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_t* offsets, int E,
                         int P, int* done, int* status, cudaStream_t s) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, BOX>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -473,7 +472,7 @@ cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_
     std::lock_guard<std::mutex> lk(mu);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-      err = cudaFuncSetAttribute(grouped_gemm_kernel<BN, STAGES>,
+      err = cudaFuncSetAttribute(grouped_gemm_kernel<BN, STAGES, BOX>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
       if (err != cudaSuccess) return err;
       attr_set[dev] = true;
@@ -497,8 +496,7 @@ cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_
     if (!encode_tmap_2d_bf16(&tm[2 * p], g->A_weights, (uint64_t)g->K, (uint64_t)E * g->MW, kBK,
                              kBM))
       return cudaErrorInvalidValue;
-    if (!encode_tmap_2d_bf16(&tm[2 * p + 1], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK,
-                             kBoxRows))
+    if (!encode_tmap_2d_bf16(&tm[2 * p + 1], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK, BOX))
       return cudaErrorInvalidValue;
   }
   cudaLaunchConfig_t cfg = {};
@@ -511,7 +509,8 @@ cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_
   attr[0].val.cooperative = a.done != nullptr ? 1 : 0;  // co-residency for the phase dependency
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<BN, STAGES>, tm[0], tm[1], tm[2], tm[3], a);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<BN, STAGES, BOX>, tm[0], tm[1], tm[2], tm[3],
+                            a);
 }
 
 }  // namespace
@@ -522,8 +521,8 @@ cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
   (void)max_rows_hint;
   // Thin token tiles when the mean expert load is small (decode), wide ones else.
   if ((long long)P <= 16LL * E)
-    return launch_impl<32, 10>(ph0, ph1, offsets, E, P, done_counter, status, s);
-  return launch_impl<256, 4>(ph0, ph1, offsets, E, P, done_counter, status, s);
+    return launch_impl<32, 10, 16>(ph0, ph1, offsets, E, P, done_counter, status, s);
+  return launch_impl<256, 4, 64>(ph0, ph1, offsets, E, P, done_counter, status, s);
 }
 
 cudaError_t launch_pack_w13(const uint16_t* w13, int E, int H, int I, uint16_t* out,

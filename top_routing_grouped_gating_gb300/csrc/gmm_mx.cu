@@ -31,13 +31,13 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kBK = 128;                          // fp8 elements per stage (128 bytes)
-constexpr int kBoxRows = 16;
+constexpr int kBoxRows = 64;
 constexpr int kThreads = 256;
 constexpr int kMaxE = 256;
 constexpr int kStages = 6;
 constexpr int kABytes = kBM * kBK;                // 16 KB
 constexpr int kBBytes = kBN * kBK;                // 16 KB
-constexpr int kBoxBytes = kBoxRows * kBK;         // 2 KB
+constexpr int kBoxBytes = kBoxRows * kBK;         // 8 KB
 constexpr int kSfBytes = 512;                     // one scale atom
 constexpr int kEpiBytes = 32 * 64 * 4 + 32 * 64 * 2 + 32 * 64;
 constexpr int kAccCols = kBN;                     // per accumulator
