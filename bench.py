@@ -179,6 +179,29 @@ def launches_per_step(cfg, router: bool = True) -> int:
     return (1 if cfg.mx else 0) + (1 if router else 0) + 1 + routing + 1 + 1 + 1
 
 
+def rank_barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max_over_ranks(v: float, world: int, device) -> float:
+    """The largest v over all ranks (the slowest rank's time)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(T: int, steps: int, world: int, ms_total: float) -> float:
+    """Tokens processed by all ranks (each rank runs its own T-token batches) per
+    second of the slowest rank's timed region."""
+    return T * steps * world / (ms_total / 1e3)
+
+
 # ------------------------------------------------------------ CPU oracle arm --
 
 
@@ -306,15 +329,10 @@ def run_ours(args, cfg):
     active = int((counts > 0).sum())
 
     def barrier():
-        if ws > 1:
-            torch.distributed.barrier()
+        rank_barrier(ws)
 
     def max_over_ranks(v: float) -> float:
-        if ws == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max_over_ranks(v, ws, dev)
 
     # ---- warm-up
     for _ in range(max(args.warmup, 3)):
@@ -388,7 +406,7 @@ def run_ours(args, cfg):
         return 0
 
     hbm, bf16, peak_kind = measured_peaks()
-    value = cfg.T * K * ws / (ms_total / 1e3)
+    value = whole_job_tokens_per_s(cfg.T, K, ws, ms_total)
     decode = cfg.T * cfg.k <= 16 * cfg.E
     gbytes = algorithmic_gemm_bytes(cfg, active)
     if cfg.mx:
@@ -414,7 +432,7 @@ def run_ours(args, cfg):
         "warmup": args.warmup, "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8 (e4m3 + e8m0/32)" if cfg.mx else "bf16", "data": "synthetic",
         "config": workload_config(cfg), "roofline": roof,
-        "e2e": {"value": cfg.T * K * ws / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_tokens_per_s(cfg.T, K, ws, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.H * 2 * (2 if cfg.mx else 1),
                 "d2h_bytes_per_step": cfg.T * cfg.H * 2},
         "gpu_launches": launches_per_step(cfg) * K,
