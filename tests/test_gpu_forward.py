@@ -83,8 +83,9 @@ def test_forward_single_expert_is_dense_mlp(layers):
     _check_forward(cfg, inp, layer)
 
 
-def test_forward_with_gpu_router(layers):
-    cfg, inp, layer = layers("qwen3_30b_a3b_decode", T=64)
+@pytest.mark.parametrize("T", [64, 300])
+def test_forward_with_gpu_router(layers, T):
+    cfg, inp, layer = layers("qwen3_30b_a3b_decode", T=T)
     x, Wg = inp["x"], inp["Wg"]
     out, ids, w = layer(x)
     torch.cuda.synchronize()

@@ -151,3 +151,25 @@ def test_forward_mx_full_size_sampled(cuda_dev):
     a = layer(inp["x"], inp["r"])[0].clone()
     b = layer(inp["x"], inp["r"])[0]
     assert torch.equal(a, b)
+
+
+def test_forward_mx_with_gpu_router(cuda_dev):
+    from tests._helpers import routing_margin_ok
+    cfg = W.with_shape(W.CONFIGS["mxfp8_prefill"], T=300, E=16, k=4, H=512, I=128)
+    inp, layer = _mx_layer(cfg)
+    out, res, ids, w = layer(inp["x"], inp["r"])
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 0
+    _, y = O.add_rmsnorm(to_np(inp["x"]), to_np(inp["r"]), to_np(inp["norm_w"]), cfg.eps)
+    Wn = to_np(inp["Wg"]).astype(np.float64)
+    lg = O.router_logits_f32(y, Wn)
+    # router error: fp32 RMSNorm output (~1e-6 relative) plus fp32 accumulation
+    tol = 1e-5 * (np.abs(y) @ np.abs(Wn)).max(axis=1)
+    safe = routing_margin_ok(lg, cfg.k, tol)
+    assert safe.sum() >= 0.9 * cfg.T
+    r_ids, _ = O.gating_topk_softmax(lg, cfg.k)
+    np.testing.assert_array_equal(to_np(ids)[safe], r_ids[safe])
+    rows = np.nonzero(safe)[0][:24]
+    ref = O.moe_forward_mx(to_np(inp["x"])[rows], to_np(inp["r"])[rows], to_np(inp["norm_w"]), cfg.eps, None,
+                           LazyExperts(inp["w13"]), LazyExperts(inp["down"]), cfg.k, logits32=lg[rows])
+    assert rel_fro(to_np(out)[rows], ref["out"]) <= REL_FRO_MX

@@ -41,7 +41,8 @@ def test_gating_without_renormalisation(cuda_dev):
 # ------------------------------------------------------------------ router --
 
 @pytest.mark.parametrize("name,T", [("tiny", 16), ("qwen3_30b_a3b_decode", 32), ("qwen3_30b_a3b_decode", 300),
-                                    ("qwen3_235b_a22b_decode", 64)])
+                                    ("qwen3_235b_a22b_decode", 64), ("qwen3_30b_a3b_prefill_zipf", 4096),
+                                    ("qwen3_235b_a22b_prefill", 1000), ("tiny", 200)])
 def test_router_logits(cuda_dev, name, T):
     cfg = W.with_shape(W.CONFIGS[name], T=T)
     inp = W.make_inputs(cfg, weights=False)
@@ -144,9 +145,10 @@ def test_grouped_gemms_match_oracle(cuda_dev, T, E, k, H, I, skew):
         if hi > lo:
             _, h_ref[lo:hi] = O.expert_mlp(An[lo:hi], to_np(w13[e]), to_np(down[e]), return_h=True)
     assert_close_layer(to_np(h), h_ref, rel=5e-3, max_abs_frac=1e-2, what="h")
-    # down projection on the GPU's own h (bf16), vs the oracle product of that h
-    y = moe.grouped_matmul(h, downp, off, E, H)
-    hn = to_np(h).astype(np.float64)
+    # down projection on its own seeded bf16 input (no GPU output feeds the oracle)
+    A2 = torch.randn(T * k, I, generator=torch.Generator().manual_seed(T + 1)).to(torch.bfloat16)
+    y = moe.grouped_matmul(A2.to(cuda_dev), downp, off, E, H)
+    hn = to_np(A2).astype(np.float64)
     y_ref = np.zeros((T * k, H))
     for e in range(E):
         lo, hi = offs[e], offs[e + 1]

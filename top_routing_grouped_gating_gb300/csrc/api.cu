@@ -109,8 +109,7 @@ ForwardLayout forward_layout(int T, int H, int E, int k, int I) {
     return at;
   };
   const size_t P = (size_t)T * k;
-  const moe::RouterPlan rp = moe::router_plan(T, H, E);
-  L.router = take((size_t)rp.splits * T * E * sizeof(float));
+  L.router = take(moe::router_ws_bytes(T, H, E, false));
   L.ids = take(P * sizeof(int32_t));
   L.w = take(P * sizeof(float));
   L.routing = take(moe::routing_ws_bytes((int)P, E));
@@ -210,8 +209,8 @@ moe_status moe_clear_device_status(moe_stream_t stream) {
 // ------------------------------------------------------------------ router --
 size_t moe_router_logits_workspace_size(int T, int H, int E) {
   if (T < 1 || H < 1 || E < 1) return 0;
-  const moe::RouterPlan rp = moe::router_plan(T, H, E);
-  return rp.splits > 1 ? align256((size_t)rp.splits * T * E * sizeof(float)) : 0;
+  const moe::RouterPlan rp = moe::router_plan_ex(T, H, E, false);
+  return (rp.splits > 1 || rp.tc) ? moe::router_ws_bytes(T, H, E, false) : 0;
 }
 
 moe_status moe_router_logits(const moe_bf16* x, const float* Wg, int T, int H, int E,
@@ -220,13 +219,19 @@ moe_status moe_router_logits(const moe_bf16* x, const float* Wg, int T, int H, i
   if (T < 1 || E < 1 || E > 256 || H < 32 || H % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   DeviceFacts* d = nullptr;
   MOE_TRY(current_device(&d));
-  const moe::RouterPlan rp = moe::router_plan(T, H, E);
-  if (rp.splits > 1) {
+  const moe::RouterPlan rp = moe::router_plan_ex(T, H, E, false);
+  if (rp.splits > 1 || rp.tc) {
     if (ws == nullptr || ws_bytes < moe_router_logits_workspace_size(T, H, E) ||
         (reinterpret_cast<uintptr_t>(ws) & 255u))
       return MOE_ERR_WORKSPACE;
     float* partial = static_cast<float*>(ws);
-    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, partial, nullptr, stream));
+    if (rp.tc) {
+      void* extra = at<uint8_t>(ws, align256((size_t)rp.splits * T * E * sizeof(float)));
+      MOE_CUDA(moe::launch_router_tc(x, false, Wg, T, H, E, rp, partial, extra, nullptr,
+                                     d->status, stream));
+    } else {
+      MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, partial, nullptr, stream));
+    }
     MOE_CUDA(moe::launch_router_reduce(partial, rp.splits, T, E, logits, stream));
   } else {
     MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, logits, nullptr, stream));
@@ -327,7 +332,7 @@ static moe_status grouped_common(const moe_bf16* A, const void* w, const int32_t
   ph.K = K;
   ph.MW = swiglu ? 2 * N : N;
   ph.n_out = N;
-  ph.swiglu = swiglu ? 1 : 0;
+  ph.epi = swiglu ? 0 : 1;
   MOE_CUDA(moe::launch_grouped_gemm(swiglu ? &ph : nullptr, swiglu ? nullptr : &ph, offsets, E, P,
                                     P, nullptr, d->status, stream));
   return MOE_OK;
@@ -408,10 +413,16 @@ moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_o
     if (fused_routing) MOE_CUDA(cudaMemsetAsync(fr.counter, 0, sizeof(int), stream));
     MOE_CUDA(moe::launch_gating(logits_override, 1, T, E, k, 1, ids, w, fuse, d->status, stream));
   } else {
-    const moe::RouterPlan rp = moe::router_plan(T, H, E);
+    const moe::RouterPlan rp = moe::router_plan_ex(T, H, E, false);
     float* part = at<float>(ws, L.router);
-    MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, part, fused_routing ? fr.counter : nullptr,
-                                stream));
+    int* zw = fused_routing ? fr.counter : nullptr;
+    if (rp.tc) {
+      void* extra = at<uint8_t>(ws, L.router + align256((size_t)rp.splits * T * E * sizeof(float)));
+      MOE_CUDA(moe::launch_router_tc(x, false, Wg, T, H, E, rp, part, extra, zw, d->status,
+                                     stream));
+    } else {
+      MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, part, zw, stream));
+    }
     MOE_CUDA(moe::launch_gating(part, rp.splits, T, E, k, 1, ids, w, fuse, d->status, stream));
   }
   if (!fused_routing)
@@ -425,14 +436,14 @@ moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_o
   g1.K = H;
   g1.MW = 2 * I;
   g1.n_out = I;
-  g1.swiglu = 1;
+  g1.epi = 0;
   g2.A_weights = down_packed;
   g2.B_act = h;
   g2.out = y2;
   g2.K = I;
   g2.MW = H;
   g2.n_out = H;
-  g2.swiglu = 0;
+  g2.epi = 1;
   if (t_gemm_ev_begin) MOE_CUDA(cudaEventRecord(t_gemm_ev_begin, stream));
   MOE_CUDA(moe::launch_grouped_gemm(&g1, &g2, offsets, E, P, T, done, d->status, stream));
   if (t_gemm_ev_end) MOE_CUDA(cudaEventRecord(t_gemm_ev_end, stream));
@@ -514,11 +525,10 @@ ForwardMxLayout forward_mx_layout(int T, int H, int E, int k, int I) {
   const size_t P = (size_t)T * k;
   const size_t R = ((P + 127) / 128) * 128 + 128 * (size_t)E;  // rows after 128-row padding
   L.pad_rows = (int)R;
-  const moe::RouterPlan rp = moe::router_plan(T, H, E);
   L.y32 = take((size_t)T * H * 4);
   L.xq = take((size_t)T * H);
   L.xs = take((size_t)T * H / 32);
-  L.router = take((size_t)rp.splits * T * E * sizeof(float));
+  L.router = take(moe::router_ws_bytes(T, H, E, true));
   L.ids = take(P * 4);
   L.w = take(P * 4);
   L.routing = take(moe::routing_ws_bytes((int)P, E));
@@ -596,10 +606,16 @@ moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
     if (fused_routing) MOE_CUDA(cudaMemsetAsync(fr.counter, 0, sizeof(int), stream));
     MOE_CUDA(moe::launch_gating(logits_override, 1, T, E, k, 1, ids, w, fuse, d->status, stream));
   } else {
-    const moe::RouterPlan rp = moe::router_plan(T, H, E);
+    const moe::RouterPlan rp = moe::router_plan_ex(T, H, E, true);
     float* part = at<float>(ws, L.router);
-    MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, E, rp, part,
-                                    fused_routing ? fr.counter : nullptr, stream));
+    int* zw = fused_routing ? fr.counter : nullptr;
+    if (rp.tc) {
+      void* extra = at<uint8_t>(ws, L.router + align256((size_t)rp.splits * T * E * sizeof(float)));
+      MOE_CUDA(moe::launch_router_tc(y32, true, Wg, T, H, E, rp, part, extra, zw, d->status,
+                                     stream));
+    } else {
+      MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, E, rp, part, zw, stream));
+    }
     MOE_CUDA(moe::launch_gating(part, rp.splits, T, E, k, 1, ids, w, fuse, d->status, stream));
   }
   if (!fused_routing)

@@ -49,10 +49,16 @@ struct GemmArgs {
   int K[2];
   int MW[2];
   int ld[2];
-  int swiglu[2];
+  int epi[2];       // 0: SwiGLU -> bf16, 1: bf16, 2: fp32 split-K partials
   int active[2];
+  int ksplit[2];    // units per (expert, weight block, token block) along K
+  int bseg[2];      // > 0: B's K coordinate = piece(k / bseg) * bseg + k % bseg
+  uint32_t bmap[2]; // 3 bits per K segment: the piece of B it reads
+  int mvalid[2];    // epi 2: valid weight rows (columns of the partial)
+  int rows_total[2];// epi 2: rows of one partial slab
   uint16_t* out[2];
-  int* done;      // per-expert count of finished phase-0 units, or null
+  float* out_f32[2];
+  int* done;        // per-expert count of finished phase-0 units, or null
   int* status;
 };
 
@@ -73,12 +79,13 @@ struct Layout {
 };
 
 struct Unit {
-  int ph, e, mb, row0, rows;
+  int ph, e, mb, ks, row0, rows;
 };
 
 struct Tables {
   const int* off;
   const int* uoff[2];
+  int ksplit[2];
   int E;
 };
 
@@ -96,11 +103,14 @@ __device__ __forceinline__ Unit decode_unit(int u, const Tables& tb) {
     else hi = mid;
   }
   r.e = lo;
+  const int S = tb.ksplit[r.ph];
   const int local = u - uo[lo];
+  r.ks = local % S;
+  const int rest = local / S;
   const int m = tb.off[lo + 1] - tb.off[lo];
   const int nb = (m + BN - 1) / BN;
-  r.mb = local / nb;
-  const int b = local - r.mb * nb;
+  r.mb = rest / nb;
+  const int b = rest - r.mb * nb;
   r.row0 = tb.off[lo] + b * BN;
   r.rows = min(BN, tb.off[lo + 1] - r.row0);
   return r;
@@ -185,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < E) {
       const int m = s_off[tid + 1] - s_off[tid];
       const int nb = (m + BN - 1) / BN;
-      u[0] = args.active[0] ? nb * (args.MW[0] / kBM) : 0;
-      u[1] = args.active[1] ? nb * (args.MW[1] / kBM) : 0;
+      u[0] = args.active[0] ? nb * (args.MW[0] / kBM) * args.ksplit[0] : 0;
+      u[1] = args.active[1] ? nb * (args.MW[1] / kBM) * args.ksplit[1] : 0;
     }
     for (int p = 0; p < 2; ++p) {
       int inc = u[p];
@@ -214,6 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tb.off = s_off;
   tb.uoff[0] = s_uoff0;
   tb.uoff[1] = s_uoff1;
+  tb.ksplit[0] = args.ksplit[0];
+  tb.ksplit[1] = args.ksplit[1];
   tb.E = E;
   const int total = s_uoff0[E] + s_uoff1[E];
 
@@ -230,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit t = decode_unit<BN>(u, tb);
         if (t.ph == 1 && args.done != nullptr) {
           const int m = s_off[t.e + 1] - s_off[t.e];
-          const int need = ((m + BN - 1) / BN) * (args.MW[0] / kBM);
+          const int need = ((m + BN - 1) / BN) * (args.MW[0] / kBM) * args.ksplit[0];
           if (!wait_counter(args.done + t.e, need, s_abort)) {
             ok = false;
             break;
@@ -242,16 +254,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nbox = (t.rows + BOX - 1) / BOX;
         const uint32_t bytes = kABytes + nbox * L::kBoxBytes;
         const int arow = t.e * args.MW[t.ph] + t.mb * kBM;
-        const int nk = args.K[t.ph] / kBK;
-        for (int kb = 0; kb < nk; ++kb) {
+        const int nks = args.K[t.ph] / kBK / args.ksplit[t.ph];
+        const int bseg = args.bseg[t.ph];
+        const uint32_t bmap = args.bmap[t.ph];
+        for (int kb = t.ks * nks; kb < (t.ks + 1) * nks; ++kb) {
           if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
             ok = false;
             break;
           }
+          const int ka = kb * kBK;
+          int kx = ka;
+          if (bseg > 0) {
+            const int seg = ka / bseg;
+            kx = static_cast<int>((bmap >> (3 * seg)) & 7u) * bseg + (ka - seg * bseg);
+          }
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sA + stage * kABytes, ta, &full[stage], kb * kBK, arow, pol_w);
+          tma_load_2d(sA + stage * kABytes, ta, &full[stage], ka, arow, pol_w);
           for (int j = 0; j < nbox; ++j)
-            tma_load_2d(sB + stage * L::kBBytes + j * L::kBoxBytes, tbm, &full[stage], kb * kBK,
+            tma_load_2d(sB + stage * L::kBBytes + j * L::kBoxBytes, tbm, &full[stage], kx,
                         t.row0 + j * BOX, pol_x);
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (par << stage);
@@ -299,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-        const int nk = args.K[t.ph] / kBK;
+        const int nk = args.K[t.ph] / kBK / args.ksplit[t.ph];
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&full[stage], par, s_abort)) {
             ok = false;
@@ -355,7 +375,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       uint16_t* out = args.out[t.ph];
       const int ld = args.ld[t.ph];
-      if (args.swiglu[t.ph]) {
+      if (args.epi[t.ph] == 2) {
+        // fp32 split-K partial: part[ks][row][col], col = weight row of this lane
+        const int col = t.mb * kBM + q * 32 + lane;
+        float* part = args.out_f32[t.ph] + (size_t)t.ks * args.rows_total[t.ph] * ld;
+        for (int c0 = 0; c0 < t.rows; c0 += 32) {
+          float v[32];
+          tmem_ld_32x32b_x32(tbase + c0, v);
+          if (col < args.mvalid[t.ph]) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c0 + j < t.rows) part[(size_t)(t.row0 + c0 + j) * ld + col] = v[j];
+          }
+        }
+      } else if (args.epi[t.ph] == 0) {
         // Each 32-lane TMEM quarter holds 16 gate rows (lanes 0-15) and the 16
         // matching up rows (lanes 16-31).  One shuffle across the half-warps pairs
         // them: lanes 0-15 finish tokens 0-15 of the chunk, lanes 16-31 tokens 16-31,
@@ -491,12 +524,19 @@ cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_
     a.K[p] = g->K;
     a.MW[p] = g->MW;
     a.ld[p] = g->n_out;
-    a.swiglu[p] = g->swiglu;
+    a.epi[p] = g->epi;
+    a.ksplit[p] = g->ksplit > 0 ? g->ksplit : 1;
+    a.bseg[p] = g->bseg;
+    a.bmap[p] = g->bmap;
+    a.mvalid[p] = g->mvalid;
+    a.rows_total[p] = g->rows_total;
     a.out[p] = g->out;
+    a.out_f32[p] = g->out_f32;
+    const uint64_t binner = g->b_inner > 0 ? (uint64_t)g->b_inner : (uint64_t)g->K;
     if (!encode_tmap_2d_bf16(&tm[2 * p], g->A_weights, (uint64_t)g->K, (uint64_t)E * g->MW, kBK,
                              kBM))
       return cudaErrorInvalidValue;
-    if (!encode_tmap_2d_bf16(&tm[2 * p + 1], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK, BOX))
+    if (!encode_tmap_2d_bf16(&tm[2 * p + 1], g->B_act, binner, (uint64_t)P, kBK, BOX))
       return cudaErrorInvalidValue;
   }
   cudaLaunchConfig_t cfg = {};

@@ -12,11 +12,23 @@ namespace moe {
 // ---- router / gating (router_gating.cu)
 struct RouterPlan {
   bool small;      // decode-size tiles (32 tokens x 32 experts x 128 rows of H)
-  int splits;      // split-K factor over H
+  bool tc = false; // tensor-core path (bf16x3 split, router_tc.cu)
+  int splits;      // split-K factor (partials part[splits][T][E] when > 1)
   int t_tiles;     // ceil(T / 32)
   int e_tiles;     // expert tiles
+  int nseg = 0;    // tc: K segments (3: bf16 activations, 6: fp32 activations)
+  size_t extra_bytes = 0;  // tc: packed weights, offsets, split activations
 };
-RouterPlan router_plan(int T, int H, int E);
+RouterPlan router_plan(int T, int H, int E);  // CUDA-core plans only
+// The plan moe_forward uses: the tensor-core path for prefill-size T.
+RouterPlan router_plan_ex(int T, int H, int E, bool f32in);
+// Workspace of a router launch under router_plan_ex: partials + extra.
+size_t router_ws_bytes(int T, int H, int E, bool f32in);
+// Tensor-core router: x is (T,H) bf16, or fp32 when f32in.  Writes partial
+// sums part[plan.splits][T][E]; extra holds plan.extra_bytes of scratch.
+cudaError_t launch_router_tc(const void* x, bool f32in, const float* Wg, int T, int H, int E,
+                             const RouterPlan& plan, float* partial, void* extra, int* zero_word,
+                             int* status, cudaStream_t s);
 // partial[s][T][E] when splits > 1, else writes out directly.  zero_word (may be
 // null) is set to 0 by the launch (the fused gating/routing counter).
 cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
@@ -66,12 +78,19 @@ cudaError_t launch_finalize(const uint16_t* y2, const float* w, const int32_t* e
 // ---- grouped GEMM (gmm.cu)
 struct GemmPhase {
   const void* A_weights;   // packed weights, rows = E * MW, cols = K
-  const uint16_t* B_act;   // activations (P, K)
-  uint16_t* out;           // (P, n_out)
+  const uint16_t* B_act;   // activations (P, b_inner or K)
+  uint16_t* out;           // (P, n_out) bf16, epi 0 and 1
   int K;                   // reduction length
   int MW;                  // weight rows per expert (2I for gate/up, H for down)
-  int n_out;               // output columns (I for gate/up, H for down)
-  int swiglu;              // 1: SwiGLU epilogue on interleaved gate/up rows
+  int n_out;               // output columns (I for gate/up, H for down); row stride of out_f32
+  int epi;                 // 0: SwiGLU on interleaved gate/up rows, 1: plain, 2: fp32 partials
+  int ksplit = 1;          // split of K into units (epi 2)
+  int b_inner = 0;         // B's row length when it differs from K
+  int bseg = 0;            // see GemmArgs::bseg
+  uint32_t bmap = 0;
+  float* out_f32 = nullptr;// epi 2: part[ksplit][rows_total][n_out]
+  int mvalid = 0;
+  int rows_total = 0;
 };
 // phases[0] and/or phases[1] (null A_weights = phase absent).  When both are
 // present they run in one persistent launch with a per-expert dependency on

@@ -106,7 +106,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   const int t = sri[p] / k;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   uint4* dst = reinterpret_cast<uint4*>(xe + (size_t)p * H);
-  for (int v = lane; v < H / 8; v += 32) dst[v] = src[v];
+  const int nv = H / 8;
+  int v = lane;
+  for (; v + 96 < nv; v += 128) {  // four independent 16-byte loads in flight per lane
+    const uint4 a = src[v], b = src[v + 32], c = src[v + 64], d = src[v + 96];
+    dst[v] = a;
+    dst[v + 32] = b;
+    dst[v + 64] = c;
+    dst[v + 96] = d;
+  }
+  for (; v < nv; v += 32) dst[v] = src[v];
 }
 
 __global__ void __launch_bounds__(kRouteThreads) expert_tokens_kernel(
