@@ -327,6 +327,10 @@ def run_ours(args, cfg):
     torch.cuda.synchronize(dev)
     counts = torch.bincount(ids.flatten().long(), minlength=cfg.E)
     active = int((counts > 0).sum())
+    if args.no_cpu_baseline:
+        # the packed copies are all the layer uses; drop the logical weights
+        del inp["w13"], inp["down"]
+        torch.cuda.empty_cache()
 
     def barrier():
         rank_barrier(ws)

@@ -232,7 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer --
-      const uint64_t pol_w = l2_policy_evict_first();
+      // weights: read once per unit in the thin-tile (decode) variant, so stream
+      // them past L2; wide token tiles re-read a weight tile for every token block
+      // of its expert, so keep them cacheable
+      const uint64_t pol_w = BN <= 32 ? l2_policy_evict_first() : l2_policy_evict_normal();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t par = 0;
@@ -562,7 +565,7 @@ cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
   // Thin token tiles when the mean expert load is small (decode), wide ones else.
   if ((long long)P <= 16LL * E)
     return launch_impl<32, 10, 16>(ph0, ph1, offsets, E, P, done_counter, status, s);
-  return launch_impl<256, 4, 64>(ph0, ph1, offsets, E, P, done_counter, status, s);
+  return launch_impl<256, 4, 128>(ph0, ph1, offsets, E, P, done_counter, status, s);
 }
 
 cudaError_t launch_pack_w13(const uint16_t* w13, int E, int H, int I, uint16_t* out,

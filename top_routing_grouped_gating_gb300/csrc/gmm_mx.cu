@@ -31,15 +31,15 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kBK = 128;                          // fp8 elements per stage (128 bytes)
-constexpr int kBoxRows = 64;
+constexpr int kBoxRows = 128;
 constexpr int kThreads = 256;
 constexpr int kMaxE = 256;
 constexpr int kStages = 6;
 constexpr int kABytes = kBM * kBK;                // 16 KB
 constexpr int kBBytes = kBN * kBK;                // 16 KB
-constexpr int kBoxBytes = kBoxRows * kBK;         // 8 KB
+constexpr int kBoxBytes = kBoxRows * kBK;         // 16 KB
 constexpr int kSfBytes = 512;                     // one scale atom
-constexpr int kEpiBytes = 32 * 64 * 4 + 32 * 64 * 2 + 32 * 64;
+constexpr int kEpiBytes = (4 * 16 * 33 + 2 * 32 * 33) * 4;  // SwiGLU exchange + h tile
 constexpr int kAccCols = kBN;                     // per accumulator
 constexpr int kSfCol = 2 * kAccCols;              // first scale-factor TMEM column
 constexpr int kTmemCols = 512;
@@ -239,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer --
-      const uint64_t pol_w = l2_policy_evict_first();
+      // weight tiles are re-read by every 128-token block of their expert
+      const uint64_t pol_w = l2_policy_evict_normal();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t par = 0;
@@ -381,54 +382,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * kAccCols);
       if (t.ph == 0) {
-        // SwiGLU, then MX quantisation of h along I: lanes of a gate warp hold the
-        // 32 consecutive features of one scale block.
-        float* xbuf = reinterpret_cast<float*>(sEpi);                      // [32 tok][64] fp32
-        uint8_t* cbuf = sEpi + 32 * 64 * 4 + 32 * 64 * 2;                  // [32 tok][64] codes
+        // SwiGLU, then MX quantisation of h along I.  Warps q and q+2 hold the gate
+        // and up rows of the same 32 features (one scale block, p = q & 1).  The pair
+        // swaps half a chunk through shared memory, so the gate warp finishes tokens
+        // 0-15 and the up warp tokens 16-31; h goes to a padded [token][feature]
+        // tile, and two lanes per token then quantise 16 features each (block
+        // maximum by one shuffle).
+        float* xb = reinterpret_cast<float*>(sEpi);          // [4 warps][16 tok][33]
+        float* hb = xb + 4 * 16 * 33;                        // [2 blocks][32 tok][33]
         const int ld = args.ld[0];
         const int ksteps = ld / 128;
         const int ks = t.mb / 2;                 // 128-feature step of the down projection
-        const int kbq = (t.mb & 1) * 2 + q;      // this warp's 32-feature block in that step
+        const int pblk = q & 1;                  // feature block of this warp pair
+        const int kbq = (t.mb & 1) * 2 + pblk;   // its 32-feature block within step ks
+        const bool gate = q < 2;
+        const uint32_t bar_id = 2 + pblk;
+        float* mine = xb + q * 16 * 33;
+        const float* other = xb + (q ^ 2) * 16 * 33;
+        float* hrow = hb + pblk * 32 * 33;
         for (int c0 = 0; c0 < t.rows; c0 += 32) {
           float v[32];
           tmem_ld_32x32b_x32(tbase + c0, v);
-          if (q >= 2) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) xbuf[j * 64 + (q - 2) * 32 + lane] = v[j];
+          for (int j = 0; j < 16; ++j) mine[j * 33 + lane] = gate ? v[16 + j] : v[j];
+          named_bar_sync(bar_id, 64);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g = gate ? v[j] : other[j * 33 + lane];
+            const float up = gate ? other[j * 33 + lane] : v[16 + j];
+            hrow[((gate ? 0 : 16) + j) * 33 + lane] = g / (1.0f + __expf(-g)) * up;
           }
-          named_bar_sync(1, 128);
-          if (q < 2) {
-            int myX = -127;
+          named_bar_sync(bar_id, 64);
+          const int tok = (gate ? 0 : 16) + (lane >> 1);
+          const int half = lane & 1;
+          float hv[16];
+          float amax = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float g = v[j];
-              const float up = xbuf[j * 64 + q * 32 + lane];
-              const float h = g / (1.0f + __expf(-g)) * up;
-              float amax = fabsf(h);
+          for (int i = 0; i < 16; ++i) {
+            hv[i] = hrow[tok * 33 + 16 * half + i];
+            amax = fmaxf(amax, fabsf(hv[i]));
+          }
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          const int X = mx_exponent(amax);
+          uint32_t w[4];
 #pragma unroll
-              for (int o = 16; o > 0; o >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-              const int X = mx_exponent(amax);
-              if (lane == j) myX = X;
-              cbuf[j * 64 + q * 32 + lane] = mx_code(h, X);
-            }
-            const int prow = t.row0 + c0 + lane;
-            if (c0 + lane < t.rows) {
+          for (int i = 0; i < 4; ++i)
+            w[i] = static_cast<uint32_t>(mx_code(hv[4 * i], X)) |
+                   (static_cast<uint32_t>(mx_code(hv[4 * i + 1], X)) << 8) |
+                   (static_cast<uint32_t>(mx_code(hv[4 * i + 2], X)) << 16) |
+                   (static_cast<uint32_t>(mx_code(hv[4 * i + 3], X)) << 24);
+          if (c0 + tok < t.rows) {
+            const int prow = t.row0 + c0 + tok;
+            *reinterpret_cast<uint4*>(args.hq + (size_t)prow * ld + t.mb * 64 + 32 * pblk +
+                                      16 * half) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (half == 0) {
               uint8_t* atom = args.h_sf + ((size_t)(prow / 128) * ksteps + ks) * kSfBytes;
-              atom[(prow & 31) * 16 + ((prow >> 5) & 3) * 4 + kbq] =
-                  static_cast<uint8_t>(myX + 127);
+              atom[(prow & 31) * 16 + ((prow >> 5) & 3) * 4 + kbq] = static_cast<uint8_t>(X + 127);
             }
           }
-          named_bar_sync(1, 128);
-          {
-            const int j = et >> 2, c = et & 3;   // 32 rows x 4 vectors of 16 codes
-            if (c0 + j < t.rows) {
-              const uint4 val = *reinterpret_cast<const uint4*>(cbuf + j * 64 + c * 16);
-              *reinterpret_cast<uint4*>(args.hq + (size_t)(t.row0 + c0 + j) * ld + t.mb * 64 +
-                                        c * 16) = val;
-            }
-          }
-          named_bar_sync(1, 128);
+          named_bar_sync(bar_id, 64);
         }
       } else {
         uint16_t* tbw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 32;
