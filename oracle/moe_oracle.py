@@ -442,3 +442,134 @@ def brute_force_topk(logits_row: np.ndarray, k: int) -> np.ndarray:
             ordered = sorted(members, key=lambda a: sum(beats(b, a) for b in members))
             return np.array(ordered, np.int64)
     raise AssertionError("no top-k subset found")
+
+
+# --------------------------------------------------------------------------- #
+# Next rows: fused add + RMSNorm + cast, EP-local routing, re-routing,         #
+# zero-computation experts                                                     #
+# --------------------------------------------------------------------------- #
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bfloat16 (nearest, ties to even) and return them as fp64:
+    keep the top 16 bits of the fp32 pattern after adding 0x7FFF + lsb."""
+    f = np.asarray(v, np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def add_rmsnorm_cast(x: np.ndarray, r: Optional[np.ndarray], w: np.ndarray, eps: float):
+    """[Q3MoE §融合RMSNorm Cast] residual add + RMSNorm with two outputs: the
+    normalised activations in FP32 for the gate (router) and in BF16 for the
+    experts.  Returns (s, y fp64, y_bf16 as fp64 values); the bf16 output is the
+    rounding of the fp32 value of y."""
+    s, y = add_rmsnorm(x, r, w, eps)
+    return s, y, bf16_round(y.astype(np.float32))
+
+
+def init_routing_v2(topk_ids: np.ndarray, E_total: int, expert_begin: int, expert_end: int):
+    """Expert-range routing [Q3MoE §计算分解(AllGather方案): init_routing_v2 keeps only
+    the tokens whose expert lies in this rank's range].  Pairs whose id is in
+    [expert_begin, expert_end) are sorted stably by local id (id - expert_begin);
+    the others get expanded_row_idx = -1 (another rank's expert, or a zero-computation
+    expert).  Ids outside [0, E_total) are invalid and also get -1."""
+    flat = np.asarray(topk_ids).reshape(-1)
+    El = expert_end - expert_begin
+    local = np.where((flat >= expert_begin) & (flat < expert_end), flat - expert_begin, -1)
+    counts = np.zeros(El, np.int64)
+    for e in local:
+        if e >= 0:
+            counts[e] += 1
+    offsets = np.zeros(El + 1, np.int64)
+    for e in range(El):
+        offsets[e + 1] = offsets[e] + counts[e]
+    seen = np.zeros(El, np.int64)
+    P = flat.shape[0]
+    eri = np.full(P, -1, np.int32)
+    sri = np.full(P, -1, np.int32)
+    for j in range(P):
+        e = int(local[j])
+        if e < 0:
+            continue
+        p = int(offsets[e] + seen[e])
+        seen[e] += 1
+        eri[j] = p
+        sri[p] = j
+    return dict(counts=counts.astype(np.int32), offsets=offsets.astype(np.int32),
+                expanded_row_idx=eri, sorted_row_idx=sri)
+
+
+def re_routing(tokens_per_expert: np.ndarray):
+    """[Q3MoE §计算分解(Double Routing方案): npu_moe_re_routing re-sorts the tokens received
+    by the AlltoAll by local expert].  Received rows arrive grouped by source rank and,
+    inside a rank's block, by local expert: counts[r][e] rows for (r, e), in that
+    order.  Re-routing orders them by expert, then source rank (stable).  Returns
+    (perm, expert_offsets): received row i goes to output row perm[i]."""
+    cnt = np.asarray(tokens_per_expert, np.int64)
+    R, El = cnt.shape
+    out_base = np.zeros((R, El), np.int64)
+    acc = 0
+    for e in range(El):
+        for r in range(R):
+            out_base[r, e] = acc
+            acc += cnt[r, e]
+    perm = np.empty(acc, np.int64)
+    i = 0
+    for r in range(R):
+        for e in range(El):
+            for q in range(cnt[r, e]):
+                perm[i] = out_base[r, e] + q
+                i += 1
+    offsets = np.zeros(El + 1, np.int64)
+    for e in range(El):
+        offsets[e + 1] = offsets[e] + cnt[:, e].sum()
+    return perm.astype(np.int32), offsets.astype(np.int32)
+
+
+def moe_forward_v2(x: np.ndarray, r: Optional[np.ndarray], norm_w: Optional[np.ndarray], eps: float,
+                   Wg: np.ndarray, w13, down, k: int, num_zero_experts: int = 0,
+                   logits32: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """The bf16 layer with the optional fused add+RMSNorm+cast in front and optional
+    zero-computation experts.
+
+    * With norm_w: s = x + r, y = RMSNorm(s); the router sees fp32 y, the experts
+      bf16(y) [Q3MoE §融合RMSNorm Cast]; without, the experts and router see x.
+    * Router scores cover E routed + Z zero-computation experts (ids E..E+Z-1).  A
+      zero-computation expert returns its input unchanged, MoE(x) = x (page
+      "基于Atlas A3集群的LongCat-Flash模型推理性能优化实践", §MoE模块实现Expert
+      Parallel, copy_expert_num), so it adds w * (expert input) to the output.
+    """
+    E = len(w13)
+    if norm_w is not None:
+        s, y, ybf = add_rmsnorm_cast(x, r, norm_w, eps)
+        router_in, expert_in = y, ybf
+    else:
+        s = None
+        router_in = expert_in = np.asarray(x, np.float64)
+    if logits32 is None:
+        logits32 = router_logits_f32(router_in, Wg)
+    ids, w = gating_topk_softmax(logits32, k)
+    rt = init_routing_v2(ids, E + num_zero_experts, 0, E)
+    T, H = expert_in.shape
+    offs, sri, eri = rt["offsets"], rt["sorted_row_idx"], rt["expanded_row_idx"]
+    y_all = np.zeros((T * k, H), np.float64)
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi > lo:
+            y_all[lo:hi] = expert_mlp(expert_in[sri[lo:hi] // k], w13[e], down[e])
+    out = np.zeros((T, H), np.float64)
+    for t in range(T):
+        for sl in range(k):
+            j = t * k + sl
+            if ids[t, sl] < E:
+                out[t] += w[t, sl] * y_all[eri[j]]
+            else:
+                out[t] += w[t, sl] * expert_in[t]
+    res = dict(logits32=np.asarray(logits32, np.float32), topk_ids=ids, topk_w=w, out=out, **rt)
+    if s is not None:
+        res["residual"] = s
+        res["y"] = router_in
+        res["y_bf16"] = expert_in
+    return res

@@ -357,3 +357,82 @@ def test_mutation_mx_off_by_one_exponent_is_caught(golden):
     _, ex = np.frexp(amax)
     wrong = int(ex[0]) - 8 + 127       # forgets the -1 of frexp
     assert wrong != c["scale_byte"]
+
+
+# ------------------------------------------------------------ next rows --
+
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(4)
+    v = np.concatenate([rng.standard_normal(50000) * 10.0 ** rng.integers(-20, 20, 50000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875]]).astype(np.float32)
+    ref = torch.tensor(v).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.bf16_round(v), ref)
+
+
+def test_add_rmsnorm_cast_outputs():
+    rng = np.random.default_rng(1)
+    x, r = rng.standard_normal((4, 64)), rng.standard_normal((4, 64))
+    w = 1 + 0.1 * rng.standard_normal(64)
+    s, y, yb = O.add_rmsnorm_cast(x, r, w, 1e-6)
+    _, y2 = O.add_rmsnorm(x, r, w, 1e-6)
+    np.testing.assert_array_equal(y, y2)
+    ref = torch.tensor(y.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(yb, ref)
+
+
+def test_init_routing_v2_full_range_is_init_routing():
+    ids = W.make_topk_ids(50, 16, 4, seed=3).numpy()
+    a = O.init_routing(ids, 16)
+    b = O.init_routing_v2(ids, 16, 0, 16)
+    for key in ("counts", "offsets", "expanded_row_idx", "sorted_row_idx"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_init_routing_v2_expert_range():
+    ids = W.make_topk_ids(80, 32, 4, seed=9).numpy()
+    b = O.init_routing_v2(ids, 32, 8, 16)
+    flat = ids.reshape(-1)
+    keep = (flat >= 8) & (flat < 16)
+    np.testing.assert_array_equal(b["counts"], np.bincount(flat[keep] - 8, minlength=8))
+    order = np.nonzero(keep)[0][np.argsort(flat[keep], kind="stable")]
+    n = int(keep.sum())
+    np.testing.assert_array_equal(b["sorted_row_idx"][:n], order)
+    assert np.all(b["expanded_row_idx"][~keep] == -1)
+    np.testing.assert_array_equal(b["expanded_row_idx"][order], np.arange(n))
+
+
+def test_re_routing_is_stable_sort_by_expert():
+    rng = np.random.default_rng(2)
+    cnt = rng.integers(0, 5, size=(4, 6))
+    perm, offs = O.re_routing(cnt)
+    labels = np.concatenate([np.full(cnt[r, e], e) for r in range(4) for e in range(6)])
+    order = np.argsort(labels, kind="stable")          # output row -> received row
+    np.testing.assert_array_equal(perm[order], np.arange(len(labels)))
+    np.testing.assert_array_equal(offs, np.concatenate([[0], np.cumsum(cnt.sum(0))]))
+
+
+def test_zero_experts_only_gives_identity_and_none_gives_v1():
+    x, Wg, w13, down, k = tiny_layer(T=7, E=4, k=2)
+    Z = 3
+    Wz = np.concatenate([Wg, np.full((Wg.shape[0], Z), 0.0)], axis=1)
+    lg = np.full((7, 4 + Z), -50.0, np.float32)
+    lg[:, 4:] = [[1.0, 2.0, 0.5]] * 7                  # top-2 are zero-computation experts
+    res = O.moe_forward_v2(x, None, None, 0.0, Wz, w13, down, k, num_zero_experts=Z, logits32=lg)
+    np.testing.assert_allclose(res["out"], x, rtol=1e-12, atol=1e-12)   # weights sum to 1
+    base = O.moe_forward(x, Wg, w13, down, k)["out"]
+    v2 = O.moe_forward_v2(x, None, None, 0.0, Wg, w13, down, k)["out"]
+    np.testing.assert_allclose(v2, base, rtol=1e-13, atol=1e-13)
+
+
+def test_prenorm_layer_is_norm_then_layer():
+    x, Wg, w13, down, k = tiny_layer(T=6, seed=11)
+    rng = np.random.default_rng(0)
+    r = rng.standard_normal(x.shape)
+    nw = 1 + 0.1 * rng.standard_normal(x.shape[1])
+    res = O.moe_forward_v2(x, r, nw, 1e-6, Wg, w13, down, k)
+    _, y, yb = O.add_rmsnorm_cast(x, r, nw, 1e-6)
+    lg = O.router_logits_f32(y, Wg)
+    ids, w = O.gating_topk_softmax(lg, k)
+    ref = O.dense_moe_reference(yb, w13, down, ids, w)
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-11, atol=1e-12)
