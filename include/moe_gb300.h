@@ -248,6 +248,71 @@ MOE_API moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const mo
                                   float* topk_w_out, void* ws, size_t ws_bytes,
                                   moe_stream_t stream);
 
+/* ------------------------------------------------------------- next rows --
+ * §融合RMSNorm Cast: residual add + RMSNorm with two outputs, FP32 for the gate
+ * (router) and BF16 for the experts.  s = x + r; residual_out = bf16(s);
+ * y = s * rsqrt(mean(s^2) + eps) * w; y32_out = y (fp32, may be NULL);
+ * ybf16_out = bf16(y).  x, r (T,H) bf16 (r may be NULL); w (H) bf16.  H % 256 == 0.
+ */
+MOE_API moe_status moe_add_rmsnorm_cast(const moe_bf16* x, const moe_bf16* r, const moe_bf16* w,
+                                        float eps, int T, int H, moe_bf16* residual_out,
+                                        float* y32_out, moe_bf16* ybf16_out, moe_stream_t stream);
+
+/* Expert-range routing (the page's init_routing_v2 of §计算分解 AllGather方案, which
+ * keeps only this rank's experts): pairs whose id lies in [expert_begin, expert_end)
+ * are sorted stably by local id (id - expert_begin), exactly as moe_init_routing;
+ * pairs with another valid id in [0, E_total) (another rank's expert, or a
+ * zero-computation expert) get expanded_row_idx = -1 without an error; ids outside
+ * [0, E_total) also get -1 and set MOE_DEV_BAD_EXPERT_ID.  Arrays are sized for the
+ * local experts: counts (E_local), expert_offsets (E_local+1); sorted_row_idx has
+ * expert_offsets[E_local] valid entries.  E_local = expert_end - expert_begin <= 256. */
+MOE_API size_t moe_init_routing_v2_workspace_size(int T, int E_local, int k);
+MOE_API moe_status moe_init_routing_v2(const moe_bf16* x, const int32_t* topk_ids, int T, int H,
+                                       int k, int E_total, int expert_begin, int expert_end,
+                                       moe_bf16* expanded_x, int32_t* expanded_row_idx,
+                                       int32_t* sorted_row_idx, int32_t* expert_offsets,
+                                       int32_t* counts, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream);
+
+/* Re-routing after an expert-parallel AlltoAll (§计算分解 Double Routing方案,
+ * npu_moe_re_routing): the N received rows arrive grouped by source rank r and,
+ * within a rank, by local expert e (tokens_per_expert[r][e] rows each, int32 (R,
+ * E_local), device).  They are reordered expert-major, then by rank (stable).
+ * x_out[perm[i]] = x_recv[i]; expert_offsets (E_local+1) of the output.  x_recv and
+ * x_out may be NULL (only perm and offsets).  H % 8 == 0. */
+MOE_API size_t moe_re_routing_workspace_size(int R, int E_local);
+MOE_API moe_status moe_re_routing(const moe_bf16* x_recv, const int32_t* tokens_per_expert, int R,
+                                  int E_local, int N, int H, moe_bf16* x_out, int32_t* perm,
+                                  int32_t* expert_offsets, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/* finalize_routing with zero-computation experts (page "基于Atlas A3集群的LongCat-
+ * Flash模型推理性能优化实践", §MoE模块实现Expert Parallel: copy_expert_num,
+ * MoE(ori_x) = ori_x): pair j adds w * y2[expanded_row_idx[j]] when that row is
+ * >= 0, else w * x_in[t] when topk_ids[j] lies in [E, E_total) (a zero-computation
+ * expert returns its input), else nothing.  topk_ids (T,k) and x_in (T,H) bf16. */
+MOE_API moe_status moe_finalize_routing_v2(const moe_bf16* y2, const float* topk_w,
+                                           const int32_t* expanded_row_idx,
+                                           const int32_t* topk_ids, const moe_bf16* x_in, int T,
+                                           int k, int H, int E, int E_total, moe_bf16* out,
+                                           moe_stream_t stream);
+
+/* The bf16 layer with the optional fused add+RMSNorm+cast in front and optional
+ * zero-computation experts.  norm_w NULL: no norm (x feeds router and experts, r
+ * and residual_out unused).  norm_w given: s = x + r, y = RMSNorm(s); the router
+ * runs on fp32 y and the experts on bf16(y); residual_out = bf16(s) (may be NULL).
+ * Wg (H, E+Z) fp32 scores E routed experts then Z zero-computation experts; top-k
+ * is taken over all E+Z; zero-computation experts add w * (their input).
+ * logits_override (T, E+Z) or NULL.  E + Z <= 256. */
+MOE_API size_t moe_forward_v2_workspace_size(int T, int H, int E, int Z, int k, int I);
+MOE_API moe_status moe_forward_v2(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w,
+                                  float eps, const float* Wg, const float* logits_override,
+                                  const void* w13_packed, const void* down_packed, int T, int H,
+                                  int E, int Z, int k, int I, moe_bf16* out,
+                                  moe_bf16* residual_out, int32_t* topk_ids_out,
+                                  float* topk_w_out, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
 /* ------------------------------------------------ allocation-free routing --
  * No counterpart in the pages: an extra entry point for callers that cannot
  * allocate device memory -- code living inside a host framework that owns all

@@ -12,6 +12,11 @@ from ._binding import (  # noqa: F401
     MoEError,
     MoELayer,
     MoELayerMX,
+    MoELayerV2,
+    add_rmsnorm_cast,
+    finalize_routing_v2,
+    init_routing_v2,
+    re_routing,
     add_rmsnorm_mxquant,
     mx_quantize,
     pack_weights_mx,

@@ -43,6 +43,17 @@ _SIGS = {
     "moe_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
                              _vp, _vp, _c_size, _vp]),
     "moe_set_gemm_events": (_c_int, [_vp, _vp]),
+    "moe_add_rmsnorm_cast": (_c_int, [_vp, _vp, _vp, _c_float, _c_int, _c_int, _vp, _vp, _vp, _vp]),
+    "moe_init_routing_v2_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
+    "moe_init_routing_v2": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp,
+                                     _vp, _vp, _c_size, _vp]),
+    "moe_re_routing_workspace_size": (_c_size, [_c_int, _c_int]),
+    "moe_re_routing": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "moe_finalize_routing_v2": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
+                                         _vp]),
+    "moe_forward_v2_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "moe_forward_v2": (_c_int, [_vp, _vp, _vp, _c_float, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                _c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_add_rmsnorm_mxquant": (_c_int, [_vp, _vp, _vp, _c_float, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp]),
     "moe_mx_quantize": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
     "moe_packed_weight_bytes_mx": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
@@ -434,6 +445,153 @@ class MoELayerMX:
                                         _ptr(self.down_q), _ptr(self.down_sf), T, H, self.E, self.k, self.I,
                                         _ptr(out), _ptr(residual_out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws),
                                         ws.numel(), _stream(dev)))
+        return out, residual_out, topk_ids, topk_w
+
+
+# ------------------------------------------------------------------- next rows
+
+
+def add_rmsnorm_cast(x: torch.Tensor, r: Optional[torch.Tensor], w: torch.Tensor, eps: float = 1e-6):
+    """Returns (residual bf16, y fp32 for the router, y bf16 for the experts)."""
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    if r is not None:
+        _need(r, "r", torch.bfloat16, dev)
+    _need(w, "w", torch.bfloat16, dev)
+    T, H = x.shape
+    with torch.cuda.device(dev):
+        res = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        y32 = torch.empty(T, H, dtype=torch.float32, device=dev)
+        ybf = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        _check("moe_add_rmsnorm_cast",
+               lib().moe_add_rmsnorm_cast(_ptr(x), _ptr(r), _ptr(w), float(eps), T, H, _ptr(res), _ptr(y32),
+                                          _ptr(ybf), _stream(dev)))
+    return res, y32, ybf
+
+
+def init_routing_v2(topk_ids: torch.Tensor, E_total: int, expert_begin: int, expert_end: int,
+                    x: Optional[torch.Tensor] = None):
+    """Routing of the experts [expert_begin, expert_end) only (other ids skipped)."""
+    _need(topk_ids, "topk_ids", torch.int32)
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    H = 0
+    if x is not None:
+        _need(x, "x", torch.bfloat16, dev)
+        H = x.shape[1]
+    El = expert_end - expert_begin
+    P = T * k
+    L = lib()
+    with torch.cuda.device(dev):
+        eri = torch.empty(P, dtype=torch.int32, device=dev)
+        sri = torch.full((P,), -1, dtype=torch.int32, device=dev)
+        off = torch.empty(El + 1, dtype=torch.int32, device=dev)
+        cnt = torch.empty(El, dtype=torch.int32, device=dev)
+        xe = torch.empty(P, H, dtype=torch.bfloat16, device=dev) if x is not None else None
+        ws = _ws(L.moe_init_routing_v2_workspace_size(T, El, k), dev)
+        _check("moe_init_routing_v2",
+               L.moe_init_routing_v2(_ptr(x), _ptr(topk_ids), T, H, k, E_total, expert_begin, expert_end, _ptr(xe),
+                                     _ptr(eri), _ptr(sri), _ptr(off), _ptr(cnt), _ptr(ws), ws.numel(),
+                                     _stream(dev)))
+    res = dict(expanded_row_idx=eri, sorted_row_idx=sri, expert_offsets=off, counts=cnt)
+    if xe is not None:
+        res["expanded_x"] = xe
+    return res
+
+
+def re_routing(tokens_per_expert: torch.Tensor, x_recv: Optional[torch.Tensor] = None, N: Optional[int] = None):
+    """Reorder AlltoAll-received rows (rank-major, then local expert) expert-major.
+    Returns (x_out or None, perm, expert_offsets)."""
+    _need(tokens_per_expert, "tokens_per_expert", torch.int32)
+    R, El = tokens_per_expert.shape
+    dev = tokens_per_expert.device
+    if N is None:
+        N = int(tokens_per_expert.sum().item())
+    H = 0
+    if x_recv is not None:
+        _need(x_recv, "x_recv", torch.bfloat16, dev)
+        H = x_recv.shape[1]
+    L = lib()
+    with torch.cuda.device(dev):
+        perm = torch.empty(max(N, 1), dtype=torch.int32, device=dev)
+        off = torch.empty(El + 1, dtype=torch.int32, device=dev)
+        xo = torch.empty(N, H, dtype=torch.bfloat16, device=dev) if x_recv is not None else None
+        ws = _ws(L.moe_re_routing_workspace_size(R, El), dev)
+        _check("moe_re_routing",
+               L.moe_re_routing(_ptr(x_recv), _ptr(tokens_per_expert), R, El, N, H, _ptr(xo), _ptr(perm), _ptr(off),
+                                _ptr(ws), ws.numel(), _stream(dev)))
+    return xo, perm[:N], off
+
+
+def finalize_routing_v2(y2: torch.Tensor, topk_w: torch.Tensor, expanded_row_idx: torch.Tensor,
+                        topk_ids: torch.Tensor, x_in: torch.Tensor, E: int, E_total: int) -> torch.Tensor:
+    _need(y2, "y2", torch.bfloat16)
+    dev = y2.device
+    _need(topk_w, "topk_w", torch.float32, dev)
+    _need(expanded_row_idx, "expanded_row_idx", torch.int32, dev)
+    _need(topk_ids, "topk_ids", torch.int32, dev)
+    _need(x_in, "x_in", torch.bfloat16, dev)
+    T, k = topk_w.shape
+    H = x_in.shape[1]
+    with torch.cuda.device(dev):
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        _check("moe_finalize_routing_v2",
+               lib().moe_finalize_routing_v2(_ptr(y2), _ptr(topk_w), _ptr(expanded_row_idx), _ptr(topk_ids),
+                                             _ptr(x_in), T, k, H, E, E_total, _ptr(out), _stream(dev)))
+    return out
+
+
+class MoELayerV2:
+    """bf16 MoE layer with the optional fused add+RMSNorm+cast in front (norm_w) and
+    optional zero-computation experts (Wg has E + Z columns; the last Z are identity
+    experts)."""
+
+    def __init__(self, Wg: torch.Tensor, w13: torch.Tensor, down: torch.Tensor, k: int, Z: int = 0,
+                 norm_w: Optional[torch.Tensor] = None, eps: float = 1e-6):
+        self.E, self.H, I2 = w13.shape
+        self.I = I2 // 2
+        self.k, self.Z, self.eps = k, Z, float(eps)
+        if Wg.shape[1] != self.E + Z:
+            raise ValueError("Wg must have E + Z columns")
+        self.Wg = Wg.contiguous()
+        self.norm_w = None if norm_w is None else norm_w.contiguous()
+        self.w13_packed, self.down_packed = pack_weights(w13.contiguous(), down.contiguous())
+        self._ws = None
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = int(lib().moe_forward_v2_workspace_size(T, self.H, self.E, self.Z, self.k, self.I))
+        if need == 0:
+            raise ValueError("unsupported layer shape")
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = _ws(need, self.Wg.device)
+        return self._ws
+
+    def __call__(self, x: torch.Tensor, r: Optional[torch.Tensor] = None,
+                 logits_override: Optional[torch.Tensor] = None, out=None, residual_out=None, topk_ids=None,
+                 topk_w=None):
+        """Returns (out, residual or None, topk_ids, topk_w)."""
+        _need(x, "x", torch.bfloat16)
+        dev = x.device
+        T, H = x.shape
+        if r is not None:
+            _need(r, "r", torch.bfloat16, dev)
+        if logits_override is not None:
+            _need(logits_override, "logits_override", torch.float32, dev)
+        ws = self.workspace(T)
+        with torch.cuda.device(dev):
+            if out is None:
+                out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            if residual_out is None and self.norm_w is not None:
+                residual_out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            if topk_ids is None:
+                topk_ids = torch.empty(T, self.k, dtype=torch.int32, device=dev)
+            if topk_w is None:
+                topk_w = torch.empty(T, self.k, dtype=torch.float32, device=dev)
+            _check("moe_forward_v2",
+                   lib().moe_forward_v2(_ptr(x), _ptr(r), _ptr(self.norm_w), self.eps, _ptr(self.Wg),
+                                        _ptr(logits_override), _ptr(self.w13_packed), _ptr(self.down_packed), T, H,
+                                        self.E, self.Z, self.k, self.I, _ptr(out), _ptr(residual_out),
+                                        _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel(), _stream(dev)))
         return out, residual_out, topk_ids, topk_w
 
 

@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/moe_gb300.h"
@@ -651,6 +652,228 @@ moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
   MOE_CUDA(moe::launch_grouped_gemm_mx(&g1, &g2, offsets, E, L.pad_rows, done, d->status, stream));
   if (t_gemm_ev_end) MOE_CUDA(cudaEventRecord(t_gemm_ev_end, stream));
   MOE_CUDA(moe::launch_finalize(y2, w, eri_pad, T, k, H, out, stream));
+  return MOE_OK;
+}
+
+// --------------------------------------------------------------- next rows --
+moe_status moe_add_rmsnorm_cast(const moe_bf16* x, const moe_bf16* r, const moe_bf16* w,
+                                float eps, int T, int H, moe_bf16* residual_out, float* y32_out,
+                                moe_bf16* ybf16_out, moe_stream_t stream) {
+  if (!x || !w || !ybf16_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (r && !aligned16(r)) || !aligned16(w) || !aligned16(ybf16_out) ||
+      (residual_out && !aligned16(residual_out)) || (y32_out && !aligned16(y32_out)))
+    return MOE_ERR_INVALID_ARG;
+  if (T < 1 || H < 256 || H % 256 != 0 || H > 32768) return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_add_rmsnorm_cast(x, r, w, eps, T, H, residual_out, y32_out, ybf16_out,
+                                        stream));
+  return MOE_OK;
+}
+
+size_t moe_init_routing_v2_workspace_size(int T, int E_local, int k) {
+  if (T < 1 || E_local < 1 || k < 1) return 0;
+  return align256(moe::routing_ws_bytes(T * k, E_local)) + align256((size_t)E_local * 4);
+}
+
+moe_status moe_init_routing_v2(const moe_bf16* x, const int32_t* topk_ids, int T, int H, int k,
+                               int E_total, int expert_begin, int expert_end, moe_bf16* expanded_x,
+                               int32_t* expanded_row_idx, int32_t* sorted_row_idx,
+                               int32_t* expert_offsets, int32_t* counts, void* ws,
+                               size_t ws_bytes, moe_stream_t stream) {
+  if (!topk_ids || !expanded_row_idx || !sorted_row_idx || !expert_offsets)
+    return MOE_ERR_INVALID_ARG;
+  if (expanded_x && (!x || !aligned16(x) || !aligned16(expanded_x))) return MOE_ERR_INVALID_ARG;
+  const int El = expert_end - expert_begin;
+  if (T < 1 || k < 1 || k > 32 || El < 1 || El > 256 || expert_begin < 0 ||
+      expert_end > E_total || (long long)T * k >= (1LL << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (expanded_x && (H < 8 || H % 8 != 0)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws == nullptr || ws_bytes < moe_init_routing_v2_workspace_size(T, El, k) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_WORKSPACE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  const int P = T * k;
+  int32_t* cnt = counts ? counts : at<int32_t>(ws, align256(moe::routing_ws_bytes(P, El)));
+  MOE_CUDA(moe::launch_routing_range(topk_ids, P, expert_begin, El, E_total, cnt, expert_offsets,
+                                     expanded_row_idx, sorted_row_idx, ws, nullptr, d->status,
+                                     stream));
+  if (expanded_x)
+    MOE_CUDA(moe::launch_gather_rows(x, sorted_row_idx, expert_offsets, El, P, H, k, expanded_x,
+                                     stream));
+  return MOE_OK;
+}
+
+size_t moe_re_routing_workspace_size(int R, int E_local) {
+  if (R < 1 || E_local < 1) return 0;
+  return align256(moe::reroute_ws_bytes(R, E_local));
+}
+
+moe_status moe_re_routing(const moe_bf16* x_recv, const int32_t* tokens_per_expert, int R,
+                          int E_local, int N, int H, moe_bf16* x_out, int32_t* perm,
+                          int32_t* expert_offsets, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  if (!tokens_per_expert || !perm || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if ((x_recv == nullptr) != (x_out == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (x_recv && (!aligned16(x_recv) || !aligned16(x_out))) return MOE_ERR_INVALID_ARG;
+  if (R < 1 || E_local < 1 || (long long)R * E_local > (1 << 20) || N < 0 ||
+      (x_recv && (H < 8 || H % 8 != 0)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws == nullptr || ws_bytes < moe_re_routing_workspace_size(R, E_local) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_WORKSPACE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_re_routing(x_recv, tokens_per_expert, R, E_local, N, H, x_out, perm,
+                                  expert_offsets, ws, stream));
+  return MOE_OK;
+}
+
+moe_status moe_finalize_routing_v2(const moe_bf16* y2, const float* topk_w,
+                                   const int32_t* expanded_row_idx, const int32_t* topk_ids,
+                                   const moe_bf16* x_in, int T, int k, int H, int E, int E_total,
+                                   moe_bf16* out, moe_stream_t stream) {
+  if (!y2 || !topk_w || !expanded_row_idx || !topk_ids || !x_in || !out || !aligned16(y2) ||
+      !aligned16(x_in) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || k > 32 || H < 8 || H % 8 != 0 || E < 0 || E_total < E)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_finalize_v2(y2, topk_w, expanded_row_idx, topk_ids, x_in, T, k, H, E,
+                                   E_total, out, stream));
+  return MOE_OK;
+}
+
+namespace {
+
+struct ForwardV2Layout {
+  ForwardLayout base;
+  size_t y32, ybf, total;
+};
+
+ForwardV2Layout forward_v2_layout(int T, int H, int E, int Z, int k, int I) {
+  ForwardV2Layout L{};
+  L.base = forward_layout(T, H, E, k, I);
+  size_t o = L.base.total;
+  // the router region of the base layout is sized for E gating columns, bf16 input;
+  // append one sized for E+Z columns and either input kind
+  const int Eg = E + Z;
+  const size_t rbytes = std::max(moe::router_ws_bytes(T, H, Eg, false),
+                                 moe::router_ws_bytes(T, H, Eg, true));
+  L.base.router = o;
+  o += align256(rbytes);
+  L.y32 = o;
+  o += align256((size_t)T * H * 4);
+  L.ybf = o;
+  o += align256((size_t)T * H * 2);
+  L.total = o;
+  return L;
+}
+
+}  // namespace
+
+size_t moe_forward_v2_workspace_size(int T, int H, int E, int Z, int k, int I) {
+  if (Z < 0 || E + Z > 256 || check_layer_shape(T, H, E + Z, k, I) != MOE_OK ||
+      check_layer_shape(T, H, E, 1, I) != MOE_OK)
+    return 0;
+  return forward_v2_layout(T, H, E, Z, k, I).total;
+}
+
+moe_status moe_forward_v2(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w, float eps,
+                          const float* Wg, const float* logits_override, const void* w13_packed,
+                          const void* down_packed, int T, int H, int E, int Z, int k, int I,
+                          moe_bf16* out, moe_bf16* residual_out, int32_t* topk_ids_out,
+                          float* topk_w_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!x || !w13_packed || !down_packed || !out) return MOE_ERR_INVALID_ARG;
+  if (!logits_override && !Wg) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (r && !aligned16(r)) || (norm_w && !aligned16(norm_w)) ||
+      !aligned16(w13_packed) || !aligned16(down_packed) || !aligned16(out) ||
+      (residual_out && !aligned16(residual_out)))
+    return MOE_ERR_INVALID_ARG;
+  if (Z < 0 || E + Z > 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+  MOE_TRY(check_layer_shape(T, H, E + Z, k, I));
+  MOE_TRY(check_layer_shape(T, H, E, 1, I));
+  if (norm_w && (H % 256 != 0 || H > 32768)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const ForwardV2Layout LV = forward_v2_layout(T, H, E, Z, k, I);
+  const ForwardLayout& L = LV.base;
+  if (ws == nullptr || ws_bytes < LV.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_WORKSPACE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  const int P = T * k;
+  const int Eg = E + Z;
+  int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(ws, L.ids);
+  float* w = topk_w_out ? topk_w_out : at<float>(ws, L.w);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* eri = at<int32_t>(ws, L.eri);
+  int32_t* sri = at<int32_t>(ws, L.sri);
+  int* done = at<int>(ws, L.done);
+  const moe_bf16* expert_in = x;
+  const float* y32 = nullptr;
+  if (norm_w) {
+    float* y = at<float>(ws, LV.y32);
+    uint16_t* ybf = at<uint16_t>(ws, LV.ybf);
+    MOE_CUDA(moe::launch_add_rmsnorm_cast(x, r, norm_w, eps, T, H, residual_out, y, ybf, stream));
+    y32 = y;
+    expert_in = ybf;
+  }
+  const bool fused_routing = moe::routing_plan(P, E).single_cta;
+  moe::GatingRouting fr{};
+  fr.counter = at<int>(ws, L.counter);
+  fr.counts = at<int32_t>(ws, L.counts);
+  fr.offsets = offsets;
+  fr.eri = eri;
+  fr.sri = sri;
+  fr.done = done;
+  fr.E_routed = E;
+  const moe::GatingRouting* fuse = fused_routing ? &fr : nullptr;
+  if (logits_override) {
+    if (fused_routing) MOE_CUDA(cudaMemsetAsync(fr.counter, 0, sizeof(int), stream));
+    MOE_CUDA(moe::launch_gating(logits_override, 1, T, Eg, k, 1, ids, w, fuse, d->status, stream));
+  } else {
+    const bool f32in = y32 != nullptr;
+    const moe::RouterPlan rp = moe::router_plan_ex(T, H, Eg, f32in);
+    float* part = at<float>(ws, L.router);
+    int* zw = fused_routing ? fr.counter : nullptr;
+    if (rp.tc) {
+      void* extra = at<uint8_t>(ws, L.router + align256((size_t)rp.splits * T * Eg * 4));
+      MOE_CUDA(moe::launch_router_tc(f32in ? static_cast<const void*>(y32) : x, f32in, Wg, T, H,
+                                     Eg, rp, part, extra, zw, d->status, stream));
+    } else if (f32in) {
+      MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, Eg, rp, part, zw, stream));
+    } else {
+      MOE_CUDA(moe::launch_router(x, Wg, T, H, Eg, rp, part, zw, stream));
+    }
+    MOE_CUDA(moe::launch_gating(part, rp.splits, T, Eg, k, 1, ids, w, fuse, d->status, stream));
+  }
+  if (!fused_routing)
+    MOE_CUDA(moe::launch_routing_range(ids, P, 0, E, Eg, fr.counts, offsets, eri, sri,
+                                       at<void>(ws, L.routing), done, d->status, stream));
+  uint16_t* xe = at<uint16_t>(ws, L.xe);
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  uint16_t* y2 = at<uint16_t>(ws, L.y2);
+  MOE_CUDA(moe::launch_gather_rows(expert_in, sri, offsets, E, P, H, k, xe, stream));
+  moe::GemmPhase g1{}, g2{};
+  g1.A_weights = w13_packed;
+  g1.B_act = xe;
+  g1.out = h;
+  g1.K = H;
+  g1.MW = 2 * I;
+  g1.n_out = I;
+  g1.epi = 0;
+  g2.A_weights = down_packed;
+  g2.B_act = h;
+  g2.out = y2;
+  g2.K = I;
+  g2.MW = H;
+  g2.n_out = H;
+  g2.epi = 1;
+  if (t_gemm_ev_begin) MOE_CUDA(cudaEventRecord(t_gemm_ev_begin, stream));
+  MOE_CUDA(moe::launch_grouped_gemm(&g1, &g2, offsets, E, P, T, done, d->status, stream));
+  if (t_gemm_ev_end) MOE_CUDA(cudaEventRecord(t_gemm_ev_end, stream));
+  MOE_CUDA(moe::launch_finalize_v2(y2, w, eri, ids, expert_in, T, k, H, E, Eg, out, stream));
   return MOE_OK;
 }
 

@@ -49,6 +49,8 @@ struct GatingRouting {
   int32_t* eri;
   int32_t* sri;
   int* done;     // E ints cleared for the grouped GEMM's dependency
+  int E_routed;  // experts [0, E_routed) are routed; ids >= E_routed (zero-computation
+                 // experts) are skipped.  0: all E gating columns are routed experts.
 };
 // Gating reads sum_{s<splits} src[s*T*E + t*E + e] (splits == 1: plain logits).
 cudaError_t launch_gating(const float* src, int splits, int T, int E, int k, int renormalize,
@@ -68,6 +70,10 @@ size_t routing_ws_bytes(int P, int E);
 cudaError_t launch_routing(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets,
                            int32_t* eri, int32_t* sri, void* ws, int* zero_counter, int* status,
                            cudaStream_t s);
+// Routing of the local experts [e_begin, e_begin + E) out of ids [0, E_total).
+cudaError_t launch_routing_range(const int32_t* ids, int P, int e_begin, int E, int E_total,
+                                 int32_t* counts, int32_t* offsets, int32_t* eri, int32_t* sri,
+                                 void* ws, int* zero_counter, int* status, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sri, const int32_t* offsets,
                                int E, int P, int H, int k, uint16_t* expanded_x, cudaStream_t s);
 cudaError_t launch_expert_tokens(const int32_t* ids, int P, int E, int32_t* counts,
@@ -129,6 +135,18 @@ struct GemmPhaseMx {
 cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1,
                                    const int32_t* offsets, int E, int P_pad_rows, int* done,
                                    int* status, cudaStream_t s);
+
+// ---- next rows (norm_route2.cu)
+cudaError_t launch_add_rmsnorm_cast(const uint16_t* x, const uint16_t* r, const uint16_t* w,
+                                    float eps, int T, int H, uint16_t* residual_out,
+                                    float* y32_out, uint16_t* ybf_out, cudaStream_t s);
+cudaError_t launch_finalize_v2(const uint16_t* y2, const float* w, const int32_t* eri,
+                               const int32_t* ids, const uint16_t* xin, int T, int k, int H, int E,
+                               int E_total, uint16_t* out, cudaStream_t s);
+size_t reroute_ws_bytes(int R, int El);
+cudaError_t launch_re_routing(const uint16_t* xin, const int32_t* cnt, int R, int El, int N, int H,
+                              uint16_t* xout, int32_t* perm, int32_t* offsets, void* ws,
+                              cudaStream_t s);
 
 // ---- device facts (api.cu)
 int device_sm_count();

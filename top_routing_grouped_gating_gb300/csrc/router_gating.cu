@@ -285,7 +285,8 @@ __global__ void __launch_bounds__(256) gating_kernel(const float* __restrict__ s
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  routing_single_cta(ids, T * k, E, fuse.counts, fuse.offsets, fuse.eri, fuse.sri, fuse.done,
+  const RouteMap rm{0, fuse.E_routed > 0 ? fuse.E_routed : E, E};
+  routing_single_cta(ids, T * k, rm, fuse.counts, fuse.offsets, fuse.eri, fuse.sri, fuse.done,
                      status, rsm);
   if (threadIdx.x == 0) *fuse.counter = 0;  // ready for the next call
 }

@@ -25,27 +25,28 @@ constexpr int kSingleCtaMaxPairs = 4096;
 constexpr int kChunkPairs = 2048;
 
 __global__ void __launch_bounds__(kRouteThreads) routing_single_cta_kernel(
-    const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
+    const int32_t* __restrict__ ids, int P, RouteMap rm, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ eri, int32_t* __restrict__ sri,
     int* __restrict__ zero_counter, int* status) {
   __shared__ RoutingSmem<kRouteThreads / 32> sm;
-  routing_single_cta(ids, P, E, counts, offsets, eri, sri, zero_counter, status, sm);
+  routing_single_cta(ids, P, rm, counts, offsets, eri, sri, zero_counter, status, sm);
 }
 
 __global__ void __launch_bounds__(kRouteThreads) routing_hist_kernel(
-    const int32_t* __restrict__ ids, int P, int E, int chunk_pairs, int32_t* __restrict__ chunk_hist,
-    int* status) {
+    const int32_t* __restrict__ ids, int P, RouteMap rm, int chunk_pairs,
+    int32_t* __restrict__ chunk_hist, int* status) {
   __shared__ int s_hist[kMaxExperts];
   const int tid = threadIdx.x;
+  const int E = rm.E;
   for (int i = tid; i < E; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
   const int j0 = blockIdx.x * chunk_pairs;
   const int j1 = min(P, j0 + chunk_pairs);
   bool bad = false;
   for (int j = j0 + tid; j < j1; j += blockDim.x) {
-    const int e = ids[j];
-    if (e >= 0 && e < E) atomicAdd(&s_hist[e], 1);
-    else bad = true;
+    const int e = local_id(ids[j], rm);
+    if (e >= 0) atomicAdd(&s_hist[e], 1);
+    else if (e == -3) bad = true;
   }
   if (bad) flag_status(status, MOE_DEV_BAD_EXPERT_ID);
   __syncthreads();
@@ -80,16 +81,17 @@ __global__ void __launch_bounds__(256) routing_scan_kernel(int32_t* __restrict__
 }
 
 __global__ void __launch_bounds__(kRouteThreads) routing_scatter_kernel(
-    const int32_t* __restrict__ ids, int P, int E, int chunk_pairs,
+    const int32_t* __restrict__ ids, int P, RouteMap rm, int chunk_pairs,
     const int32_t* __restrict__ chunk_base, int32_t* __restrict__ eri, int32_t* __restrict__ sri) {
   __shared__ int s_base[kMaxExperts];
   __shared__ int s_wcnt[(kRouteThreads / 32) * kMaxExperts];
   const int tid = threadIdx.x;
+  const int E = rm.E;
   for (int i = tid; i < E; i += blockDim.x) s_base[i] = chunk_base[(size_t)blockIdx.x * E + i];
   for (int i = tid; i < (kRouteThreads / 32) * E; i += blockDim.x) s_wcnt[i] = 0;
   __syncthreads();
   const int j0 = blockIdx.x * chunk_pairs;
-  scatter_range(ids, j0, min(P, j0 + chunk_pairs), E, s_base, s_wcnt, eri, sri);
+  scatter_range(ids, j0, min(P, j0 + chunk_pairs), rm, s_base, s_wcnt, eri, sri);
 }
 
 // expanded_x[p] = x[sri[p] / k] for p < offsets[E]; one warp per row, 16-byte copies.
@@ -202,17 +204,25 @@ size_t routing_ws_bytes(int P, int E) {
 cudaError_t launch_routing(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets,
                            int32_t* eri, int32_t* sri, void* ws, int* zero_counter, int* status,
                            cudaStream_t s) {
+  return launch_routing_range(ids, P, 0, E, E, counts, offsets, eri, sri, ws, zero_counter, status,
+                              s);
+}
+
+cudaError_t launch_routing_range(const int32_t* ids, int P, int e_begin, int E, int E_total,
+                                 int32_t* counts, int32_t* offsets, int32_t* eri, int32_t* sri,
+                                 void* ws, int* zero_counter, int* status, cudaStream_t s) {
   const RoutingPlan r = routing_plan(P, E);
+  const RouteMap rm{e_begin, E, E_total};
   if (r.single_cta) {
-    routing_single_cta_kernel<<<1, kRouteThreads, 0, s>>>(ids, P, E, counts, offsets, eri, sri,
+    routing_single_cta_kernel<<<1, kRouteThreads, 0, s>>>(ids, P, rm, counts, offsets, eri, sri,
                                                           zero_counter, status);
     return cudaGetLastError();
   }
   int32_t* chunk_hist = static_cast<int32_t*>(ws);
-  routing_hist_kernel<<<r.chunks, kRouteThreads, 0, s>>>(ids, P, E, r.chunk_pairs, chunk_hist,
+  routing_hist_kernel<<<r.chunks, kRouteThreads, 0, s>>>(ids, P, rm, r.chunk_pairs, chunk_hist,
                                                          status);
   routing_scan_kernel<<<1, 256, 0, s>>>(chunk_hist, r.chunks, E, counts, offsets, zero_counter);
-  routing_scatter_kernel<<<r.chunks, kRouteThreads, 0, s>>>(ids, P, E, r.chunk_pairs, chunk_hist,
+  routing_scatter_kernel<<<r.chunks, kRouteThreads, 0, s>>>(ids, P, rm, r.chunk_pairs, chunk_hist,
                                                             eri, sri);
   return cudaGetLastError();
 }

@@ -12,6 +12,22 @@ namespace {
 
 constexpr int kMaxExperts = 256;
 
+// Which ids this routing call sorts: local experts [begin, begin + E) out of ids
+// [0, E_total).  Other valid ids (another rank's experts, zero-computation
+// experts) are skipped without error; ids outside [0, E_total) are invalid.
+struct RouteMap {
+  int begin;
+  int E;
+  int E_total;
+};
+
+// >= 0: local expert; -2: skipped; -3: invalid id.
+__device__ __forceinline__ int local_id(int id, const RouteMap& rm) {
+  if (id < 0 || id >= rm.E_total) return -3;
+  const int l = id - rm.begin;
+  return (l >= 0 && l < rm.E) ? l : -2;
+}
+
 // Exclusive scan of one value per thread for threads [0, 256); every thread of
 // the block must call it.  s_tmp: 8 ints.  Returns the exclusive prefix; *total
 // receives the sum of all 256 values.
@@ -40,17 +56,19 @@ __device__ __forceinline__ int block_excl_scan_256(int v, int* s_tmp, int* total
 
 // Scatter pairs [j_begin, j_end) in order.  s_base[e] = first free row of e for
 // this range (advanced as rounds complete); s_wcnt = (warps x E) zeros.
-__device__ __forceinline__ void scatter_range(const int32_t* __restrict__ ids, int j_begin, int j_end, int E,
+__device__ __forceinline__ void scatter_range(const int32_t* __restrict__ ids, int j_begin, int j_end,
+                                              const RouteMap& rm,
                               int* s_base, int* s_wcnt, int32_t* __restrict__ eri,
                               int32_t* __restrict__ sri) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
+  const int E = rm.E;
   for (int j0 = j_begin; j0 < j_end; j0 += blockDim.x) {
     const int j = j0 + tid;
     int e = -1;                       // -1: no pair in this slot
     if (j < j_end) {
-      e = __ldcg(ids + j);  // may have been written by other CTAs of this grid
-      if (e < 0 || e >= E) e = -2;    // -2: invalid id, pair dropped
+      e = local_id(__ldcg(ids + j), rm);  // ids may come from other CTAs of this grid
+      if (e < 0) e = -2;                  // not routed here: pair dropped
     }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -88,10 +106,11 @@ struct RoutingSmem {
 };
 
 // Histogram, exclusive scan and stable scatter of all P pairs by one CTA
-// (blockDim.x == 32 * NWARPS >= 256).  zero_counter (E ints, may be null) is
-// cleared on the way.
+// (blockDim.x == 32 * NWARPS >= 256) for the local experts of rm.  zero_counter
+// (rm.E ints, may be null) is cleared on the way.
 template <int NWARPS>
-__device__ __forceinline__ void routing_single_cta(const int32_t* __restrict__ ids, int P, int E,
+__device__ __forceinline__ void routing_single_cta(const int32_t* __restrict__ ids, int P,
+                                                   const RouteMap& rm,
                                                    int32_t* __restrict__ counts,
                                                    int32_t* __restrict__ offsets,
                                                    int32_t* __restrict__ eri,
@@ -99,6 +118,7 @@ __device__ __forceinline__ void routing_single_cta(const int32_t* __restrict__ i
                                                    int* __restrict__ zero_counter, int* status,
                                                    RoutingSmem<NWARPS>& sm) {
   const int tid = threadIdx.x;
+  const int E = rm.E;
   for (int i = tid; i < kMaxExperts; i += blockDim.x) sm.hist[i] = 0;
   for (int i = tid; i < NWARPS * E; i += blockDim.x) sm.wcnt[i] = 0;
   if (zero_counter != nullptr)
@@ -106,9 +126,9 @@ __device__ __forceinline__ void routing_single_cta(const int32_t* __restrict__ i
   __syncthreads();
   bool bad = false;
   for (int j = tid; j < P; j += blockDim.x) {
-    const int e = __ldcg(ids + j);
-    if (e >= 0 && e < E) atomicAdd(&sm.hist[e], 1);
-    else bad = true;
+    const int e = local_id(__ldcg(ids + j), rm);
+    if (e >= 0) atomicAdd(&sm.hist[e], 1);
+    else if (e == -3) bad = true;
   }
   if (bad) flag_status(status, MOE_DEV_BAD_EXPERT_ID);
   __syncthreads();
@@ -122,7 +142,7 @@ __device__ __forceinline__ void routing_single_cta(const int32_t* __restrict__ i
   }
   if (tid == 0) offsets[E] = total;
   __syncthreads();
-  scatter_range(ids, 0, P, E, sm.base, sm.wcnt, eri, sri);
+  scatter_range(ids, 0, P, rm, sm.base, sm.wcnt, eri, sri);
 }
 
 }  // namespace

@@ -37,6 +37,8 @@ class MoEConfig:
     router: str = "uniform"   # "uniform" or "zipf"
     zipf_s: float = 1.2
     mx: bool = False          # MXFP8 variant (add + RMSNorm + MX quant in front)
+    prenorm: bool = False     # bf16 layer with fused add + RMSNorm + cast in front
+    Z: int = 0                # zero-computation (identity) experts after the E routed ones
     eps: float = 1e-6
     seed: int = 0
 
@@ -55,6 +57,10 @@ CONFIGS: Dict[str, MoEConfig] = {
     "qwen3_235b_a22b_prefill": MoEConfig("qwen3_235b_a22b_prefill", T=8192, H=4096, E=128, k=8,
                                          I=1536),
     "mxfp8_prefill": MoEConfig("mxfp8_prefill", T=4096, H=4096, E=128, k=8, I=1536, mx=True),
+    # next rows: fused add+RMSNorm+cast in front of the decode layer; identity experts
+    "qwen3_30b_a3b_decode_prenorm": MoEConfig("qwen3_30b_a3b_decode_prenorm", T=32, H=2048, E=128, k=8,
+                                              I=768, prenorm=True),
+    "zero_experts_decode": MoEConfig("zero_experts_decode", T=32, H=2048, E=128, k=8, I=768, Z=64),
 }
 
 
@@ -75,34 +81,35 @@ def _randn(gen: torch.Generator, shape, std: float, mean: float = 0.0, device="c
 def make_inputs(cfg: MoEConfig, device: str = "cpu", weights: bool = True) -> Dict[str, torch.Tensor]:
     """Draw the config's inputs on ``device`` (the generator lives on that device).
 
-    Returns bf16 ``x`` (T,H), fp32 ``Wg`` (H,E), bf16 ``w13`` (E,H,2I) whose first I
+    Returns bf16 ``x`` (T,H), fp32 ``Wg`` (H,E+Z), bf16 ``w13`` (E,H,2I) whose first I
     columns are gate_proj and last I are up_proj, bf16 ``down`` (E,I,H); for the MXFP8
-    variant also bf16 ``r`` (T,H) and bf16 ``norm_w`` (H,).  bf16 casts round to
+    and pre-norm variants also bf16 ``r`` (T,H) and bf16 ``norm_w`` (H,).  bf16 casts round to
     nearest even.  ``weights=False`` skips w13/down (for routing-only checks).
     """
     gen = torch.Generator(device=device)
     gen.manual_seed(cfg.seed)
     out: Dict[str, torch.Tensor] = {}
     x = _randn(gen, (cfg.T, cfg.H), 1.0, device=device)
-    if cfg.mx:
+    normed = cfg.mx or cfg.prenorm
+    if normed:
         r = _randn(gen, (cfg.T, cfg.H), 1.0, device=device)
-    Wg = _randn(gen, (cfg.H, cfg.E), 0.02, device=device)
+    Wg = _randn(gen, (cfg.H, cfg.E + cfg.Z), 0.02, device=device)
     if cfg.router == "zipf":
         perm = torch.randperm(cfg.E, generator=gen, device=device)
         rank = torch.empty(cfg.E, dtype=torch.float32, device=device)
         rank[perm] = torch.arange(1, cfg.E + 1, dtype=torch.float32, device=device)
-        Wg[0, :] = -cfg.zipf_s * torch.log(rank)
+        Wg[0, :cfg.E] = -cfg.zipf_s * torch.log(rank)
         x[:, 0] = 1.0
     elif cfg.router != "uniform":
         raise ValueError(f"unknown router kind {cfg.router!r}")
     out["x"] = x.to(torch.bfloat16)
-    if cfg.mx:
+    if normed:
         out["r"] = r.to(torch.bfloat16)
     out["Wg"] = Wg.contiguous()
     if weights:
         out["w13"] = _randn(gen, (cfg.E, cfg.H, 2 * cfg.I), 0.02, device=device).to(torch.bfloat16)
         out["down"] = _randn(gen, (cfg.E, cfg.I, cfg.H), 0.02, device=device).to(torch.bfloat16)
-        if cfg.mx:
+        if normed:
             out["norm_w"] = _randn(gen, (cfg.H,), 0.1, mean=1.0, device=device).to(torch.bfloat16)
     return out
 
