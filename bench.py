@@ -157,10 +157,11 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def algorithmic_gemm_bytes(cfg, active: int) -> int:
+def algorithmic_gemm_bytes(cfg, active: int, pairs: int = -1) -> int:
     """Bytes one grouped-GEMM launch must move: the active experts' w13 and down
-    weights, the expert-sorted activations in, h out and back in, y2 out."""
-    P = cfg.T * cfg.k
+    weights, the expert-sorted activations in, h out and back in, y2 out (for the
+    token-expert pairs routed to real experts)."""
+    P = cfg.T * cfg.k if pairs < 0 else pairs
     weights = active * 3 * cfg.H * cfg.I * 2
     acts = P * cfg.H * 2 + 2 * P * cfg.I * 2 + P * cfg.H * 2
     return weights + acts
@@ -171,12 +172,17 @@ def gemm_flops(cfg) -> float:
 
 
 def launches_per_step(cfg, router: bool = True) -> int:
-    """Kernels one moe_forward call launches: router, gating (routing fused into it
-    when P <= 4096, else histogram + scan + scatter), row expansion, grouped GEMM,
-    finalize; the MXFP8 layer adds the fused add+RMSNorm+quant kernel."""
+    """Kernels one forward call launches: the fused norm kernel (MXFP8 and pre-norm
+    layers), the router (one CUDA-core kernel for T <= 64; else weight split/pack,
+    an activation split for fp32 inputs, and the tensor-core GEMM), gating (routing
+    fused into it when P <= 4096, else histogram + scan + scatter), row expansion,
+    grouped GEMM, finalize."""
     P = cfg.T * cfg.k
     routing = 0 if P <= 4096 else 3
-    return (1 if cfg.mx else 0) + (1 if router else 0) + 1 + routing + 1 + 1 + 1
+    f32_router = cfg.mx or cfg.prenorm
+    router_k = (1 if cfg.T <= 64 else (3 if f32_router else 2)) if router else 0
+    norm = 1 if (cfg.mx or cfg.prenorm) else 0
+    return norm + router_k + 1 + routing + 1 + 1 + 1
 
 
 def rank_barrier(world: int) -> None:
@@ -218,7 +224,10 @@ def oracle_arrays(inp):
 
 def oracle_step(O, arrays, cfg, rows):
     a = arrays
-    if cfg.mx:
+    if cfg.prenorm or cfg.Z:
+        O.moe_forward_v2(a["x"][rows], a["r"][rows] if cfg.prenorm else None, a.get("norm_w"), cfg.eps, a["Wg"],
+                         a["w13"], a["down"], cfg.k, num_zero_experts=cfg.Z)
+    elif cfg.mx:
         O.moe_forward_mx(a["x"][rows], a["r"][rows], a["norm_w"], cfg.eps, a["Wg"], a["w13"], a["down"], cfg.k)
     else:
         O.moe_forward(a["x"][rows], a["Wg"], a["w13"], a["down"], cfg.k, keep_intermediates=False)
@@ -281,7 +290,12 @@ def run_reference(args, cfg):
 
 
 def workload_config(cfg):
-    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+    extra = {}
+    if cfg.Z:
+        extra["zero_computation_experts"] = cfg.Z
+    if cfg.prenorm:
+        extra["fused_add_rmsnorm_cast"] = True
+    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, **extra,
             "router": cfg.router, "seed": cfg.seed, "parallelism": "replicas (token batches), no collective",
             "l2": "inputs larger than L2: the active experts' weights streamed per step exceed the 129 MB L2"}
 
@@ -317,6 +331,15 @@ def run_ours(args, cfg):
 
         def step(xx, rr=r):
             return layer(xx, rr, **bufs)[0]
+    elif cfg.prenorm or cfg.Z:
+        layer = moe.MoELayerV2(inp["Wg"], inp["w13"], inp["down"], cfg.k, Z=cfg.Z,
+                               norm_w=inp["norm_w"] if cfg.prenorm else None, eps=cfg.eps)
+        r = inp["r"] if cfg.prenorm else None
+        out, res, ids, w = layer(x, r)
+        bufs = dict(out=out, residual_out=res, topk_ids=ids, topk_w=w)
+
+        def step(xx, rr=r):
+            return layer(xx, rr, **bufs)[0]
     else:
         layer = moe.MoELayer(inp["Wg"], inp["w13"], inp["down"], cfg.k)
         out, ids, w = layer(x)
@@ -325,8 +348,9 @@ def run_ours(args, cfg):
         def step(xx, rr=None):
             return layer(xx, **bufs)[0]
     torch.cuda.synchronize(dev)
-    counts = torch.bincount(ids.flatten().long(), minlength=cfg.E)
+    counts = torch.bincount(ids.flatten().long(), minlength=cfg.E + cfg.Z)[:cfg.E]
     active = int((counts > 0).sum())
+    routed_pairs = int(counts.sum())
     if args.no_cpu_baseline:
         # the packed copies are all the layer uses; drop the logical weights
         del inp["w13"], inp["down"]
@@ -378,14 +402,15 @@ def run_ours(args, cfg):
 
     # ---- end-to-end: pinned host input -> device -> layer -> pinned host output
     x_host = x.cpu().pin_memory()
-    r_host = inp["r"].cpu().pin_memory() if cfg.mx else None
+    has_r = cfg.mx or cfg.prenorm
+    r_host = inp["r"].cpu().pin_memory() if has_r else None
     o_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
-    r_dev = torch.empty_like(x) if cfg.mx else None
+    r_dev = torch.empty_like(x) if has_r else None
 
     def e2e_step():
         x_dev.copy_(x_host, non_blocking=True)
-        if cfg.mx:
+        if has_r:
             r_dev.copy_(r_host, non_blocking=True)
         o = step(x_dev, r_dev)
         o_host.copy_(o, non_blocking=True)
@@ -412,7 +437,7 @@ def run_ours(args, cfg):
     hbm, bf16, peak_kind = measured_peaks()
     value = whole_job_tokens_per_s(cfg.T, K, ws, ms_total)
     decode = cfg.T * cfg.k <= 16 * cfg.E
-    gbytes = algorithmic_gemm_bytes(cfg, active)
+    gbytes = algorithmic_gemm_bytes(cfg, active, routed_pairs)
     if cfg.mx:
         bf16 = bf16 * 2.0   # MXFP8 dense peak: measured bf16 x the nominal fp8/bf16 ratio (4.5/2.25)
     if decode:
@@ -437,7 +462,7 @@ def run_ours(args, cfg):
         "vs_baseline": None, "dtype": "mxfp8 (e4m3 + e8m0/32)" if cfg.mx else "bf16", "data": "synthetic",
         "config": workload_config(cfg), "roofline": roof,
         "e2e": {"value": whole_job_tokens_per_s(cfg.T, K, ws, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": cfg.T * cfg.H * 2 * (2 if cfg.mx else 1),
+                "h2d_bytes_per_step": cfg.T * cfg.H * 2 * (2 if has_r else 1),
                 "d2h_bytes_per_step": cfg.T * cfg.H * 2},
         "gpu_launches": launches_per_step(cfg) * K,
         "clocks": clocks,
@@ -457,12 +482,81 @@ def run_ours(args, cfg):
     return 0
 
 
+def run_ep_routing(args, cfg):
+    """One expert-parallel rank's routing at a prefill size: init_routing_v2 keeps the
+    pairs of this rank's experts (the first E/ep_ranks) and gathers their rows, then
+    re_routing reorders those rows from (source rank, expert) blocks -- the token
+    slices of the ep_ranks ranks -- into expert-major order.  HBM-bound: the
+    algorithmic bytes are the gathered rows written and the re-routed rows read and
+    written (2 bytes per element)."""
+    import numpy as np
+    import torch
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    if args.impl == "reference":
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "the CPU oracle arm covers the layer workloads; this routing-only workload has none"}))
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from top_routing_grouped_gating_gb300 import build as B
+    B.build()
+    import top_routing_grouped_gating_gb300 as moe
+    from top_routing_grouped_gating_gb300 import workloads as W
+    inp = W.make_inputs(cfg, device=f"cuda:{local}", weights=False)
+    x = inp["x"]
+    ids, _ = moe.gating_topk_softmax(moe.router_logits(x, inp["Wg"]), cfg.k)
+    El = cfg.E // cfg.ep_ranks
+    R = cfg.ep_ranks
+    ids_h = ids.cpu().numpy()
+    blocks = np.array_split(np.arange(cfg.T), R)
+    cnt = np.stack([np.bincount(ids_h[b].reshape(-1)[ids_h[b].reshape(-1) < El], minlength=El)
+                    for b in blocks]).astype(np.int32)
+    cnt_d = torch.from_numpy(cnt).to(dev)
+    N = int(cnt.sum())
+
+    def step():
+        rt = moe.init_routing_v2(ids, cfg.E, 0, El, x=x)
+        moe.re_routing(cnt_d, rt["expanded_x"][:N], N)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    s0.record()
+    for _ in range(args.steps):
+        step()
+    s1.record()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = s0.elapsed_time(s1)
+    hbm, _, kind = measured_peaks()
+    nbytes = 3 * N * cfg.H * 2
+    achieved = nbytes * args.steps / (ms / 1e3) / 1e9
+    line = {"metric": "expert-parallel rank routing tokens/s (init_routing_v2 + re_routing)",
+            "value": cfg.T * args.steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 rows, int32 ids", "data": "synthetic",
+            "config": dict(workload_config(cfg), ep_ranks=R, local_experts=El, local_pairs=N),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "peak_source": kind, "traffic": None, "algorithmic_bytes": nbytes,
+                         "kernel": "routing + gather + re-routing, whole step"},
+            "gpu_launches": 6 * args.steps, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     from top_routing_grouped_gating_gb300 import workloads as W
     if args.workload not in W.CONFIGS:
         raise SystemExit(f"unknown workload {args.workload}; one of {sorted(W.CONFIGS)}")
     cfg = W.CONFIGS[args.workload]
+    if cfg.ep_ranks:
+        return run_ep_routing(args, cfg)
     if args.impl == "reference":
         return run_reference(args, cfg)
     return run_ours(args, cfg)

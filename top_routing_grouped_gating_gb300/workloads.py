@@ -39,6 +39,7 @@ class MoEConfig:
     mx: bool = False          # MXFP8 variant (add + RMSNorm + MX quant in front)
     prenorm: bool = False     # bf16 layer with fused add + RMSNorm + cast in front
     Z: int = 0                # zero-computation (identity) experts after the E routed ones
+    ep_ranks: int = 0         # > 0: routing of one expert-parallel rank's experts only
     eps: float = 1e-6
     seed: int = 0
 
@@ -61,6 +62,10 @@ CONFIGS: Dict[str, MoEConfig] = {
     "qwen3_30b_a3b_decode_prenorm": MoEConfig("qwen3_30b_a3b_decode_prenorm", T=32, H=2048, E=128, k=8,
                                               I=768, prenorm=True),
     "zero_experts_decode": MoEConfig("zero_experts_decode", T=32, H=2048, E=128, k=8, I=768, Z=64),
+    # one rank of 4-way expert parallelism at the Qwen3-235B prefill size: expert-range
+    # routing of all gathered tokens plus re-routing of the received blocks
+    "ep4_rank_routing_qwen3_235b_prefill": MoEConfig("ep4_rank_routing_qwen3_235b_prefill", T=8192,
+                                                     H=4096, E=128, k=8, I=1536, ep_ranks=4),
 }
 
 
