@@ -104,7 +104,8 @@ def profiled_traffic(workload: str):
     m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", txt)
     if not m_b or not m_h:
         return None
-    src = os.path.join(ROOT, "top_routing_grouped_gating_gb300", "csrc", "gmm.cu")
+    src = os.path.join(ROOT, "top_routing_grouped_gating_gb300", "csrc",
+                       "gmm_mx.cu" if workload.startswith("mxfp8") else "gmm.cu")
     if m_h.group(1) != file_sha(src):
         return None
     return float(m_b.group(1))
@@ -162,6 +163,10 @@ def algorithmic_gemm_bytes(cfg, active: int, pairs: int = -1) -> int:
     weights, the expert-sorted activations in, h out and back in, y2 out (for the
     token-expert pairs routed to real experts)."""
     P = cfg.T * cfg.k if pairs < 0 else pairs
+    if cfg.mx:  # e4m3 codes plus one E8M0 byte per 32 elements; y2 stays bf16
+        weights = active * 3 * cfg.H * cfg.I * 33 // 32
+        acts = P * cfg.H * 33 // 32 + 2 * P * cfg.I * 33 // 32 + P * cfg.H * 2
+        return weights + acts
     weights = active * 3 * cfg.H * cfg.I * 2
     acts = P * cfg.H * 2 + 2 * P * cfg.I * 2 + P * cfg.H * 2
     return weights + acts
