@@ -573,3 +573,93 @@ def moe_forward_v2(x: np.ndarray, r: Optional[np.ndarray], norm_w: Optional[np.n
         res["y"] = router_in
         res["y_bf16"] = expert_in
     return res
+
+
+# --------------------------------------------------------------------------- #
+# W4A8: MXFP4 (e2m1) expert weights, MXFP8 activations                        #
+# --------------------------------------------------------------------------- #
+
+E2M1_MAX = 6.0
+E2M1_EMAX = 2          # 6 = 1.5 * 2^2
+
+
+def e2m1_value(code: int) -> float:
+    """Value of a 4-bit e2m1 code: 1 sign, 2 exponent (bias 1), 1 mantissa bit;
+    exponent field 0 is subnormal (m/2 * 2^0); no inf or NaN (OCP MX v1.0)."""
+    s = -1.0 if (code >> 3) & 1 else 1.0
+    ex = (code >> 1) & 3
+    m = code & 1
+    if ex == 0:
+        return s * 0.5 * m
+    return s * (1.0 + 0.5 * m) * 2.0 ** (ex - 1)
+
+
+_E2M1_POS = np.array([e2m1_value(c) for c in range(8)], np.float64)   # 0 .. 6, ascending
+
+
+def e2m1_encode(v: np.ndarray) -> np.ndarray:
+    """Round to the nearest e2m1 value, ties to the even code, saturating at +-6
+    (the page's W4A8 uses MXFP4 weights, [Q3MoE §计算分解(AllGather方案)])."""
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), E2M1_MAX)
+    hi = np.clip(np.searchsorted(_E2M1_POS, a, side="left"), 0, 7)
+    lo = np.clip(hi - 1, 0, 7)
+    dlo = a - _E2M1_POS[lo]
+    dhi = _E2M1_POS[hi] - a
+    code = np.where((dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0)), hi, lo).astype(np.int64)
+    return (code | (np.signbit(v).astype(np.int64) << 3)).astype(np.uint8)
+
+
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    table = np.array([e2m1_value(c) for c in range(16)], np.float64)
+    return table[np.asarray(codes, np.int64) & 15]
+
+
+def mx4_quantize(y: np.ndarray, block: int = MX_BLOCK):
+    """MXFP4 along the last axis: X = floor(log2 amax) - 2 clamped to [-127,127],
+    codes = e2m1(y / 2^X); returns (codes uint8, one per element, and scale bytes)."""
+    y = np.asarray(y, np.float64)
+    n = y.shape[-1]
+    yb = y.reshape(y.shape[:-1] + (n // block, block))
+    amax = np.max(np.abs(yb), axis=-1)
+    X = np.full(amax.shape, -127, np.int64)
+    nz = amax > 0
+    _, ex = np.frexp(amax[nz])
+    X[nz] = np.clip((ex - 1) - E2M1_EMAX, -127, 127)
+    codes = e2m1_encode(yb / np.exp2(X.astype(np.float64))[..., None])
+    return codes.reshape(y.shape), (X + 127).astype(np.uint8)
+
+
+def mx4_roundtrip(y: np.ndarray, axis: int = -1) -> np.ndarray:
+    y = np.moveaxis(np.asarray(y, np.float64), axis, -1)
+    q, s = mx4_quantize(y)
+    n = y.shape[-1]
+    v = e2m1_decode(q).reshape(y.shape[:-1] + (n // MX_BLOCK, MX_BLOCK))
+    v = v * np.exp2(s.astype(np.float64) - 127.0)[..., None]
+    return np.moveaxis(v.reshape(y.shape), -1, axis)
+
+
+def moe_forward_w4a8(x, r, norm_w, eps, Wg, w13, down, k, logits32=None):
+    """The MXFP8 layer of moe_forward_mx with MXFP4 expert weights: identical except
+    that w13 (along H) and down (along I) are quantised to e2m1 + E8M0/32."""
+    s, y = add_rmsnorm(x, r, norm_w, eps)
+    if logits32 is None:
+        logits32 = router_logits_f32(y, Wg)
+    yq = mx_roundtrip(y, axis=-1)
+    ids, w = gating_topk_softmax(logits32, k)
+    E = len(w13)
+    rt = init_routing(ids, E)
+    T, H = y.shape
+    offs, sri, eri = rt["offsets"], rt["sorted_row_idx"], rt["expanded_row_idx"]
+    y_all = np.zeros((T * k, H), np.float64)
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi == lo:
+            continue
+        h = swiglu(yq[sri[lo:hi] // k] @ mx4_roundtrip(w13[e], axis=0))
+        y_all[lo:hi] = mx_roundtrip(h) @ mx4_roundtrip(down[e], axis=0)
+    out = np.zeros((T, H), np.float64)
+    for t in range(T):
+        for s_ in range(k):
+            out[t] += w[t, s_] * y_all[eri[t * k + s_]]
+    return dict(residual=s, logits32=np.asarray(logits32, np.float32), topk_ids=ids, topk_w=w, out=out, **rt)

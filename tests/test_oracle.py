@@ -436,3 +436,61 @@ def test_prenorm_layer_is_norm_then_layer():
     ids, w = O.gating_topk_softmax(lg, k)
     ref = O.dense_moe_reference(yb, w13, down, ids, w)
     np.testing.assert_allclose(res["out"], ref, rtol=1e-11, atol=1e-12)
+
+
+# ------------------------------------------------------------------- W4A8 --
+
+
+def test_e2m1_golden(golden):
+    for c in golden("e2m1.json")["cases"]:
+        assert int(O.e2m1_encode(np.array([c["value"]]))[0]) == c["code"], c["derivation"]
+
+
+def test_e2m1_roundtrip_and_nearest():
+    codes = np.arange(16)
+    vals = O.e2m1_decode(codes)
+    np.testing.assert_array_equal(O.e2m1_encode(vals)[vals != 0], codes[vals != 0])
+    rng = np.random.default_rng(0)
+    v = rng.uniform(-6, 6, 20000)
+    d = O.e2m1_decode(O.e2m1_encode(v))
+    grid = np.unique(np.abs(vals))
+    best = np.min(np.abs(np.abs(v)[:, None] - grid[None, :]), axis=1)
+    np.testing.assert_allclose(np.abs(np.abs(v) - np.abs(d)), best, atol=1e-15)
+    assert np.all(np.sign(d[d != 0]) == np.sign(v[d != 0]))
+
+
+def test_mx4_scale_rule_and_error_bound():
+    rng = np.random.default_rng(1)
+    y = rng.standard_normal((32, 128)) * np.exp2(rng.integers(-10, 10, size=(32, 1)))
+    q, s = O.mx4_quantize(y)
+    X = s.astype(np.int64) - 127
+    amax = np.abs(y.reshape(32, 4, 32)).max(-1)
+    r = amax / np.exp2(X)
+    assert np.all((r >= 4) & (r < 8))
+    deq = O.mx4_roundtrip(y)
+    scale = np.repeat(np.exp2(X), 32, axis=1)
+    sat = np.abs(y) > 6 * scale
+    err = np.abs(deq - y)
+    assert np.all(err[~sat] <= np.maximum(np.abs(y[~sat]) * 0.25, 0.25 * scale[~sat]) + 1e-12)
+    np.testing.assert_allclose(np.abs(deq[sat]), 6 * scale[sat])
+
+
+def test_w4a8_layer_matches_dense_composition():
+    rng = np.random.default_rng(5)
+    T, H, E, k, I = 5, 64, 4, 2, 32
+    x, r = rng.standard_normal((T, H)), rng.standard_normal((T, H))
+    nw = 1 + 0.1 * rng.standard_normal(H)
+    Wg = rng.standard_normal((H, E)) * 0.3
+    w13 = [rng.standard_normal((H, 2 * I)) * 0.2 for _ in range(E)]
+    down = [rng.standard_normal((I, H)) * 0.2 for _ in range(E)]
+    res = O.moe_forward_w4a8(x, r, nw, 1e-6, Wg, w13, down, k)
+    _, y = O.add_rmsnorm(x, r, nw, 1e-6)
+    ids, w = O.gating_topk_softmax(O.router_logits_f32(y, Wg), k)
+    ref = np.zeros((T, H))
+    for t in range(T):
+        a = O.mx_roundtrip(y[t:t + 1])
+        for sl in range(k):
+            e = ids[t, sl]
+            h = O.swiglu(a @ O.mx4_roundtrip(w13[e], axis=0))
+            ref[t] += w[t, sl] * (O.mx_roundtrip(h) @ O.mx4_roundtrip(down[e], axis=0))[0]
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-11, atol=1e-12)
