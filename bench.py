@@ -105,7 +105,7 @@ def profiled_traffic(workload: str):
     if not m_b or not m_h:
         return None
     src = os.path.join(ROOT, "top_routing_grouped_gating_gb300", "csrc",
-                       "gmm_mx.cu" if workload.startswith("mxfp8") else "gmm.cu")
+                       "gmm_mx.cu" if workload.startswith(("mxfp8", "w4a8")) else "gmm.cu")
     if m_h.group(1) != file_sha(src):
         return None
     return float(m_b.group(1))
@@ -163,8 +163,8 @@ def algorithmic_gemm_bytes(cfg, active: int, pairs: int = -1) -> int:
     weights, the expert-sorted activations in, h out and back in, y2 out (for the
     token-expert pairs routed to real experts)."""
     P = cfg.T * cfg.k if pairs < 0 else pairs
-    if cfg.mx:  # e4m3 codes plus one E8M0 byte per 32 elements; y2 stays bf16
-        weights = active * 3 * cfg.H * cfg.I * 33 // 32
+    if cfg.mx:  # e4m3 (e2m1: half a byte) codes plus one E8M0 byte per 32 elements; y2 stays bf16
+        weights = active * 3 * cfg.H * cfg.I * (17 if cfg.w4 else 33) // 32
         acts = P * cfg.H * 33 // 32 + 2 * P * cfg.I * 33 // 32 + P * cfg.H * 2
         return weights + acts
     weights = active * 3 * cfg.H * cfg.I * 2
@@ -232,6 +232,8 @@ def oracle_step(O, arrays, cfg, rows):
     if cfg.prenorm or cfg.Z:
         O.moe_forward_v2(a["x"][rows], a["r"][rows] if cfg.prenorm else None, a.get("norm_w"), cfg.eps, a["Wg"],
                          a["w13"], a["down"], cfg.k, num_zero_experts=cfg.Z)
+    elif cfg.w4:
+        O.moe_forward_w4a8(a["x"][rows], a["r"][rows], a["norm_w"], cfg.eps, a["Wg"], a["w13"], a["down"], cfg.k)
     elif cfg.mx:
         O.moe_forward_mx(a["x"][rows], a["r"][rows], a["norm_w"], cfg.eps, a["Wg"], a["w13"], a["down"], cfg.k)
     else:
@@ -329,7 +331,8 @@ def run_ours(args, cfg):
     x = inp["x"]
     stream = torch.cuda.current_stream(dev)
     if cfg.mx:
-        layer = moe.MoELayerMX(inp["Wg"], inp["w13"], inp["down"], inp["norm_w"], cfg.k, cfg.eps)
+        cls = moe.MoELayerW4A8 if cfg.w4 else moe.MoELayerMX
+        layer = cls(inp["Wg"], inp["w13"], inp["down"], inp["norm_w"], cfg.k, cfg.eps)
         r = inp["r"]
         out, res, ids, w = layer(x, r)
         bufs = dict(out=out, residual_out=res, topk_ids=ids, topk_w=w)
@@ -452,6 +455,7 @@ def run_ours(args, cfg):
                 else "fallback 6.8 TB/s"}
     else:
         achieved = gemm_flops(cfg) / (gemm_ms / 1e3) / 1e12
+        # e2m1 x e4m3 runs in the same f8f6f4 MMA kind, at the fp8 rate
         src = "bf16_tflops x 2 (nominal MXFP8/bf16 ratio)" if cfg.mx else "bf16_tflops"
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
                 "frac": achieved / bf16,
@@ -464,7 +468,8 @@ def run_ours(args, cfg):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "mxfp8 (e4m3 + e8m0/32)" if cfg.mx else "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": ("w4a8 (weights e2m1 + e8m0/32, activations e4m3 + e8m0/32)" if cfg.w4
+                                       else "mxfp8 (e4m3 + e8m0/32)" if cfg.mx else "bf16"), "data": "synthetic",
         "config": workload_config(cfg), "roofline": roof,
         "e2e": {"value": whole_job_tokens_per_s(cfg.T, K, ws, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.H * 2 * (2 if has_r else 1),

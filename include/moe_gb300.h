@@ -248,6 +248,40 @@ MOE_API moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const mo
                                   float* topk_w_out, void* ws, size_t ws_bytes,
                                   moe_stream_t stream);
 
+/* ------------------------------------------------------------------ W4A8 --
+ * The MXFP8 layer with MXFP4 expert weights (W4A8: 4-bit weights, 8-bit
+ * activations).  Page "基于Atlas A3、950训练/推理集群的Qwen3-MoE模型低时延推理性能优化实践",
+ * §概述 (W4A8 mixed-precision prefill) and §计算分解 AllGather方案 (W4A8 = MXFP4
+ * weights, activations through npu_dynamic_mx_quant); the page fixes no rounding or
+ * scale rule, so this library takes OCP MXFP4 v1.0: blocks of 32 consecutive weights along the reduction axis
+ * share an E8M0 scale 2^X, X = floor(log2(max|v|)) - 2 (2 = the exponent of e2m1's
+ * largest value 6) clamped to [-127,127], all-zero block X = -127; codes are
+ * e2m1(v / 2^X), nearest-even, saturating at +-6.  Activations and h stay MXFP8 as
+ * in moe_forward_mx.
+ *
+ * moe_pack_weights_mx4: as moe_pack_weights_mx, but codes are packed two per byte
+ * (element 2j of a row in the low nibble of byte j) and stored tile-major: the
+ * codes of row r, K-elements [128 s, 128 s + 128) of expert e are the 64 bytes at
+ * ((e * rows / 128 + r / 128) * K / 128 + s) * 8192 + (r % 128) * 64, rows = 2I for
+ * w13 (K = H) and H for down (K = I).  Scale atoms are as moe_pack_weights_mx.
+ *   which: 0 w13 codes (E*2I*H/2 bytes), 1 w13 scales (E*2I*H/32), 2 down codes
+ *   (E*H*I/2), 3 down scales (E*H*I/32).  H % 128 == 0, I % 128 == 0.
+ * moe_forward_w4a8: arguments as moe_forward_mx with the packed MXFP4 weights; code
+ *   buffers 32-byte aligned (MOE_ERR_INVALID_ARG otherwise).  Workspace size as
+ *   moe_forward_mx. */
+MOE_API size_t moe_packed_weight_bytes_mx4(int E, int H, int I, int which);
+MOE_API moe_status moe_pack_weights_mx4(const moe_bf16* w13, const moe_bf16* down, int E, int H,
+                                        int I, void* w13_q, void* w13_sf, void* down_q,
+                                        void* down_sf, moe_stream_t stream);
+MOE_API size_t moe_forward_w4a8_workspace_size(int T, int H, int E, int k, int I);
+MOE_API moe_status moe_forward_w4a8(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w,
+                                    float eps, const float* Wg, const float* logits_override,
+                                    const void* w13_q, const void* w13_sf, const void* down_q,
+                                    const void* down_sf, int T, int H, int E, int k, int I,
+                                    moe_bf16* out, moe_bf16* residual_out, int32_t* topk_ids_out,
+                                    float* topk_w_out, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream);
+
 /* ------------------------------------------------------------- next rows --
  * §融合RMSNorm Cast: residual add + RMSNorm with two outputs, FP32 for the gate
  * (router) and BF16 for the experts.  s = x + r; residual_out = bf16(s);

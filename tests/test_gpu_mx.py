@@ -143,6 +143,19 @@ def test_forward_mx_small(cuda_dev, T, E, k, H, I):
     _check_mx_forward(cfg, inp, layer)
 
 
+def test_forward_mx_decode_tiles_skewed(cuda_dev):
+    """Few pairs per expert on average (the narrow-tile shape) but Zipf-skewed, so the
+    busiest expert spans several 32-token tiles and every 32-row group of a scale atom."""
+    cfg = W.with_shape(W.CONFIGS["mxfp8_prefill"], T=256, E=16, k=1, H=256, I=128, router="zipf",
+                       zipf_s=2.0)
+    inp, layer = _mx_layer(cfg)
+    assert cfg.T * cfg.k <= 16 * cfg.E
+    _check_mx_forward(cfg, inp, layer)
+    _, y = O.add_rmsnorm(to_np(inp["x"]), to_np(inp["r"]), to_np(inp["norm_w"]), cfg.eps)
+    ids, _ = O.gating_topk_softmax(O.router_logits_f32(y, to_np(inp["Wg"])), cfg.k)
+    assert np.bincount(ids.ravel(), minlength=cfg.E).max() > 128   # two atoms, all groups
+
+
 def test_forward_mx_full_size_sampled(cuda_dev):
     cfg = W.CONFIGS["mxfp8_prefill"]
     inp, layer = _mx_layer(cfg)

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     MoELayer,
     MoELayerMX,
     MoELayerV2,
+    MoELayerW4A8,
     add_rmsnorm_cast,
     finalize_routing_v2,
     init_routing_v2,
@@ -20,6 +21,7 @@ from ._binding import (  # noqa: F401
     add_rmsnorm_mxquant,
     mx_quantize,
     pack_weights_mx,
+    pack_weights_mx4,
     clear_device_status,
     compute_expert_tokens,
     exported_symbols,

@@ -61,6 +61,11 @@ _SIGS = {
     "moe_forward_mx_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "moe_forward_mx": (_c_int, [_vp, _vp, _vp, _c_float, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                 _c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "moe_packed_weight_bytes_mx4": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "moe_pack_weights_mx4": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp]),
+    "moe_forward_w4a8_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "moe_forward_w4a8": (_c_int, [_vp, _vp, _vp, _c_float, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                  _c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_init_routing_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp,
                                           _vp]),
 }
@@ -380,24 +385,36 @@ def mx_quantize(y: torch.Tensor):
     return q, sc
 
 
-def pack_weights_mx(w13: torch.Tensor, down: torch.Tensor):
-    """Logical bf16 w13 (E,H,2I), down (E,I,H) -> (w13_q, w13_sf, down_q, down_sf) uint8 buffers."""
+def _pack_block_scaled(w13, down, suffix):
     _need(w13, "w13", torch.bfloat16)
     _need(down, "down", torch.bfloat16, w13.device)
     E, H, I2 = w13.shape
     I = I2 // 2
     L = lib()
     dev = w13.device
+    size = getattr(L, "moe_packed_weight_bytes_" + suffix)
     with torch.cuda.device(dev):
-        bufs = [torch.empty(L.moe_packed_weight_bytes_mx(E, H, I, i), dtype=torch.uint8, device=dev)
-                for i in range(4)]
-        _check("moe_pack_weights_mx", L.moe_pack_weights_mx(_ptr(w13), _ptr(down), E, H, I, *[_ptr(b) for b in bufs],
-                                                            _stream(dev)))
+        bufs = [torch.empty(size(E, H, I, i), dtype=torch.uint8, device=dev) for i in range(4)]
+        name = "moe_pack_weights_" + suffix
+        _check(name, getattr(L, name)(_ptr(w13), _ptr(down), E, H, I, *[_ptr(b) for b in bufs], _stream(dev)))
     return tuple(bufs)
+
+
+def pack_weights_mx(w13: torch.Tensor, down: torch.Tensor):
+    """Logical bf16 w13 (E,H,2I), down (E,I,H) -> MXFP8 (w13_q, w13_sf, down_q, down_sf) uint8 buffers."""
+    return _pack_block_scaled(w13, down, "mx")
+
+
+def pack_weights_mx4(w13: torch.Tensor, down: torch.Tensor):
+    """As pack_weights_mx with MXFP4 codes, two e2m1 codes per byte (low nibble first)."""
+    return _pack_block_scaled(w13, down, "mx4")
 
 
 class MoELayerMX:
     """MXFP8 MoE layer: fused add+RMSNorm+MX quant in front, block-scaled grouped GEMMs."""
+
+    _pack = staticmethod(pack_weights_mx)
+    _fwd = "moe_forward_mx"
 
     def __init__(self, Wg: torch.Tensor, w13: torch.Tensor, down: torch.Tensor, norm_w: torch.Tensor, k: int,
                  eps: float = 1e-6):
@@ -407,13 +424,13 @@ class MoELayerMX:
         self.eps = float(eps)
         self.Wg = Wg.contiguous()
         self.norm_w = norm_w.contiguous()
-        self.w13_q, self.w13_sf, self.down_q, self.down_sf = pack_weights_mx(w13.contiguous(), down.contiguous())
+        self.w13_q, self.w13_sf, self.down_q, self.down_sf = self._pack(w13.contiguous(), down.contiguous())
         self._ws = None
 
     def workspace(self, T: int) -> torch.Tensor:
-        need = int(lib().moe_forward_mx_workspace_size(T, self.H, self.E, self.k, self.I))
+        need = int(getattr(lib(), self._fwd + "_workspace_size")(T, self.H, self.E, self.k, self.I))
         if need == 0:
-            raise ValueError("unsupported MXFP8 layer shape")
+            raise ValueError("unsupported block-scaled layer shape")
         if self._ws is None or self._ws.numel() < need:
             self._ws = _ws(need, self.Wg.device)
         return self._ws
@@ -439,13 +456,20 @@ class MoELayerMX:
                 topk_ids = torch.empty(T, self.k, dtype=torch.int32, device=dev)
             if topk_w is None:
                 topk_w = torch.empty(T, self.k, dtype=torch.float32, device=dev)
-            _check("moe_forward_mx",
-                   lib().moe_forward_mx(_ptr(x), _ptr(r), _ptr(self.norm_w), self.eps, _ptr(self.Wg),
-                                        _ptr(logits_override), _ptr(self.w13_q), _ptr(self.w13_sf),
-                                        _ptr(self.down_q), _ptr(self.down_sf), T, H, self.E, self.k, self.I,
-                                        _ptr(out), _ptr(residual_out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws),
-                                        ws.numel(), _stream(dev)))
+            _check(self._fwd,
+                   getattr(lib(), self._fwd)(_ptr(x), _ptr(r), _ptr(self.norm_w), self.eps, _ptr(self.Wg),
+                                             _ptr(logits_override), _ptr(self.w13_q), _ptr(self.w13_sf),
+                                             _ptr(self.down_q), _ptr(self.down_sf), T, H, self.E, self.k, self.I,
+                                             _ptr(out), _ptr(residual_out), _ptr(topk_ids), _ptr(topk_w),
+                                             _ptr(ws), ws.numel(), _stream(dev)))
         return out, residual_out, topk_ids, topk_w
+
+
+class MoELayerW4A8(MoELayerMX):
+    """The MXFP8 layer with MXFP4 (e2m1 + E8M0/32) expert weights."""
+
+    _pack = staticmethod(pack_weights_mx4)
+    _fwd = "moe_forward_w4a8"
 
 
 # ------------------------------------------------------------------- next rows

@@ -165,6 +165,20 @@ bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t elem_by
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_2d_strided(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base,
+                            uint64_t inner, uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
+                            uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                          uint32_t box_inner, uint32_t box_rows) {
   return encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, rows, box_inner,
@@ -513,6 +527,7 @@ struct ForwardMxLayout {
   size_t y32, xq, xs, router, ids, w, routing, counts, offsets, eri, sri, done, counter, xe,
       xe_sf, eri_pad, hq, h_sf, y2, total;
   int pad_rows;
+  int pad;  // row padding of each expert block (one scale atom per pad rows and K step)
 };
 
 ForwardMxLayout forward_mx_layout(int T, int H, int E, int k, int I) {
@@ -524,8 +539,10 @@ ForwardMxLayout forward_mx_layout(int T, int H, int E, int k, int I) {
     return at;
   };
   const size_t P = (size_t)T * k;
-  const size_t R = ((P + 127) / 128) * 128 + 128 * (size_t)E;  // rows after 128-row padding
+  // an upper bound on the padded rows for either padding (a multiple of 128)
+  const size_t R = ((P + 127) / 128) * 128 + 128 * (size_t)E;
   L.pad_rows = (int)R;
+  L.pad = moe::mx_pad_rows((long long)P, E);
   L.y32 = take((size_t)T * H * 4);
   L.xq = take((size_t)T * H);
   L.xs = take((size_t)T * H / 32);
@@ -540,10 +557,10 @@ ForwardMxLayout forward_mx_layout(int T, int H, int E, int k, int I) {
   L.done = take((size_t)E * 4);
   L.counter = take(4);
   L.xe = take(R * H);
-  L.xe_sf = take(R * H / 32);
+  L.xe_sf = take(R / L.pad * (H / 128) * 512);
   L.eri_pad = take(P * 4);
   L.hq = take(R * I);
-  L.h_sf = take(R * I / 32);
+  L.h_sf = take(R / L.pad * (I / 128) * 512);
   L.y2 = take(R * H * 2);
   L.total = o;
   return L;
@@ -563,13 +580,19 @@ size_t moe_forward_mx_workspace_size(int T, int H, int E, int k, int I) {
   return forward_mx_layout(T, H, E, k, I).total;
 }
 
-moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w, float eps,
-                          const float* Wg, const float* logits_override, const void* w13_q,
-                          const void* w13_sf, const void* down_q, const void* down_sf, int T,
-                          int H, int E, int k, int I, moe_bf16* out, moe_bf16* residual_out,
-                          int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
-                          moe_stream_t stream) {
+namespace {
+
+// The block-scaled layer; w4 selects MXFP4 (packed e2m1) expert weights.
+moe_status forward_mx_impl(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w, float eps,
+                           const float* Wg, const float* logits_override, const void* w13_q,
+                           const void* w13_sf, const void* down_q, const void* down_sf, int T,
+                           int H, int E, int k, int I, moe_bf16* out, moe_bf16* residual_out,
+                           int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                           bool w4, cudaStream_t stream) {
   if (!x || !norm_w || !w13_q || !w13_sf || !down_q || !down_sf || !out)
+    return MOE_ERR_INVALID_ARG;
+  // packed e2m1 rows are read by TMA from 32-byte aligned addresses
+  if (w4 && ((reinterpret_cast<uintptr_t>(w13_q) | reinterpret_cast<uintptr_t>(down_q)) & 31u))
     return MOE_ERR_INVALID_ARG;
   if (!logits_override && !Wg) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || (r && !aligned16(r)) || !aligned16(norm_w) || !aligned16(w13_q) ||
@@ -625,7 +648,7 @@ moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
   uint8_t* xe = at<uint8_t>(ws, L.xe);
   uint8_t* xe_sf = at<uint8_t>(ws, L.xe_sf);
   int32_t* eri_pad = at<int32_t>(ws, L.eri_pad);
-  MOE_CUDA(moe::launch_mx_expand(xq, xs, ids, eri, offsets, E, P, H, k, xe, xe_sf, eri_pad,
+  MOE_CUDA(moe::launch_mx_expand(xq, xs, ids, eri, offsets, E, P, H, k, L.pad, xe, xe_sf, eri_pad,
                                  stream));
   uint8_t* hq = at<uint8_t>(ws, L.hq);
   uint8_t* h_sf = at<uint8_t>(ws, L.h_sf);
@@ -648,11 +671,68 @@ moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
   g2.K = I;
   g2.MW = H;
   g2.n_out = H;
+  g1.a_fp4 = g2.a_fp4 = w4;
   if (t_gemm_ev_begin) MOE_CUDA(cudaEventRecord(t_gemm_ev_begin, stream));
-  MOE_CUDA(moe::launch_grouped_gemm_mx(&g1, &g2, offsets, E, L.pad_rows, done, d->status, stream));
+  MOE_CUDA(moe::launch_grouped_gemm_mx(&g1, &g2, offsets, E, L.pad, L.pad_rows, done, d->status,
+                                         stream));
   if (t_gemm_ev_end) MOE_CUDA(cudaEventRecord(t_gemm_ev_end, stream));
   MOE_CUDA(moe::launch_finalize(y2, w, eri_pad, T, k, H, out, stream));
   return MOE_OK;
+}
+
+}  // namespace
+
+moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w, float eps,
+                          const float* Wg, const float* logits_override, const void* w13_q,
+                          const void* w13_sf, const void* down_q, const void* down_sf, int T,
+                          int H, int E, int k, int I, moe_bf16* out, moe_bf16* residual_out,
+                          int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  return forward_mx_impl(x, r, norm_w, eps, Wg, logits_override, w13_q, w13_sf, down_q, down_sf, T,
+                         H, E, k, I, out, residual_out, topk_ids_out, topk_w_out, ws, ws_bytes,
+                         false, stream);
+}
+
+// ------------------------------------------------------------------ W4A8 --
+size_t moe_packed_weight_bytes_mx4(int E, int H, int I, int which) {
+  if (E < 1 || H < 1 || I < 1) return 0;
+  const size_t w = (size_t)E * H * I;
+  switch (which) {
+    case 0: return w;           // 2I x H e2m1 codes per expert, two per byte
+    case 1: return 2 * w / 32;
+    case 2: return w / 2;
+    case 3: return w / 32;
+    default: return 0;
+  }
+}
+
+moe_status moe_pack_weights_mx4(const moe_bf16* w13, const moe_bf16* down, int E, int H, int I,
+                                void* w13_q, void* w13_sf, void* down_q, void* down_sf,
+                                moe_stream_t stream) {
+  if ((w13 && (!w13_q || !w13_sf)) || (down && (!down_q || !down_sf))) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > 256 || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  MOE_CUDA(moe::launch_pack_mx4(w13, down, E, H, I, static_cast<uint8_t*>(w13_q),
+                                static_cast<uint8_t*>(w13_sf), static_cast<uint8_t*>(down_q),
+                                static_cast<uint8_t*>(down_sf), stream));
+  return MOE_OK;
+}
+
+size_t moe_forward_w4a8_workspace_size(int T, int H, int E, int k, int I) {
+  return moe_forward_mx_workspace_size(T, H, E, k, I);
+}
+
+moe_status moe_forward_w4a8(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w,
+                            float eps, const float* Wg, const float* logits_override,
+                            const void* w13_q, const void* w13_sf, const void* down_q,
+                            const void* down_sf, int T, int H, int E, int k, int I, moe_bf16* out,
+                            moe_bf16* residual_out, int32_t* topk_ids_out, float* topk_w_out,
+                            void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return forward_mx_impl(x, r, norm_w, eps, Wg, logits_override, w13_q, w13_sf, down_q, down_sf, T,
+                         H, E, k, I, out, residual_out, topk_ids_out, topk_w_out, ws, ws_bytes,
+                         true, stream);
 }
 
 // --------------------------------------------------------------- next rows --

@@ -12,8 +12,13 @@
 //    rows x 4 blocks each, loaded with 1-D bulk copies); the MMA thread copies them
 //    into a per-stage TMEM slot with tcgen05.cp before the stage's four MMAs, and
 //    MMA kk uses byte kk of each scale word;
-//  - the expert-sorted activations are padded so each expert starts on a 128-row
-//    boundary (one token block = one scale atom per K step);
+//  - the expert-sorted activations are padded so each expert starts on a kPad-row
+//    boundary, with one scale atom per kPad-row block and K step;
+//  - two tile shapes: 128 x 128 with 128-row activation boxes and kPad = 128 for
+//    prefill, and a decode shape of 128 x 32 with 16-row boxes, a deeper ring and
+//    kPad = 32.  With kPad = 32 a tile's B scales always sit in the first TMEM
+//    column of the copied atom, so the MMA's scale address is never offset by a
+//    32-row group (a one-column offset was rejected as a misaligned address);
 //  - the gate/up epilogue applies SwiGLU and MX-quantises h along I (a warp's 32
 //    lanes hold one 32-feature block of one token), writing e4m3 codes and scale
 //    atoms that the down projection then reads.
@@ -29,25 +34,30 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBN = 128;
 constexpr int kBK = 128;                          // fp8 elements per stage (128 bytes)
-constexpr int kBoxRows = 128;
 constexpr int kThreads = 256;
 constexpr int kMaxE = 256;
-constexpr int kStages = 6;
 constexpr int kABytes = kBM * kBK;                // 16 KB
-constexpr int kBBytes = kBN * kBK;                // 16 KB
-constexpr int kBoxBytes = kBoxRows * kBK;         // 16 KB
 constexpr int kSfBytes = 512;                     // one scale atom
 constexpr int kEpiBytes = (4 * 16 * 33 + 2 * 32 * 33) * 4;  // SwiGLU exchange + h tile
-constexpr int kAccCols = kBN;                     // per accumulator
-constexpr int kSfCol = 2 * kAccCols;              // first scale-factor TMEM column
-constexpr int kTmemCols = 512;
 
-struct L {
+// Tile shape: kBN tokens per unit, kStages pipeline stages, B boxes of kBoxRows rows.
+template <int BN_, int STAGES_, int BOX_, int PAD_>
+struct MxShape {
+  static constexpr int kBN = BN_;
+  static constexpr int kPad = PAD_;                    // row padding of each expert block
+  static constexpr int kStages = STAGES_;
+  static constexpr int kBoxRows = BOX_;
+  static constexpr int kBBytes = kBN * kBK;
+  static constexpr int kBoxBytes = kBoxRows * kBK;
+  static constexpr int kAccCols = kBN;                 // per accumulator
+  static constexpr int kSfCol = 2 * kAccCols;          // first scale-factor TMEM column
+  static constexpr int kColsUsed = kSfCol + 8 * kStages;
+  static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512);
+  // smem layout
   static constexpr int kA = 0;
   static constexpr int kB = kA + kStages * kABytes;
-  static constexpr int kSf = kB + kStages * kBBytes;              // per stage: SFA, SFB
+  static constexpr int kSf = kB + kStages * kBBytes;   // per stage: SFA, SFB
   static constexpr int kEpi = kSf + kStages * 2 * kSfBytes;
   static constexpr int kBar = kEpi + kEpiBytes;
   static constexpr int kNumBars = 2 * kStages + 5;
@@ -56,7 +66,12 @@ struct L {
   static constexpr int kEnd = kTables + (4 * (kMaxE + 1) + 8) * 4;
   static constexpr int kSmemBytes = kEnd + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kColsUsed <= 512, "tensor memory budget");
+  static_assert(kBN % 32 == 0 && kPad == kBN && kBN % kBoxRows == 0, "tile shape");
+  static_assert(kBBytes % 1024 == 0 && kBoxBytes % 1024 == 0, "swizzle atoms");
 };
+using ShapePrefill = MxShape<128, 6, 128, 128>;
+using ShapeDecode = MxShape<32, 9, 16, 32>;
 
 struct MxArgs {
   const int32_t* offsets;
@@ -65,6 +80,7 @@ struct MxArgs {
   int MW[2];
   int ld[2];
   int active[2];
+  int a_fp4[2];             // A is e2m1 (TMA-unpacked to 16-byte groups) instead of e4m3
   const uint8_t* a_sf[2];   // weight scale atoms [E][MW/128][K/128][512]
   const uint8_t* b_sf[2];   // activation scale atoms [Ppad/128][K/128][512]
   uint8_t* hq;              // phase-0 output codes (Ppad, ld0)
@@ -85,6 +101,7 @@ struct Tables {
   int E;
 };
 
+template <int kBN>
 __device__ __forceinline__ Unit decode_unit(int u, const Tables& tb) {
   Unit r;
   const int total0 = tb.uoff[0][tb.E];
@@ -141,11 +158,16 @@ __device__ __forceinline__ uint8_t mx_code(float v, int X) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3));
 }
 
+template <class S>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA0,
                            const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmA1,
                            const __grid_constant__ CUtensorMap tmB1, const MxArgs args) {
+  constexpr int kBN = S::kBN, kStages = S::kStages, kBoxRows = S::kBoxRows, kPad = S::kPad;
+  constexpr int kBBytes = S::kBBytes, kBoxBytes = S::kBoxBytes;
+  constexpr int kAccCols = S::kAccCols, kSfCol = S::kSfCol, kTmemCols = S::kTmemCols;
+  using L = S;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -204,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nb = (m + kBN - 1) / kBN;
       v[0] = args.active[0] ? nb * (args.MW[0] / kBM) : 0;
       v[1] = args.active[1] ? nb * (args.MW[1] / kBM) : 0;
-      v[2] = nb * kBN;
+      v[2] = ((m + kPad - 1) / kPad) * kPad;
     }
     int* dsts[3] = {s_uoff0, s_uoff1, s_poff};
     for (int p = 0; p < 3; ++p) {
@@ -240,14 +262,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer --
       // weight tiles are re-read by every 128-token block of their expert
-      const uint64_t pol_w = l2_policy_evict_normal();
+      const uint64_t pol_w = kBN <= 32 ? l2_policy_evict_first() : l2_policy_evict_normal();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t par = 0;
       uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, tb);
+        const Unit t = decode_unit<kBN>(u, tb);
         if (t.ph == 1 && args.done != nullptr) {
           const int m = s_off[t.e + 1] - s_off[t.e];
           const int need = ((m + kBN - 1) / kBN) * (args.MW[0] / kBM);
@@ -262,18 +284,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int K = args.K[t.ph];
         const int nk = K / kBK;
         const int nbox = (t.rows + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = kABytes + nbox * kBoxBytes + 2 * kSfBytes;
+        // an e2m1 tile fills the same 16 KB of smem as an e4m3 one (each 16-code group
+        // padded to 16 bytes), but only its 8 KB of packed codes count as transferred
+        const uint32_t abytes = args.a_fp4[t.ph] ? kABytes / 2 : kABytes;
+        const uint32_t bytes = abytes + nbox * kBoxBytes + 2 * kSfBytes;
         const int arow = t.e * args.MW[t.ph] + t.mb * kBM;
+        const int atile0 = (t.e * (args.MW[t.ph] / kBM) + t.mb) * nk;
         const uint8_t* asf =
             args.a_sf[t.ph] + ((size_t)(t.e * (args.MW[t.ph] / kBM) + t.mb) * nk) * kSfBytes;
-        const uint8_t* bsf = args.b_sf[t.ph] + ((size_t)(t.row0 / kBN) * nk) * kSfBytes;
+        const uint8_t* bsf = args.b_sf[t.ph] + ((size_t)(t.row0 / kPad) * nk) * kSfBytes;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sA + stage * kABytes, ta, &full[stage], kb * kBK, arow, pol_w);
+          if (args.a_fp4[t.ph])  // tile-major e2m1: tile (e, mb, kb) is rows [128 * tile, +128)
+            tma_load_2d(sA + stage * kABytes, ta, &full[stage], 0, (atile0 + kb) * kBM, pol_w);
+          else
+            tma_load_2d(sA + stage * kABytes, ta, &full[stage], kb * kBK, arow, pol_w);
           for (int j = 0; j < nbox; ++j)
             tma_load_2d(sB + stage * kBBytes + j * kBoxBytes, tbm, &full[stage], kb * kBK,
                         t.row0 + j * kBoxRows, pol_x);
@@ -314,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t par = 0, apar = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, tb);
+        const Unit t = decode_unit<kBN>(u, tb);
         const int n = (t.rows + 15) & ~15;
         if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort)) {
           ok = false;
@@ -339,7 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 32; ++kk)
             tc_mma_mxf8(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32),
-                        idesc_mxf8_f32(kBM, n, kk, kk), sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
+                        idesc_mxf8_f32(kBM, n, kk, kk) | (args.a_fp4[t.ph] ? (5u << 7) : 0u), sfa_t,
+                        sfb_t, (kb | kk) ? 1u : 0u);
           tc_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
@@ -366,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t apar = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit t = decode_unit(u, tb);
+      const Unit t = decode_unit<kBN>(u, tb);
       if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort) ? 1 : 0;
       named_bar_sync(1, 128);
       const int ok = s_flag[0];
@@ -436,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(args.hq + (size_t)prow * ld + t.mb * 64 + 32 * pblk +
                                       16 * half) = make_uint4(w[0], w[1], w[2], w[3]);
             if (half == 0) {
-              uint8_t* atom = args.h_sf + ((size_t)(prow / 128) * ksteps + ks) * kSfBytes;
-              atom[(prow & 31) * 16 + ((prow >> 5) & 3) * 4 + kbq] = static_cast<uint8_t>(X + 127);
+              uint8_t* atom = args.h_sf + ((size_t)(prow / kPad) * ksteps + ks) * kSfBytes;
+              atom[(prow & 31) * 16 + ((prow % kPad) >> 5) * 4 + kbq] = static_cast<uint8_t>(X + 127);
             }
           }
           named_bar_sync(bar_id, 64);
@@ -492,11 +522,17 @@ bool encode_tmap_2d_u8(CUtensorMap* tm, const void* base, uint64_t inner, uint64
                         box_rows);
 }
 
-}  // namespace
+// Tile-major packed e2m1 weights seen as (E * MW * K / 128) rows of 128 codes (64
+// bytes); TMA unpacks each 16-code group into 8 data bytes + 8 gap bytes, so a
+// 128 x 128 box fills the same 16 KB of 128-byte smem rows as an e4m3 tile.
+bool encode_tmap_2d_fp4(CUtensorMap* tm, const void* base, uint64_t rows) {
+  return encode_tmap_2d_strided(tm, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, base, kBK, rows,
+                                kBK / 2, kBK, kBM);
+}
 
-cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1,
-                                   const int32_t* offsets, int E, int P_pad_rows, int* done,
-                                   int* status, cudaStream_t s) {
+template <class S>
+cudaError_t launch_shape(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1, const int32_t* offsets,
+                         int E, int P_pad_rows, int* done, int* status, cudaStream_t s) {
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -506,8 +542,8 @@ cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph
     std::lock_guard<std::mutex> lk(mu);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-      err = cudaFuncSetAttribute(grouped_gemm_mx_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+      err = cudaFuncSetAttribute(grouped_gemm_mx_kernel<S>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
       if (err != cudaSuccess) return err;
       attr_set[dev] = true;
     }
@@ -527,10 +563,14 @@ cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph
     a.ld[p] = g->n_out;
     a.a_sf[p] = g->A_sf;
     a.b_sf[p] = g->B_sf;
-    if (!encode_tmap_2d_u8(&tm[2 * p], g->A_q, (uint64_t)g->K, (uint64_t)E * g->MW, kBK, kBM))
-      return cudaErrorInvalidValue;
+    a.a_fp4[p] = g->a_fp4 ? 1 : 0;
+    const bool ok_a =
+        g->a_fp4 ? encode_tmap_2d_fp4(&tm[2 * p], g->A_q, (uint64_t)E * g->MW * (g->K / kBK))
+                 : encode_tmap_2d_u8(&tm[2 * p], g->A_q, (uint64_t)g->K, (uint64_t)E * g->MW, kBK,
+                                     kBM);
+    if (!ok_a) return cudaErrorInvalidValue;
     if (!encode_tmap_2d_u8(&tm[2 * p + 1], g->B_q, (uint64_t)g->K, (uint64_t)P_pad_rows, kBK,
-                           kBoxRows))
+                           S::kBoxRows))
       return cudaErrorInvalidValue;
   }
   if (ph0) {
@@ -541,14 +581,27 @@ cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(device_sm_count(), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = a.done != nullptr ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_kernel, tm[0], tm[1], tm[2], tm[3], a);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_kernel<S>, tm[0], tm[1], tm[2], tm[3], a);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1,
+                                   const int32_t* offsets, int E, int pad, int P_pad_rows,
+                                   int* done, int* status, cudaStream_t s) {
+  // few tokens per expert: narrow tiles and a deeper ring keep more weight bytes in flight
+  if (pad == ShapeDecode::kPad)
+    return launch_shape<ShapeDecode>(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
+  if (pad == ShapePrefill::kPad)
+    return launch_shape<ShapePrefill>(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

@@ -118,9 +118,16 @@ cudaError_t launch_mx_quantize(const float* y, int rows, int n, uint8_t* q, uint
 cudaError_t launch_pack_mx(const uint16_t* w13, const uint16_t* down, int E, int H, int I,
                            uint8_t* w13q, uint8_t* w13sf, uint8_t* downq, uint8_t* downsf,
                            cudaStream_t s);
+cudaError_t launch_pack_mx4(const uint16_t* w13, const uint16_t* down, int E, int H, int I,
+                            uint8_t* w13q, uint8_t* w13sf, uint8_t* downq, uint8_t* downsf,
+                            cudaStream_t s);
+// Row padding of the expert-sorted MX activations, and with it the block-scaled
+// GEMM's tile shape: 32 (narrow tiles, one scale atom per 32 rows) when the layer
+// has at most 16 token-expert pairs per expert on average, else 128.
+inline int mx_pad_rows(long long P, int E) { return P <= 16LL * E ? 32 : 128; }
 cudaError_t launch_mx_expand(const uint8_t* xq, const uint8_t* xs, const int32_t* ids,
                              const int32_t* eri, const int32_t* offsets, int E, int P, int H,
-                             int k, uint8_t* xe, uint8_t* xe_sf, int32_t* eri_pad,
+                             int k, int pad, uint8_t* xe, uint8_t* xe_sf, int32_t* eri_pad,
                              cudaStream_t s);
 struct GemmPhaseMx {
   const void* A_q;          // packed e4m3 weights, rows = E * MW, K bytes each
@@ -131,10 +138,13 @@ struct GemmPhaseMx {
   uint8_t* out_sf;          // phase 0: h scale atoms
   uint16_t* out_bf16;       // phase 1: y (rows, n_out)
   int K, MW, n_out;
+  bool a_fp4 = false;       // weights are packed e2m1 (two per byte) instead of e4m3
 };
+// pad = mx_pad_rows(P, E) of the activation layout (selects the tile shape);
+// P_pad_rows = rows of that padded layout.
 cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1,
-                                   const int32_t* offsets, int E, int P_pad_rows, int* done,
-                                   int* status, cudaStream_t s);
+                                   const int32_t* offsets, int E, int pad, int P_pad_rows,
+                                   int* done, int* status, cudaStream_t s);
 
 // ---- next rows (norm_route2.cu)
 cudaError_t launch_add_rmsnorm_cast(const uint16_t* x, const uint16_t* r, const uint16_t* w,
@@ -156,5 +166,9 @@ bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t elem_by
                     uint32_t box_rows);
 bool encode_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                          uint32_t box_inner, uint32_t box_rows);
+// Explicit row pitch (bytes), for packed sub-byte element types.
+bool encode_tmap_2d_strided(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base,
+                            uint64_t inner, uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
+                            uint32_t box_rows);
 
 }  // namespace moe

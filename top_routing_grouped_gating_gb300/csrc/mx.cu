@@ -20,6 +20,7 @@
 // Weight scales are stored as atoms per (expert, 128-row block, K step); the
 // expert-sorted activations are padded so every expert starts on a 128-row
 // boundary and their scales are atoms per (128-row group, K step).
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -198,15 +199,74 @@ __global__ void __launch_bounds__(256) pack_mx_kernel(const uint16_t* __restrict
   }
 }
 
-// Expert-sorted, 128-row-padded expansion of MX activations: pair j (token t = j/k,
-// expert e, unpadded row p = eri[j]) goes to padded row
-//   prow = poff[e] + (p - off[e]),  poff[e] = sum_{e' < e} roundup(count[e'], 128).
-// Copies the H code bytes of token t and its H/32 scales (into atoms), and
-// records prow in eri_pad[j].  One warp per pair.
+// MXFP4 (e2m1 + E8M0/32) pre-quantisation of weights along K, same row order and
+// scale atoms as pack_mx_kernel: X = floor(log2 amax) - 2 (6 = 1.5 * 2^2 is e2m1's
+// largest value), codes e2m1(v / 2^X) nearest-even, saturating.  Codes are packed
+// two per byte, element 2i in the low nibble, and stored tile-major: the 128 rows
+// x 128 K-elements of one (expert, 128-row block, K step) tile are 8 KB of
+// consecutive memory, row after row (64 bytes each), so the GEMM reads every
+// weight tile as one contiguous block.
+template <bool kW13>
+__global__ void __launch_bounds__(256) pack_mx4_kernel(const uint16_t* __restrict__ w, int K,
+                                                       int ncols, int I, uint8_t* __restrict__ q,
+                                                       uint8_t* __restrict__ sf) {
+  __shared__ float tile[128][33];
+  const int k0 = blockIdx.x * 128, r0 = blockIdx.y * 32, e = blockIdx.z;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  int col0;
+  if (kW13) {
+    const int blk = r0 / 128, within = r0 % 128;
+    col0 = within < 64 ? blk * 64 + within : I + blk * 64 + (within - 64);
+  } else {
+    col0 = r0;
+  }
+  for (int i = ty; i < 128; i += 8)
+    tile[i][tx] = __uint_as_float(static_cast<uint32_t>(
+                                      w[((size_t)e * K + k0 + i) * ncols + col0 + tx])
+                                  << 16);
+  __syncthreads();
+  const int rows_total = ncols;
+  const int ksteps = K / 128;
+  for (int rr = 0; rr < 4; ++rr) {
+    const int lr = ty * 4 + rr;
+    const int row = r0 + lr;
+    for (int kb = 0; kb < 4; ++kb) {
+      const float v = tile[kb * 32 + tx][lr];
+      float amax = fabsf(v);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const uint32_t bits = __float_as_uint(amax);
+      const int ef = static_cast<int>((bits >> 23) & 0xFF);
+      int X = ef == 0 ? -127 : ef - 127 - 2;
+      X = X < -127 ? -127 : (X > 127 ? 127 : X);
+      const int nx = -X, a = nx > 126 ? 126 : nx;
+      const float scaled = v * exp2i(a) * exp2i(nx - a);
+      const uint32_t c =
+          static_cast<uint32_t>(__nv_cvt_float_to_fp4(scaled, __NV_E2M1, cudaRoundNearest)) & 15u;
+      const uint32_t hi = __shfl_down_sync(0xffffffffu, c, 1);
+      if ((tx & 1) == 0)
+        q[(((size_t)e * (rows_total / 128) + row / 128) * ksteps + k0 / 128) * 8192 +
+          (row & 127) * 64 + (kb * 32 + tx) / 2] =
+            static_cast<uint8_t>(c | (hi << 4));
+      if (tx == 0) {
+        const size_t atom = ((size_t)e * (rows_total / 128) + row / 128) * ksteps + k0 / 128;
+        sf[atom * 512 + atom_offset(row & 127, kb)] = static_cast<uint8_t>(X + 127);
+      }
+    }
+  }
+}
+
+// Expert-sorted, padded expansion of MX activations: pair j (token t = j/k, expert
+// e, unpadded row p = eri[j]) goes to padded row
+//   prow = poff[e] + (p - off[e]),  poff[e] = sum_{e' < e} roundup(count[e'], pad),
+// pad = 128 (one scale atom per 128 rows) or 32 (one atom per 32 rows, only its
+// first 32-row group used: the narrow-tile GEMM shape).  Copies the H code bytes of
+// token t and its H/32 scales (into atoms), and records prow in eri_pad[j].  One
+// warp per pair.
 __global__ void __launch_bounds__(256) mx_expand_kernel(
     const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, const int32_t* __restrict__ ids,
     const int32_t* __restrict__ eri, const int32_t* __restrict__ offsets, int E, int P, int H, int k,
-    uint8_t* __restrict__ xe, uint8_t* __restrict__ xe_sf, int32_t* __restrict__ eri_pad) {
+    int pad, uint8_t* __restrict__ xe, uint8_t* __restrict__ xe_sf, int32_t* __restrict__ eri_pad) {
   pdl_wait();
   pdl_trigger();
   __shared__ int s_poff[257];
@@ -218,7 +278,7 @@ __global__ void __launch_bounds__(256) mx_expand_kernel(
     int acc = 0;
     for (int e = 0; e < E; ++e) {
       s_poff[e] = acc;
-      acc += ((s_off[e + 1] - s_off[e] + 127) / 128) * 128;
+      acc += ((s_off[e + 1] - s_off[e] + pad - 1) / pad) * pad;
     }
     s_poff[E] = acc;
   }
@@ -238,9 +298,9 @@ __global__ void __launch_bounds__(256) mx_expand_kernel(
   uint4* dst = reinterpret_cast<uint4*>(xe + (size_t)prow * H);
   for (int v = lane; v < H / 16; v += 32) dst[v] = src[v];
   const int ksteps = H / 128;
-  uint8_t* atoms = xe_sf + (size_t)(prow / 128) * ksteps * 512;
+  uint8_t* atoms = xe_sf + (size_t)(prow / pad) * ksteps * 512;
   for (int b = lane; b < H / 32; b += 32)
-    atoms[(size_t)(b / 4) * 512 + atom_offset(prow & 127, b & 3)] = xs[(size_t)t * (H / 32) + b];
+    atoms[(size_t)(b / 4) * 512 + atom_offset(prow % pad, b & 3)] = xs[(size_t)t * (H / 32) + b];
 }
 
 }  // namespace
@@ -283,13 +343,29 @@ cudaError_t launch_pack_mx(const uint16_t* w13, const uint16_t* down, int E, int
   return cudaGetLastError();
 }
 
+cudaError_t launch_pack_mx4(const uint16_t* w13, const uint16_t* down, int E, int H, int I,
+                            uint8_t* w13q, uint8_t* w13sf, uint8_t* downq, uint8_t* downsf,
+                            cudaStream_t s) {
+  dim3 block(32, 8);
+  if (w13 != nullptr) {
+    dim3 grid(H / 128, 2 * I / 32, E);
+    pack_mx4_kernel<true><<<grid, block, 0, s>>>(w13, H, 2 * I, I, w13q, w13sf);
+  }
+  if (down != nullptr) {
+    dim3 grid(I / 128, H / 32, E);
+    pack_mx4_kernel<false><<<grid, block, 0, s>>>(down, I, H, I, downq, downsf);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_mx_expand(const uint8_t* xq, const uint8_t* xs, const int32_t* ids,
                              const int32_t* eri, const int32_t* offsets, int E, int P, int H,
-                             int k, uint8_t* xe, uint8_t* xe_sf, int32_t* eri_pad,
+                             int k, int pad, uint8_t* xe, uint8_t* xe_sf, int32_t* eri_pad,
                              cudaStream_t s) {
+  if (pad != 32 && pad != 128) return cudaErrorInvalidValue;
   const int blocks = (P + 7) / 8;
   return launch_pdl(mx_expand_kernel, dim3(blocks), dim3(256), 0, s, xq, xs, ids, eri, offsets, E,
-                    P, H, k, xe, xe_sf, eri_pad);
+                    P, H, k, pad, xe, xe_sf, eri_pad);
 }
 
 }  // namespace moe

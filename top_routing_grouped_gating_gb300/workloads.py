@@ -37,6 +37,7 @@ class MoEConfig:
     router: str = "uniform"   # "uniform" or "zipf"
     zipf_s: float = 1.2
     mx: bool = False          # MXFP8 variant (add + RMSNorm + MX quant in front)
+    w4: bool = False          # with mx: MXFP4 expert weights (W4A8)
     prenorm: bool = False     # bf16 layer with fused add + RMSNorm + cast in front
     Z: int = 0                # zero-computation (identity) experts after the E routed ones
     ep_ranks: int = 0         # > 0: routing of one expert-parallel rank's experts only
@@ -58,6 +59,10 @@ CONFIGS: Dict[str, MoEConfig] = {
     "qwen3_235b_a22b_prefill": MoEConfig("qwen3_235b_a22b_prefill", T=8192, H=4096, E=128, k=8,
                                          I=1536),
     "mxfp8_prefill": MoEConfig("mxfp8_prefill", T=4096, H=4096, E=128, k=8, I=1536, mx=True),
+    "mxfp8_decode": MoEConfig("mxfp8_decode", T=64, H=4096, E=128, k=8, I=1536, mx=True),
+    # W4A8: the MXFP8 layer with MXFP4 (e2m1 + E8M0/32) expert weights, Qwen3-235B shape
+    "w4a8_prefill": MoEConfig("w4a8_prefill", T=4096, H=4096, E=128, k=8, I=1536, mx=True, w4=True),
+    "w4a8_decode": MoEConfig("w4a8_decode", T=64, H=4096, E=128, k=8, I=1536, mx=True, w4=True),
     # next rows: fused add+RMSNorm+cast in front of the decode layer; identity experts
     "qwen3_30b_a3b_decode_prenorm": MoEConfig("qwen3_30b_a3b_decode_prenorm", T=32, H=2048, E=128, k=8,
                                               I=768, prenorm=True),
