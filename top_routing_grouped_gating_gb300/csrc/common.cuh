@@ -233,6 +233,13 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_f32(int M, int N, uint32_t sfa
          | (sfa_id << 29);                           // A scale-factor byte
 }
 
+// The scale-factor byte fields of a kind::mxf8f6f4 instruction descriptor alone.
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t sfa_id, uint32_t sfb_id) {
+  return (sfb_id << 4) | (sfa_id << 29);
+}
+static_assert((idesc_mxf8_f32(128, 64, 0, 0) | idesc_sf_ids(3, 2)) == idesc_mxf8_f32(128, 64, 3, 2),
+              "scale-factor id fields");
+
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format: f32

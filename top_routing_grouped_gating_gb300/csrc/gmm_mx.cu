@@ -42,9 +42,13 @@ constexpr int kSfBytes = 512;                     // one scale atom
 constexpr int kEpiBytes = (4 * 16 * 33 + 2 * 32 * 33) * 4;  // SwiGLU exchange + h tile
 
 // Tile shape: kBN tokens per unit, kStages pipeline stages, B boxes of kBoxRows rows.
-template <int BN_, int STAGES_, int BOX_, int PAD_>
+template <int BN_, int STAGES_, int BOX_, int PAD_, bool PAIR_>
 struct MxShape {
   static constexpr int kBN = BN_;
+  // Stage release and scale readiness signalled per pair of stages (fewer barrier
+  // operations on the MMA thread, but a shorter producer lookahead).
+  static constexpr bool kPair = PAIR_;
+  static constexpr int kGroup = kPair ? 2 : 1;
   static constexpr int kPad = PAD_;                    // row padding of each expert block
   static constexpr int kStages = STAGES_;
   static constexpr int kBoxRows = BOX_;
@@ -60,7 +64,7 @@ struct MxShape {
   static constexpr int kSf = kB + kStages * kBBytes;   // per stage: SFA, SFB
   static constexpr int kEpi = kSf + kStages * 2 * kSfBytes;
   static constexpr int kBar = kEpi + kEpiBytes;
-  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kNumBars = kStages + 2 * (kStages / kGroup) + 6;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTables = kMisc + 16;
   static constexpr int kEnd = kTables + (4 * (kMaxE + 1) + 8) * 4;
@@ -69,9 +73,13 @@ struct MxShape {
   static_assert(kColsUsed <= 512, "tensor memory budget");
   static_assert(kBN % 32 == 0 && kPad == kBN && kBN % kBoxRows == 0, "tile shape");
   static_assert(kBBytes % 1024 == 0 && kBoxBytes % 1024 == 0, "swizzle atoms");
+  static_assert(kStages % kGroup == 0, "stages are released and signalled in pairs");
 };
-using ShapePrefill = MxShape<128, 6, 128, 128>;
-using ShapeDecode = MxShape<32, 9, 16, 32>;
+using ShapePrefill = MxShape<128, 6, 128, 128, false>;
+// e4m3 decode is bound by HBM bytes in flight (more stages); e2m1 decode moves half
+// the bytes per stage and is bound by the MMA thread's issue rate (paired barriers)
+using ShapeDecode = MxShape<32, 9, 16, 32, false>;
+using ShapeDecodeFp4 = MxShape<32, 8, 16, 32, true>;
 
 struct MxArgs {
   const int32_t* offsets;
@@ -177,9 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sEpi = smem + L::kEpi;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  // empty[g] / sfready[g] cover the stages of group g (one stage, or the pair 2g, 2g + 1)
+  constexpr int kG = S::kGroup, kNG = kStages / kG;
+  uint64_t* sfready = empty + kNG;
+  uint64_t* tfull = sfready + kNG;
   uint64_t* tempty = tfull + 2;
-  uint64_t* fin = tempty + 2;
+  uint64_t* fin = tempty + 2;            // MMA issuer's drain on abort
+  uint64_t* fin_sf = fin + 1;            // scale copier's drain on abort
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   int* s_off = reinterpret_cast<int*>(smem + L::kTables);
@@ -193,15 +205,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 2);  // weight + activation producer
+    for (int g = 0; g < kNG; ++g) {
+      mbar_init(&empty[g], 1);
+      mbar_init(&sfready[g], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 4);
     }
     mbar_init(fin, 1);
+    mbar_init(fin_sf, 1);
     *s_abort = 0;
     fence_barrier_init();
   }
@@ -258,135 +272,190 @@ __global__ void __launch_bounds__(kThreads, 1)
   tb.E = E;
   const int total = s_uoff0[E] + s_uoff1[E];
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------ TMA producer --
-      // weight tiles are re-read by every 128-token block of their expert
-      const uint64_t pol_w = kBN <= 32 ? l2_policy_evict_first() : l2_policy_evict_normal();
-      const uint64_t pol_x = l2_policy_evict_last();
-      int stage = 0;
-      uint32_t par = 0;
-      uint32_t issued_mask = 0, issued_par = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit t = decode_unit<kBN>(u, tb);
-        if (t.ph == 1 && args.done != nullptr) {
-          const int m = s_off[t.e + 1] - s_off[t.e];
-          const int need = ((m + kBN - 1) / kBN) * (args.MW[0] / kBM);
-          if (!wait_counter(args.done + t.e, need, s_abort)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_global();
+  // Each tcgen05 / TMA instruction costs its issuing thread tens of clocks, so the
+  // per-stage issue work is spread over four single-thread roles: weight loads
+  // (warp 0), activation loads (warp 2), scale-atom copies into TMEM (warp 3) and
+  // the MMAs (warp 1).  A stage is full when both producers' bytes have landed.
+  // Scale readiness and stage release are signalled per group of kG stages (with
+  // pairs, one commit and one wait per pair instead of per stage): sfready[g] when
+  // the copier's tcgen05.cp of the group are done, empty[g] when its MMAs are done
+  // (that also retires the copies, which ran before them).  A CTA's last stage
+  // closes its group even when the group is not complete.
+  int my_stages = 0;   // stages this CTA runs (closes the last pair)
+  {
+    const int total0 = s_uoff0[E];
+    const int g = gridDim.x, b = blockIdx.x;
+    const int mine = b < total ? (total - b + g - 1) / g : 0;
+    const int mine0 = b < total0 ? (total0 - b + g - 1) / g : 0;
+    my_stages = mine0 * (args.K[0] / kBK) + (mine - mine0) * (args.K[1] / kBK);
+  }
+  if ((warp == 0 || warp == 2) && lane == 0) {
+    // ------------------------------------------------------ TMA producers --
+    const bool weights = warp == 0;
+    // weight tiles are re-read by every token block of their expert
+    const uint64_t pol_w = kBN <= 32 ? l2_policy_evict_first() : l2_policy_evict_normal();
+    const uint64_t pol_x = l2_policy_evict_last();
+    int stage = 0;
+    uint32_t par = 0;
+    uint32_t issued_mask = 0, issued_par = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit t = decode_unit<kBN>(u, tb);
+      if (!weights && t.ph == 1 && args.done != nullptr) {
+        // the down projection's activations are h of this expert's gate/up units
+        const int m = s_off[t.e + 1] - s_off[t.e];
+        const int need = ((m + kBN - 1) / kBN) * (args.MW[0] / kBM);
+        if (!wait_counter(args.done + t.e, need, s_abort)) {
+          ok = false;
+          break;
         }
-        const CUtensorMap* ta = t.ph ? &tmA1 : &tmA0;
-        const CUtensorMap* tbm = t.ph ? &tmB1 : &tmB0;
-        const int K = args.K[t.ph];
-        const int nk = K / kBK;
-        const int nbox = (t.rows + kBoxRows - 1) / kBoxRows;
-        // an e2m1 tile fills the same 16 KB of smem as an e4m3 one (each 16-code group
-        // padded to 16 bytes), but only its 8 KB of packed codes count as transferred
-        const uint32_t abytes = args.a_fp4[t.ph] ? kABytes / 2 : kABytes;
-        const uint32_t bytes = abytes + nbox * kBoxBytes + 2 * kSfBytes;
-        const int arow = t.e * args.MW[t.ph] + t.mb * kBM;
-        const int atile0 = (t.e * (args.MW[t.ph] / kBM) + t.mb) * nk;
-        const uint8_t* asf =
-            args.a_sf[t.ph] + ((size_t)(t.e * (args.MW[t.ph] / kBM) + t.mb) * nk) * kSfBytes;
-        const uint8_t* bsf = args.b_sf[t.ph] + ((size_t)(t.row0 / kPad) * nk) * kSfBytes;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[stage], bytes);
+        fence_proxy_async_global();
+      }
+      const int K = args.K[t.ph];
+      const int nk = K / kBK;
+      const int nbox = (t.rows + kBoxRows - 1) / kBoxRows;
+      // an e2m1 tile fills the same 16 KB of smem as an e4m3 one (each 16-code group
+      // padded to 16 bytes), but only its 8 KB of packed codes count as transferred
+      const uint32_t abytes = args.a_fp4[t.ph] ? kABytes / 2 : kABytes;
+      const uint32_t bytes = weights ? abytes + kSfBytes : nbox * kBoxBytes + kSfBytes;
+      const CUtensorMap* tm = weights ? (t.ph ? &tmA1 : &tmA0) : (t.ph ? &tmB1 : &tmB0);
+      const int arow = t.e * args.MW[t.ph] + t.mb * kBM;
+      const int atile0 = (t.e * (args.MW[t.ph] / kBM) + t.mb) * nk;
+      const uint8_t* sfsrc =
+          weights ? args.a_sf[t.ph] + ((size_t)(t.e * (args.MW[t.ph] / kBM) + t.mb) * nk) * kSfBytes
+                  : args.b_sf[t.ph] + ((size_t)(t.row0 / kPad) * nk) * kSfBytes;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (stage % kG == 0 && !mbar_wait(&empty[stage / kG], par ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], bytes);
+        uint8_t* sf = sSF + stage * 2 * kSfBytes + (weights ? 0 : kSfBytes);
+        if (weights) {
           if (args.a_fp4[t.ph])  // tile-major e2m1: tile (e, mb, kb) is rows [128 * tile, +128)
-            tma_load_2d(sA + stage * kABytes, ta, &full[stage], 0, (atile0 + kb) * kBM, pol_w);
+            tma_load_2d(sA + stage * kABytes, tm, &full[stage], 0, (atile0 + kb) * kBM, pol_w);
           else
-            tma_load_2d(sA + stage * kABytes, ta, &full[stage], kb * kBK, arow, pol_w);
+            tma_load_2d(sA + stage * kABytes, tm, &full[stage], kb * kBK, arow, pol_w);
+          bulk_load_1d(sf, sfsrc + (size_t)kb * kSfBytes, kSfBytes, &full[stage], pol_w);
+        } else {
           for (int j = 0; j < nbox; ++j)
-            tma_load_2d(sB + stage * kBBytes + j * kBoxBytes, tbm, &full[stage], kb * kBK,
+            tma_load_2d(sB + stage * kBBytes + j * kBoxBytes, tm, &full[stage], kb * kBK,
                         t.row0 + j * kBoxRows, pol_x);
-          uint8_t* sf = sSF + stage * 2 * kSfBytes;
-          bulk_load_1d(sf, asf + (size_t)kb * kSfBytes, kSfBytes, &full[stage], pol_w);
-          bulk_load_1d(sf + kSfBytes, bsf + (size_t)kb * kSfBytes, kSfBytes, &full[stage], pol_x);
-          issued_mask |= 1u << stage;
-          issued_par = (issued_par & ~(1u << stage)) | (par << stage);
-          if (++stage == kStages) {
-            stage = 0;
-            par ^= 1u;
-          }
+          bulk_load_1d(sf, sfsrc + (size_t)kb * kSfBytes, kSfBytes, &full[stage], pol_x);
         }
-      }
-      if (ok) {
-        for (int i = 0; i < kStages; ++i) {
-          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
-            ok = false;
-            break;
-          }
-          if (++stage == kStages) {
-            stage = 0;
-            par ^= 1u;
-          }
+        issued_mask |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (par << stage);
+        if (++stage == kStages) {
+          stage = 0;
+          par ^= 1u;
         }
-      }
-      if (!ok) {
-        *s_abort = 1;
-        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-        for (int s = 0; s < kStages; ++s)
-          if ((issued_mask >> s) & 1u) mbar_wait(&full[s], (issued_par >> s) & 1u, nullptr);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // -------------------------------------------------------- MMA issuer --
-      int stage = 0, acc = 0;
-      uint32_t par = 0, apar = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit t = decode_unit<kBN>(u, tb);
-        const int n = (t.rows + 15) & ~15;
-        if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort)) {
+    if (ok && weights) {
+      // all stage groups released: no MMA still reads this CTA's shared memory
+      if (stage % kG) stage += kG - stage % kG;   // a partly used group was closed early
+      if (stage == kStages) {
+        stage = 0;
+        par ^= 1u;
+      }
+      for (int i = 0; i < kNG; ++i) {
+        if (!mbar_wait(&empty[stage / kG], par ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        stage += kG;
+        if (stage == kStages) {
+          stage = 0;
+          par ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      *s_abort = 1;
+      flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+      // let this thread's copies land before the CTA can exit (bounded waits)
+      for (int s2 = 0; s2 < kStages; ++s2)
+        if ((issued_mask >> s2) & 1u) mbar_wait(&full[s2], (issued_par >> s2) & 1u, nullptr);
+    }
+  } else if (warp == 3 && lane == 0) {
+    // --------------------------------------------------- scale-atom copier --
+    int stage = 0, done_stages = 0;
+    uint32_t par = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit t = decode_unit<kBN>(u, tb);
+      const int nk = args.K[t.ph] / kBK;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(&full[stage], par, s_abort)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
-        const int nk = args.K[t.ph] / kBK;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&full[stage], par, s_abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * 8);
-          const uint32_t sfb_t = sfa_t + 4;
-          const uint32_t sf_s = smem_u32(sSF + stage * 2 * kSfBytes);
-          tc_cp_32x128b_warpx4(sfa_t, smem_desc_noswz(sf_s, 128));
-          tc_cp_32x128b_warpx4(sfb_t, smem_desc_noswz(sf_s + kSfBytes, 128));
-          const uint32_t a0 = smem_u32(sA + stage * kABytes);
-          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 32; ++kk)
-            tc_mma_mxf8(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32),
-                        idesc_mxf8_f32(kBM, n, kk, kk) | (args.a_fp4[t.ph] ? (5u << 7) : 0u), sfa_t,
-                        sfb_t, (kb | kk) ? 1u : 0u);
-          tc_commit(&empty[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            par ^= 1u;
-          }
+        const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * 8);
+        const uint32_t sf_s = smem_u32(sSF + stage * 2 * kSfBytes);
+        tc_cp_32x128b_warpx4(sfa_t, smem_desc_noswz(sf_s, 128));
+        tc_cp_32x128b_warpx4(sfa_t + 4, smem_desc_noswz(sf_s + kSfBytes, 128));
+        ++done_stages;
+        if (stage % kG == kG - 1 || done_stages == my_stages) tc_commit(&sfready[stage / kG]);
+        if (++stage == kStages) {
+          stage = 0;
+          par ^= 1u;
         }
-        if (!ok) break;
-        tc_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) apar ^= 1u;
       }
-      if (!ok) {
-        *s_abort = 1;
-        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-        tc_commit(fin);
-        mbar_wait(fin, 0, nullptr);
+    }
+    if (!ok) {
+      *s_abort = 1;
+      flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+      tc_commit(fin_sf);
+      mbar_wait(fin_sf, 0, nullptr);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // -------------------------------------------------------- MMA issuer --
+    int stage = 0, acc = 0, done_stages = 0;
+    uint32_t par = 0, apar = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit t = decode_unit<kBN>(u, tb);
+      const int n = (t.rows + 15) & ~15;
+      const uint32_t idesc0 = idesc_mxf8_f32(kBM, n, 0, 0) | (args.a_fp4[t.ph] ? (5u << 7) : 0u);
+      if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort)) {
+        ok = false;
+        break;
       }
+      tc_fence_after_sync();
+      const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+      const int nk = args.K[t.ph] / kBK;
+      for (int kb = 0; kb < nk; ++kb) {
+        // the scales' copy completing implies the stages' operands have landed
+        if (stage % kG == 0 && !mbar_wait(&sfready[stage / kG], par, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * 8);
+        const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * kABytes));
+        const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
+#pragma unroll
+        for (int kk = 0; kk < kBK / 32; ++kk)   // +32 bytes along K = +2 in the start field
+          tc_mma_mxf8(d, adesc + 2 * kk, bdesc + 2 * kk, idesc0 | idesc_sf_ids(kk, kk), sfa_t,
+                      sfa_t + 4, (kb | kk) ? 1u : 0u);
+        ++done_stages;
+        if (stage % kG == kG - 1 || done_stages == my_stages) tc_commit(&empty[stage / kG]);
+        if (++stage == kStages) {
+          stage = 0;
+          par ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit(&tfull[acc]);
+      acc ^= 1;
+      if (acc == 0) apar ^= 1u;
+    }
+    if (!ok) {
+      *s_abort = 1;
+      flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+      tc_commit(fin);
+      mbar_wait(fin, 0, nullptr);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue --
@@ -597,8 +666,11 @@ cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph
                                    const int32_t* offsets, int E, int pad, int P_pad_rows,
                                    int* done, int* status, cudaStream_t s) {
   // few tokens per expert: narrow tiles and a deeper ring keep more weight bytes in flight
-  if (pad == ShapeDecode::kPad)
+  if (pad == ShapeDecode::kPad) {
+    const bool fp4 = (ph0 ? ph0->a_fp4 : false) || (ph1 ? ph1->a_fp4 : false);
+    if (fp4) return launch_shape<ShapeDecodeFp4>(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
     return launch_shape<ShapeDecode>(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
+  }
   if (pad == ShapePrefill::kPad)
     return launch_shape<ShapePrefill>(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
   return cudaErrorInvalidValue;
