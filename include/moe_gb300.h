@@ -248,6 +248,35 @@ MOE_API moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const mo
                                   float* topk_w_out, void* ws, size_t ws_bytes,
                                   moe_stream_t stream);
 
+/* Standalone block-scaled grouped GEMMs (§高性能专家计算 grouped_matmul on MXFP8
+ * operands; SwiGLU from §计算分解; h MX-quantised as in moe_forward_mx).
+ *   A_q (P,K) e4m3 codes of expert-sorted rows (expert e owns rows
+ *   [expert_offsets[e], expert_offsets[e+1])), A_scale (P,K/32) E8M0 bytes, row-major
+ *   (the layout moe_mx_quantize and moe_add_rmsnorm_mxquant produce);
+ *   weights from moe_pack_weights_mx (weight_format 0, e4m3) or moe_pack_weights_mx4
+ *   (weight_format 1, e2m1; code buffer 32-byte aligned); expert_offsets (E+1) int32
+ *   on the device, offsets[E] <= P.
+ * moe_grouped_matmul_swiglu_mx: g = A.w13[e][:, :N], u = A.w13[e][:, N:] (fp32
+ *   accumulation), h = SiLU(g) * u, MX-quantised along N: h_q (P,N) e4m3 and
+ *   h_scale (P,N/32) E8M0, row-major.  N = I.
+ * moe_grouped_matmul_mx: y = A.w[e] (fp32 accumulation) rounded once to bf16, y (P,N).
+ * Rows at or past expert_offsets[E] are neither read nor written.  K % 128 == 0,
+ * N % 128 == 0, E <= 256.  ws >= moe_grouped_matmul_mx_workspace_size(E,P,K,N,swiglu)
+ * bytes, 256-byte aligned (the rows are re-laid out there with each expert padded for
+ * the block-scaled tensor-core tiles). */
+MOE_API size_t moe_grouped_matmul_mx_workspace_size(int E, int P, int K, int N, int swiglu);
+MOE_API moe_status moe_grouped_matmul_swiglu_mx(const uint8_t* A_q, const uint8_t* A_scale,
+                                                const void* w13_q, const void* w13_sf,
+                                                int weight_format, const int32_t* expert_offsets,
+                                                int E, int P, int K, int N, uint8_t* h_q,
+                                                uint8_t* h_scale, void* ws, size_t ws_bytes,
+                                                moe_stream_t stream);
+MOE_API moe_status moe_grouped_matmul_mx(const uint8_t* A_q, const uint8_t* A_scale,
+                                         const void* w_q, const void* w_sf, int weight_format,
+                                         const int32_t* expert_offsets, int E, int P, int K, int N,
+                                         moe_bf16* y, void* ws, size_t ws_bytes,
+                                         moe_stream_t stream);
+
 /* ------------------------------------------------------------------ W4A8 --
  * The MXFP8 layer with MXFP4 expert weights (W4A8: 4-bit weights, 8-bit
  * activations).  Page "基于Atlas A3、950训练/推理集群的Qwen3-MoE模型低时延推理性能优化实践",

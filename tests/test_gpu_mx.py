@@ -186,3 +186,61 @@ def test_forward_mx_with_gpu_router(cuda_dev):
     ref = O.moe_forward_mx(to_np(inp["x"])[rows], to_np(inp["r"])[rows], to_np(inp["norm_w"]), cfg.eps, None,
                            LazyExperts(inp["w13"]), LazyExperts(inp["down"]), cfg.k, logits32=lg[rows])
     assert rel_fro(to_np(out)[rows], ref["out"]) <= REL_FRO_MX
+
+
+@pytest.mark.parametrize("T,E,k,H,I,fmt", [
+    (64, 8, 2, 256, 128, 0),      # P <= 16E: narrow tiles, 32-row padding
+    (64, 8, 2, 256, 128, 1),
+    (300, 4, 2, 256, 256, 0),     # wide tiles, 128-row padding, experts over 128 rows
+    (300, 4, 2, 512, 128, 1),
+])
+def test_grouped_gemms_mx_match_oracle(cuda_dev, T, E, k, H, I, fmt):
+    """Standalone block-scaled GEMMs on expert-sorted MX rows.  The activations are
+    MX-quantised by the oracle from seeded fp32 data; expected values are the oracle's
+    fp64 products of the dequantised operands (h then MX-quantised along I)."""
+    rng = np.random.default_rng(T + E + fmt)
+    ids = W.make_topk_ids(T, E, k, seed=T + 3)
+    rt = O.init_routing(to_np(ids), E)
+    P = T * k
+    A = rng.standard_normal((P, H)).astype(np.float32)
+    Aq, Asc = O.mx_quantize(A.astype(np.float64))
+    Adq = O.mx_dequantize(Aq, Asc)
+    g = torch.Generator().manual_seed(T + 11)
+    w13 = (torch.randn(E, H, 2 * I, generator=g) * 0.05).to(torch.bfloat16)
+    down = (torch.randn(E, I, H, generator=g) * 0.05).to(torch.bfloat16)
+    pack = moe.pack_weights_mx4 if fmt else moe.pack_weights_mx
+    rt_w = O.mx4_roundtrip if fmt else O.mx_roundtrip
+    w13_q, w13_sf, down_q, down_sf = pack(w13.to(cuda_dev), down.to(cuda_dev))
+    off = torch.from_numpy(rt["offsets"].astype(np.int32)).to(cuda_dev)
+    Aq_d = torch.from_numpy(Aq).to(cuda_dev)
+    Asc_d = torch.from_numpy(Asc).to(cuda_dev)
+    h_q, h_sc = moe.grouped_matmul_swiglu_mx(Aq_d, Asc_d, w13_q, w13_sf, off, E, I, weight_format=fmt)
+    # down projection on its own seeded MX rows (no GPU output feeds the oracle)
+    A2 = rng.standard_normal((P, I)).astype(np.float32)
+    A2q, A2sc = O.mx_quantize(A2.astype(np.float64))
+    y = moe.grouped_matmul_mx(torch.from_numpy(A2q).to(cuda_dev), torch.from_numpy(A2sc).to(cuda_dev),
+                              down_q, down_sf, off, E, H, weight_format=fmt)
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 0
+    offs = rt["offsets"]
+    h_ref = np.zeros((P, I))
+    y_ref = np.zeros((P, H))
+    A2dq = O.mx_dequantize(A2q, A2sc)
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi == lo:
+            continue
+        h_ref[lo:hi] = O.swiglu(Adq[lo:hi] @ rt_w(to_np(w13[e]).astype(np.float64), axis=0))
+        y_ref[lo:hi] = A2dq[lo:hi] @ rt_w(to_np(down[e]).astype(np.float64), axis=0)
+    # y: one bf16 rounding after fp32 accumulation of exactly representable products
+    assert rel_fro(to_np(y).astype(np.float64), y_ref) <= 5e-3
+    # h: the GPU quantises its fp32 h; codes and scales match the oracle's quantisation
+    # of the fp64 h except where the two sit on opposite sides of a rounding boundary
+    rq, rsc = O.mx_quantize(h_ref)
+    got = O.mx_dequantize(to_np(h_q).astype(np.uint8), to_np(h_sc).astype(np.uint8))
+    ref = O.mx_dequantize(rq, rsc)
+    diff = got != ref
+    assert diff.mean() < 2e-3, diff.mean()
+    step = np.exp2(np.repeat(rsc.astype(np.float64), 32, axis=1) - 127) * 2.0 ** -2
+    assert np.all(np.abs(got - ref)[diff] <= np.maximum(np.abs(ref[diff]) * 2.0 ** -3, step[diff]))
+    assert (to_np(h_sc) != rsc).mean() < 2e-3

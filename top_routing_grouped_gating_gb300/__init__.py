@@ -32,6 +32,8 @@ from ._binding import (  # noqa: F401
     get_device_status,
     grouped_matmul,
     grouped_matmul_swiglu,
+    grouped_matmul_mx,
+    grouped_matmul_swiglu_mx,
     init_routing,
     lib,
     library_path,

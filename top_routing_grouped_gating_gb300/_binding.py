@@ -66,6 +66,11 @@ _SIGS = {
     "moe_forward_w4a8_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "moe_forward_w4a8": (_c_int, [_vp, _vp, _vp, _c_float, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                   _c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "moe_grouped_matmul_mx_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "moe_grouped_matmul_swiglu_mx": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int,
+                                              _vp, _vp, _vp, _c_size, _vp]),
+    "moe_grouped_matmul_mx": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _vp,
+                                       _vp, _c_size, _vp]),
     "moe_init_routing_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp,
                                           _vp]),
 }
@@ -408,6 +413,44 @@ def pack_weights_mx(w13: torch.Tensor, down: torch.Tensor):
 def pack_weights_mx4(w13: torch.Tensor, down: torch.Tensor):
     """As pack_weights_mx with MXFP4 codes, two e2m1 codes per byte (low nibble first)."""
     return _pack_block_scaled(w13, down, "mx4")
+
+
+def _gemm_mx(A_q, A_scale, w_q, w_sf, expert_offsets, E, N, weight_format, swiglu):
+    _need(A_q, "A_q", torch.uint8)
+    dev = A_q.device
+    _need(A_scale, "A_scale", torch.uint8, dev)
+    _need(expert_offsets, "expert_offsets", torch.int32, dev)
+    P, K = A_q.shape
+    L = lib()
+    with torch.cuda.device(dev):
+        need = int(L.moe_grouped_matmul_mx_workspace_size(E, P, K, N, int(swiglu)))
+        if need == 0:
+            raise ValueError("unsupported block-scaled GEMM shape")
+        ws = _ws(need, dev)
+        if swiglu:
+            h_q = torch.empty(P, N, dtype=torch.uint8, device=dev)
+            h_sc = torch.empty(P, N // 32, dtype=torch.uint8, device=dev)
+            _check("moe_grouped_matmul_swiglu_mx",
+                   L.moe_grouped_matmul_swiglu_mx(_ptr(A_q), _ptr(A_scale), _ptr(w_q), _ptr(w_sf), weight_format,
+                                                  _ptr(expert_offsets), E, P, K, N, _ptr(h_q), _ptr(h_sc),
+                                                  _ptr(ws), ws.numel(), _stream(dev)))
+            return h_q, h_sc
+        y = torch.empty(P, N, dtype=torch.bfloat16, device=dev)
+        _check("moe_grouped_matmul_mx",
+               L.moe_grouped_matmul_mx(_ptr(A_q), _ptr(A_scale), _ptr(w_q), _ptr(w_sf), weight_format,
+                                       _ptr(expert_offsets), E, P, K, N, _ptr(y), _ptr(ws), ws.numel(),
+                                       _stream(dev)))
+        return y
+
+
+def grouped_matmul_swiglu_mx(A_q, A_scale, w13_q, w13_sf, expert_offsets, E: int, I: int, weight_format: int = 0):
+    """Block-scaled grouped GEMM + SwiGLU on expert-sorted MX rows -> (h codes (P,I), h scales (P,I/32))."""
+    return _gemm_mx(A_q, A_scale, w13_q, w13_sf, expert_offsets, E, I, weight_format, True)
+
+
+def grouped_matmul_mx(A_q, A_scale, w_q, w_sf, expert_offsets, E: int, N: int, weight_format: int = 0):
+    """Block-scaled grouped GEMM on expert-sorted MX rows -> y (P,N) bf16."""
+    return _gemm_mx(A_q, A_scale, w_q, w_sf, expert_offsets, E, N, weight_format, False)
 
 
 class MoELayerMX:

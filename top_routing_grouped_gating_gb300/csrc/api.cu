@@ -720,6 +720,119 @@ moe_status moe_pack_weights_mx4(const moe_bf16* w13, const moe_bf16* down, int E
   return MOE_OK;
 }
 
+// ------------------------------------------- standalone block-scaled GEMMs --
+namespace {
+
+struct GemmMxLayout {
+  size_t xq, xsf, row_map, oq, osf, obf, total;
+  int pad, rows;
+};
+
+GemmMxLayout gemm_mx_layout(int E, int P, int K, int N, bool swiglu) {
+  GemmMxLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  const size_t R = (((size_t)P + 127) / 128) * 128 + 128 * (size_t)E;
+  L.rows = (int)R;
+  L.pad = moe::mx_pad_rows((long long)P, E);
+  L.xq = take(R * K);
+  L.xsf = take(R / L.pad * (K / 128) * 512);
+  L.row_map = take((size_t)P * 4);
+  if (swiglu) {
+    L.oq = take(R * N);
+    L.osf = take(R / L.pad * (N / 128) * 512);
+  } else {
+    L.obf = take(R * N * 2);
+  }
+  L.total = o;
+  return L;
+}
+
+moe_status check_gemm_mx_shape(int E, int P, int K, int N) {
+  if (E < 1 || E > 256 || P < 1 || K < 128 || N < 128 || K % 128 != 0 || N % 128 != 0)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)P + 128LL * E + 128 >= (1LL << 31) / 4 || K > 32768 || N > 32768)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+moe_status gemm_mx_common(const uint8_t* A_q, const uint8_t* A_scale, const void* w_q,
+                          const void* w_sf, int weight_format, const int32_t* offsets, int E,
+                          int P, int K, int N, bool swiglu, uint8_t* h_q, uint8_t* h_scale,
+                          moe_bf16* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!A_q || !A_scale || !w_q || !w_sf || !offsets) return MOE_ERR_INVALID_ARG;
+  if (swiglu ? (!h_q || !h_scale) : !y) return MOE_ERR_INVALID_ARG;
+  if (weight_format != 0 && weight_format != 1) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(A_q) || !aligned16(w_q) || !aligned16(w_sf) ||
+      (swiglu ? !aligned16(h_q) : !aligned16(y)))
+    return MOE_ERR_INVALID_ARG;
+  if (weight_format == 1 && (reinterpret_cast<uintptr_t>(w_q) & 31u)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_gemm_mx_shape(E, P, K, N));
+  const GemmMxLayout L = gemm_mx_layout(E, P, K, N, swiglu);
+  if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_WORKSPACE;
+  DeviceFacts* d = nullptr;
+  MOE_TRY(current_device(&d));
+  uint8_t* xq = at<uint8_t>(ws, L.xq);
+  uint8_t* xsf = at<uint8_t>(ws, L.xsf);
+  int32_t* row_map = at<int32_t>(ws, L.row_map);
+  MOE_CUDA(moe::launch_mx_pad_sorted(A_q, A_scale, offsets, E, P, K, L.pad, xq, xsf, row_map,
+                                     stream));
+  moe::GemmPhaseMx g{};
+  g.A_q = w_q;
+  g.A_sf = static_cast<const uint8_t*>(w_sf);
+  g.B_q = xq;
+  g.B_sf = xsf;
+  g.K = K;
+  g.n_out = N;
+  g.a_fp4 = weight_format == 1;
+  if (swiglu) {
+    g.MW = 2 * N;
+    g.out_q = at<uint8_t>(ws, L.oq);
+    g.out_sf = at<uint8_t>(ws, L.osf);
+    MOE_CUDA(moe::launch_grouped_gemm_mx(&g, nullptr, offsets, E, L.pad, L.rows, nullptr,
+                                         d->status, stream));
+    MOE_CUDA(moe::launch_mx_unpad(g.out_q, g.out_sf, nullptr, row_map, offsets + E, P, N, L.pad,
+                                  h_q, h_scale, nullptr, stream));
+  } else {
+    g.MW = N;
+    g.out_bf16 = at<uint16_t>(ws, L.obf);
+    MOE_CUDA(moe::launch_grouped_gemm_mx(nullptr, &g, offsets, E, L.pad, L.rows, nullptr,
+                                         d->status, stream));
+    MOE_CUDA(moe::launch_mx_unpad(nullptr, nullptr, g.out_bf16, row_map, offsets + E, P, N, L.pad,
+                                  nullptr, nullptr, y, stream));
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+size_t moe_grouped_matmul_mx_workspace_size(int E, int P, int K, int N, int swiglu) {
+  if (check_gemm_mx_shape(E, P, K, N) != MOE_OK) return 0;
+  return gemm_mx_layout(E, P, K, N, swiglu != 0).total;
+}
+
+moe_status moe_grouped_matmul_swiglu_mx(const uint8_t* A_q, const uint8_t* A_scale,
+                                        const void* w13_q, const void* w13_sf, int weight_format,
+                                        const int32_t* expert_offsets, int E, int P, int K, int N,
+                                        uint8_t* h_q, uint8_t* h_scale, void* ws, size_t ws_bytes,
+                                        moe_stream_t stream) {
+  return gemm_mx_common(A_q, A_scale, w13_q, w13_sf, weight_format, expert_offsets, E, P, K, N,
+                        true, h_q, h_scale, nullptr, ws, ws_bytes, stream);
+}
+
+moe_status moe_grouped_matmul_mx(const uint8_t* A_q, const uint8_t* A_scale, const void* w_q,
+                                 const void* w_sf, int weight_format,
+                                 const int32_t* expert_offsets, int E, int P, int K, int N,
+                                 moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return gemm_mx_common(A_q, A_scale, w_q, w_sf, weight_format, expert_offsets, E, P, K, N, false,
+                        nullptr, nullptr, y, ws, ws_bytes, stream);
+}
+
 size_t moe_forward_w4a8_workspace_size(int T, int H, int E, int k, int I) {
   return moe_forward_mx_workspace_size(T, H, E, k, I);
 }

@@ -121,6 +121,13 @@ cudaError_t launch_pack_mx(const uint16_t* w13, const uint16_t* down, int E, int
 cudaError_t launch_pack_mx4(const uint16_t* w13, const uint16_t* down, int E, int H, int I,
                             uint8_t* w13q, uint8_t* w13sf, uint8_t* downq, uint8_t* downsf,
                             cudaStream_t s);
+// Expert-sorted MX rows <-> the padded GEMM layout (standalone block-scaled GEMMs).
+cudaError_t launch_mx_pad_sorted(const uint8_t* q, const uint8_t* sc, const int32_t* offsets,
+                                 int E, int P, int K, int pad, uint8_t* out_q, uint8_t* out_sf,
+                                 int32_t* row_map, cudaStream_t s);
+cudaError_t launch_mx_unpad(const uint8_t* pq, const uint8_t* psf, const uint16_t* pbf,
+                            const int32_t* row_map, const int32_t* offsets_end, int P, int N,
+                            int pad, uint8_t* q, uint8_t* sc, uint16_t* y, cudaStream_t s);
 // Row padding of the expert-sorted MX activations, and with it the block-scaled
 // GEMM's tile shape: 32 (narrow tiles, one scale atom per 32 rows) when the layer
 // has at most 16 token-expert pairs per expert on average, else 128.

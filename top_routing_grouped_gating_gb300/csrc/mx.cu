@@ -303,7 +303,91 @@ __global__ void __launch_bounds__(256) mx_expand_kernel(
     atoms[(size_t)(b / 4) * 512 + atom_offset(prow % pad, b & 3)] = xs[(size_t)t * (H / 32) + b];
 }
 
+// Expert-sorted MX rows (row p of expert e = the e-th block of `offsets`, codes (P, K)
+// and row-major scales (P, K/32)) into the padded layout of mx_expand_kernel.
+// row_map[p] = padded row.  One warp per row; rows at or past offsets[E] are skipped.
+__global__ void __launch_bounds__(256) mx_pad_sorted_kernel(
+    const uint8_t* __restrict__ q, const uint8_t* __restrict__ sc,
+    const int32_t* __restrict__ offsets, int E, int P, int K, int pad, uint8_t* __restrict__ out_q,
+    uint8_t* __restrict__ out_sf, int32_t* __restrict__ row_map) {
+  __shared__ int s_poff[257];
+  __shared__ int s_off[257];
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int i = tid; i <= E; i += blockDim.x) s_off[i] = offsets[i];
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      s_poff[e] = acc;
+      acc += ((s_off[e + 1] - s_off[e] + pad - 1) / pad) * pad;
+    }
+    s_poff[E] = acc;
+  }
+  __syncthreads();
+  const int p = (blockIdx.x * blockDim.x + tid) >> 5;
+  if (p >= P || p >= s_off[E]) return;
+  int lo = 0, hi = E;  // s_off[lo] <= p < s_off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_off[mid] <= p) lo = mid;
+    else hi = mid;
+  }
+  const int prow = s_poff[lo] + (p - s_off[lo]);
+  if (lane == 0) row_map[p] = prow;
+  const uint4* src = reinterpret_cast<const uint4*>(q + (size_t)p * K);
+  uint4* dst = reinterpret_cast<uint4*>(out_q + (size_t)prow * K);
+  for (int v = lane; v < K / 16; v += 32) dst[v] = src[v];
+  const int ksteps = K / 128;
+  uint8_t* atoms = out_sf + (size_t)(prow / pad) * ksteps * 512;
+  for (int b = lane; b < K / 32; b += 32)
+    atoms[(size_t)(b / 4) * 512 + atom_offset(prow % pad, b & 3)] = sc[(size_t)p * (K / 32) + b];
+}
+
+// The inverse for GEMM outputs: padded MX rows (codes + scale atoms) or padded bf16
+// rows back to expert-sorted rows p < offsets[E].  One warp per row.
+__global__ void __launch_bounds__(256) mx_unpad_kernel(
+    const uint8_t* __restrict__ pq, const uint8_t* __restrict__ psf,
+    const uint16_t* __restrict__ pbf, const int32_t* __restrict__ row_map,
+    const int32_t* __restrict__ offsets_end, int P, int N, int pad, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ sc, uint16_t* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (p >= P || p >= *offsets_end) return;
+  const int prow = row_map[p];
+  if (pbf != nullptr) {
+    const uint4* src = reinterpret_cast<const uint4*>(pbf + (size_t)prow * N);
+    uint4* dst = reinterpret_cast<uint4*>(y + (size_t)p * N);
+    for (int v = lane; v < N / 8; v += 32) dst[v] = src[v];
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(pq + (size_t)prow * N);
+  uint4* dst = reinterpret_cast<uint4*>(q + (size_t)p * N);
+  for (int v = lane; v < N / 16; v += 32) dst[v] = src[v];
+  const int ksteps = N / 128;
+  const uint8_t* atoms = psf + (size_t)(prow / pad) * ksteps * 512;
+  for (int b = lane; b < N / 32; b += 32)
+    sc[(size_t)p * (N / 32) + b] = atoms[(size_t)(b / 4) * 512 + atom_offset(prow % pad, b & 3)];
+}
+
 }  // namespace
+
+cudaError_t launch_mx_pad_sorted(const uint8_t* q, const uint8_t* sc, const int32_t* offsets,
+                                 int E, int P, int K, int pad, uint8_t* out_q, uint8_t* out_sf,
+                                 int32_t* row_map, cudaStream_t s) {
+  if (pad != 32 && pad != 128) return cudaErrorInvalidValue;
+  mx_pad_sorted_kernel<<<(P + 7) / 8, 256, 0, s>>>(q, sc, offsets, E, P, K, pad, out_q, out_sf,
+                                                    row_map);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_unpad(const uint8_t* pq, const uint8_t* psf, const uint16_t* pbf,
+                            const int32_t* row_map, const int32_t* offsets_end, int P, int N,
+                            int pad, uint8_t* q, uint8_t* sc, uint16_t* y, cudaStream_t s) {
+  if (pad != 32 && pad != 128) return cudaErrorInvalidValue;
+  mx_unpad_kernel<<<(P + 7) / 8, 256, 0, s>>>(pq, psf, pbf, row_map, offsets_end, P, N, pad, q, sc,
+                                               y);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_add_rmsnorm_mxquant(const uint16_t* x, const uint16_t* r, const uint16_t* w,
                                        float eps, int T, int H, uint16_t* residual_out,
