@@ -42,9 +42,15 @@ constexpr int kSfBytes = 512;                     // one scale atom
 constexpr int kEpiBytes = (4 * 16 * 33 + 2 * 32 * 33) * 4;  // SwiGLU exchange + h tile
 
 // Tile shape: kBN tokens per unit, kStages pipeline stages, B boxes of kBoxRows rows.
-template <int BN_, int STAGES_, int BOX_, int PAD_, bool PAIR_>
+// With kAbsorb > 0 an expert's last token block takes up to kAbsorb rows beyond kBN
+// (instead of a separate, nearly empty block whose MMAs would cost as much issue time
+// as a full one); those rows come in one extra kAbsorb-row box, and their B scales
+// are the next 128-row atom, copied into the next four TMEM columns.
+template <int BN_, int STAGES_, int BOX_, int PAD_, bool PAIR_, int ABSORB_>
 struct MxShape {
   static constexpr int kBN = BN_;
+  static constexpr int kAbsorb = ABSORB_;
+  static constexpr int kMaxRows = kBN + kAbsorb;      // largest token block
   // Stage release and scale readiness signalled per pair of stages (fewer barrier
   // operations on the MMA thread, but a shorter producer lookahead).
   static constexpr bool kPair = PAIR_;
@@ -52,17 +58,23 @@ struct MxShape {
   static constexpr int kPad = PAD_;                    // row padding of each expert block
   static constexpr int kStages = STAGES_;
   static constexpr int kBoxRows = BOX_;
-  static constexpr int kBBytes = kBN * kBK;
+  static constexpr int kBBytes = kMaxRows * kBK;
   static constexpr int kBoxBytes = kBoxRows * kBK;
-  static constexpr int kAccCols = kBN;                 // per accumulator
-  static constexpr int kSfCol = 2 * kAccCols;          // first scale-factor TMEM column
-  static constexpr int kColsUsed = kSfCol + 8 * kStages;
+  // B scale atoms per stage (one per 128 rows of the largest block), plus one for A
+  static constexpr int kSfAtoms = 1 + (kMaxRows + 127) / 128;
+  static constexpr int kSfStageCols = 4 * kSfAtoms;
+  // TMEM: accumulator 1 starts kAccStride columns after accumulator 0 (a power of two);
+  // the scale slots sit after accumulator 0 when kMaxRows is not a power of two
+  static constexpr bool kPow2 = (kMaxRows & (kMaxRows - 1)) == 0;
+  static constexpr int kAccStride = kPow2 ? kMaxRows : 256;
+  static constexpr int kSfCol = kPow2 ? 2 * kMaxRows : kMaxRows;
+  static constexpr int kColsUsed = kPow2 ? kSfCol + kSfStageCols * kStages : kAccStride + kMaxRows;
   static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512);
   // smem layout
   static constexpr int kA = 0;
   static constexpr int kB = kA + kStages * kABytes;
-  static constexpr int kSf = kB + kStages * kBBytes;   // per stage: SFA, SFB
-  static constexpr int kEpi = kSf + kStages * 2 * kSfBytes;
+  static constexpr int kSf = kB + kStages * kBBytes;   // per stage: SFA, SFB atoms
+  static constexpr int kEpi = kSf + kStages * kSfAtoms * kSfBytes;
   static constexpr int kBar = kEpi + kEpiBytes;
   static constexpr int kNumBars = kStages + 2 * (kStages / kGroup) + 6;
   static constexpr int kMisc = kBar + kNumBars * 8;
@@ -71,15 +83,32 @@ struct MxShape {
   static constexpr int kSmemBytes = kEnd + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kColsUsed <= 512, "tensor memory budget");
+  static_assert(kPow2 || kSfCol + kSfStageCols * kStages <= kAccStride, "scale slots fit");
   static_assert(kBN % 32 == 0 && kPad == kBN && kBN % kBoxRows == 0, "tile shape");
-  static_assert(kBBytes % 1024 == 0 && kBoxBytes % 1024 == 0, "swizzle atoms");
+  static_assert(kAbsorb % 16 == 0 && kAbsorb < kBN && kMaxRows <= 256, "absorbed rows");
+  static_assert(kBBytes % 1024 == 0 && kBoxBytes % 1024 == 0 && (kBN * kBK) % 1024 == 0,
+                "swizzle atoms");
   static_assert(kStages % kGroup == 0, "stages are released and signalled in pairs");
 };
-using ShapePrefill = MxShape<128, 6, 128, 128, false>;
+using ShapePrefill = MxShape<128, 5, 128, 128, false, 32>;
 // e4m3 decode is bound by HBM bytes in flight (more stages); e2m1 decode moves half
 // the bytes per stage and is bound by the MMA thread's issue rate (paired barriers)
-using ShapeDecode = MxShape<32, 9, 16, 32, false>;
-using ShapeDecodeFp4 = MxShape<32, 8, 16, 32, true>;
+using ShapeDecode = MxShape<32, 9, 16, 32, false, 0>;
+using ShapeDecodeFp4 = MxShape<32, 8, 16, 32, true, 0>;
+
+// Token blocks of an expert with m rows: blocks of kBN, the last one taking up to
+// kAbsorb more (never empty: (nb - 1) * kBN < m - kAbsorb when nb > 1).
+template <int kBN, int kAbsorb>
+__host__ __device__ constexpr int token_blocks(int m) {
+  return m <= 0 ? 0
+                : (kAbsorb ? ((m - kAbsorb + kBN - 1) / kBN > 1 ? (m - kAbsorb + kBN - 1) / kBN : 1)
+                           : (m + kBN - 1) / kBN);
+}
+static_assert(token_blocks<128, 32>(0) == 0 && token_blocks<128, 32>(1) == 1 &&
+                  token_blocks<128, 32>(160) == 1 && token_blocks<128, 32>(161) == 2 &&
+                  token_blocks<128, 32>(288) == 2 && token_blocks<128, 32>(289) == 3 &&
+                  token_blocks<32, 0>(33) == 2,
+              "token blocks");
 
 struct MxArgs {
   const int32_t* offsets;
@@ -109,7 +138,7 @@ struct Tables {
   int E;
 };
 
-template <int kBN>
+template <int kBN, int kAbsorb>
 __device__ __forceinline__ Unit decode_unit(int u, const Tables& tb) {
   Unit r;
   const int total0 = tb.uoff[0][tb.E];
@@ -125,11 +154,11 @@ __device__ __forceinline__ Unit decode_unit(int u, const Tables& tb) {
   r.e = lo;
   const int local = u - uo[lo];
   const int m = tb.off[lo + 1] - tb.off[lo];
-  const int nb = (m + kBN - 1) / kBN;
+  const int nb = token_blocks<kBN, kAbsorb>(m);
   r.mb = local / nb;
   r.nb = local - r.mb * nb;
   r.row0 = tb.poff[lo] + r.nb * kBN;
-  r.rows = min(kBN, m - r.nb * kBN);
+  r.rows = r.nb == nb - 1 ? m - r.nb * kBN : kBN;
   return r;
 }
 
@@ -171,10 +200,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA0,
                            const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmA1,
-                           const __grid_constant__ CUtensorMap tmB1, const MxArgs args) {
+                           const __grid_constant__ CUtensorMap tmB1,
+                           const __grid_constant__ CUtensorMap tmX0,   // absorbed-row boxes
+                           const __grid_constant__ CUtensorMap tmX1, const MxArgs args) {
   constexpr int kBN = S::kBN, kStages = S::kStages, kBoxRows = S::kBoxRows, kPad = S::kPad;
+  constexpr int kAbsorb = S::kAbsorb, kSfAtoms = S::kSfAtoms, kSfStageCols = S::kSfStageCols;
   constexpr int kBBytes = S::kBBytes, kBoxBytes = S::kBoxBytes;
-  constexpr int kAccCols = S::kAccCols, kSfCol = S::kSfCol, kTmemCols = S::kTmemCols;
+  constexpr int kAccStride = S::kAccStride, kSfCol = S::kSfCol, kTmemCols = S::kTmemCols;
   using L = S;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -224,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB0);
     tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB1);
+    if (kAbsorb) {
+      tma_prefetch_desc(&tmX0);
+      tma_prefetch_desc(&tmX1);
+    }
   }
   if (warp == 2) {
     tmem_alloc(s_tmem, kTmemCols);
@@ -237,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int v[3] = {0, 0, 0};
     if (tid < E) {
       const int m = s_off[tid + 1] - s_off[tid];
-      const int nb = (m + kBN - 1) / kBN;
+      const int nb = token_blocks<kBN, kAbsorb>(m);
       v[0] = args.active[0] ? nb * (args.MW[0] / kBM) : 0;
       v[1] = args.active[1] ? nb * (args.MW[1] / kBM) : 0;
       v[2] = ((m + kPad - 1) / kPad) * kPad;
@@ -300,11 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued_mask = 0, issued_par = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit t = decode_unit<kBN>(u, tb);
+      const Unit t = decode_unit<kBN, kAbsorb>(u, tb);
       if (!weights && t.ph == 1 && args.done != nullptr) {
         // the down projection's activations are h of this expert's gate/up units
         const int m = s_off[t.e + 1] - s_off[t.e];
-        const int need = ((m + kBN - 1) / kBN) * (args.MW[0] / kBM);
+        const int need = token_blocks<kBN, kAbsorb>(m) * (args.MW[0] / kBM);
         if (!wait_counter(args.done + t.e, need, s_abort)) {
           ok = false;
           break;
@@ -313,11 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int K = args.K[t.ph];
       const int nk = K / kBK;
-      const int nbox = (t.rows + kBoxRows - 1) / kBoxRows;
+      const int nbox = (min(t.rows, kBN) + kBoxRows - 1) / kBoxRows;
+      const bool tail = kAbsorb > 0 && t.rows > kBN;   // absorbed rows in a second atom
       // an e2m1 tile fills the same 16 KB of smem as an e4m3 one (each 16-code group
       // padded to 16 bytes), but only its 8 KB of packed codes count as transferred
       const uint32_t abytes = args.a_fp4[t.ph] ? kABytes / 2 : kABytes;
-      const uint32_t bytes = weights ? abytes + kSfBytes : nbox * kBoxBytes + kSfBytes;
+      const uint32_t bytes =
+          weights ? abytes + kSfBytes
+                  : nbox * kBoxBytes + (tail ? kAbsorb * kBK + 2 * kSfBytes : kSfBytes);
       const CUtensorMap* tm = weights ? (t.ph ? &tmA1 : &tmA0) : (t.ph ? &tmB1 : &tmB0);
       const int arow = t.e * args.MW[t.ph] + t.mb * kBM;
       const int atile0 = (t.e * (args.MW[t.ph] / kBM) + t.mb) * nk;
@@ -330,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&full[stage], bytes);
-        uint8_t* sf = sSF + stage * 2 * kSfBytes + (weights ? 0 : kSfBytes);
+        uint8_t* sf = sSF + stage * kSfAtoms * kSfBytes + (weights ? 0 : kSfBytes);
         if (weights) {
           if (args.a_fp4[t.ph])  // tile-major e2m1: tile (e, mb, kb) is rows [128 * tile, +128)
             tma_load_2d(sA + stage * kABytes, tm, &full[stage], 0, (atile0 + kb) * kBM, pol_w);
@@ -342,6 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sB + stage * kBBytes + j * kBoxBytes, tm, &full[stage], kb * kBK,
                         t.row0 + j * kBoxRows, pol_x);
           bulk_load_1d(sf, sfsrc + (size_t)kb * kSfBytes, kSfBytes, &full[stage], pol_x);
+          if (tail) {
+            tma_load_2d(sB + stage * kBBytes + kBN * kBK, t.ph ? &tmX1 : &tmX0, &full[stage],
+                        kb * kBK, t.row0 + kBN, pol_x);
+            // the next 128-row block's atom for the same K step
+            bulk_load_1d(sf + kSfBytes, sfsrc + ((size_t)nk + kb) * kSfBytes, kSfBytes,
+                         &full[stage], pol_x);
+          }
         }
         issued_mask |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (par << stage);
@@ -383,18 +429,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t par = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit t = decode_unit<kBN>(u, tb);
+      const Unit t = decode_unit<kBN, kAbsorb>(u, tb);
       const int nk = args.K[t.ph] / kBK;
+      const bool tail = kAbsorb > 0 && t.rows > kBN;
       for (int kb = 0; kb < nk; ++kb) {
         if (!mbar_wait(&full[stage], par, s_abort)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * 8);
-        const uint32_t sf_s = smem_u32(sSF + stage * 2 * kSfBytes);
+        const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * kSfStageCols);
+        const uint32_t sf_s = smem_u32(sSF + stage * kSfAtoms * kSfBytes);
         tc_cp_32x128b_warpx4(sfa_t, smem_desc_noswz(sf_s, 128));
         tc_cp_32x128b_warpx4(sfa_t + 4, smem_desc_noswz(sf_s + kSfBytes, 128));
+        if (tail) tc_cp_32x128b_warpx4(sfa_t + 8, smem_desc_noswz(sf_s + 2 * kSfBytes, 128));
         ++done_stages;
         if (stage % kG == kG - 1 || done_stages == my_stages) tc_commit(&sfready[stage / kG]);
         if (++stage == kStages) {
@@ -415,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t par = 0, apar = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit t = decode_unit<kBN>(u, tb);
+      const Unit t = decode_unit<kBN, kAbsorb>(u, tb);
       const int n = (t.rows + 15) & ~15;
       const uint32_t idesc0 = idesc_mxf8_f32(kBM, n, 0, 0) | (args.a_fp4[t.ph] ? (5u << 7) : 0u);
       if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort)) {
@@ -423,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+      const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccStride);
       const int nk = args.K[t.ph] / kBK;
       for (int kb = 0; kb < nk; ++kb) {
         // the scales' copy completing implies the stages' operands have landed
@@ -432,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * 8);
+        const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * kSfStageCols);
         const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * kABytes));
         const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
 #pragma unroll
@@ -465,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t apar = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit t = decode_unit<kBN>(u, tb);
+      const Unit t = decode_unit<kBN, kAbsorb>(u, tb);
       if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort) ? 1 : 0;
       named_bar_sync(1, 128);
       const int ok = s_flag[0];
@@ -479,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * kAccCols);
+                             static_cast<uint32_t>(acc * kAccStride);
       if (t.ph == 0) {
         // SwiGLU, then MX quantisation of h along I.  Warps q and q+2 hold the gate
         // and up rows of the same 32 features (one scale block, p = q & 1).  The pair
@@ -622,7 +670,7 @@ cudaError_t launch_shape(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1, const i
   a.E = E;
   a.done = (ph0 && ph1) ? done : nullptr;
   a.status = status;
-  CUtensorMap tm[4];
+  CUtensorMap tm[6];   // A0, B0, A1, B1, then the absorbed-row B boxes of both phases
   const GemmPhaseMx* phs[2] = {ph0, ph1};
   for (int p = 0; p < 2; ++p) {
     const GemmPhaseMx* g = phs[p] ? phs[p] : (ph0 ? ph0 : ph1);
@@ -641,6 +689,13 @@ cudaError_t launch_shape(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1, const i
     if (!encode_tmap_2d_u8(&tm[2 * p + 1], g->B_q, (uint64_t)g->K, (uint64_t)P_pad_rows, kBK,
                            S::kBoxRows))
       return cudaErrorInvalidValue;
+    if (S::kAbsorb > 0) {
+      if (!encode_tmap_2d_u8(&tm[4 + p], g->B_q, (uint64_t)g->K, (uint64_t)P_pad_rows, kBK,
+                             S::kAbsorb))
+        return cudaErrorInvalidValue;
+    } else {
+      tm[4 + p] = tm[2 * p + 1];
+    }
   }
   if (ph0) {
     a.hq = ph0->out_q;
@@ -657,7 +712,8 @@ cudaError_t launch_shape(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1, const i
   attr[0].val.cooperative = a.done != nullptr ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_kernel<S>, tm[0], tm[1], tm[2], tm[3], a);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_kernel<S>, tm[0], tm[1], tm[2], tm[3], tm[4],
+                            tm[5], a);
 }
 
 }  // namespace
