@@ -383,6 +383,8 @@ def run_ours(args, cfg):
     timed = list(range(0, K, GEMM_EVERY))
     gb = {i: torch.cuda.Event(enable_timing=True) for i in timed}
     ge = {i: torch.cuda.Event(enable_timing=True) for i in timed}
+    sb = {i: torch.cuda.Event(enable_timing=True) for i in timed}   # whole-step events, same steps
+    se = {i: torch.cuda.Event(enable_timing=True) for i in timed}
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
@@ -396,8 +398,10 @@ def run_ours(args, cfg):
             gb[i].record(stream)
             ge[i].record(stream)
             moe.set_gemm_events(gb[i], ge[i])
+            sb[i].record(stream)
         step(x)
         if i in gb:
+            se[i].record(stream)
             moe.set_gemm_events(None, None)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -405,7 +409,14 @@ def run_ours(args, cfg):
     clocks = sampler.stop()
     moe.set_gemm_events(None, None)
     ms_total = max_over_ranks(t_start.elapsed_time(t_end))
-    gemm_ms = statistics.mean(gb[i].elapsed_time(ge[i]) for i in timed)
+    gemm_samples = [gb[i].elapsed_time(ge[i]) for i in timed]
+    step_samples = [sb[i].elapsed_time(se[i]) for i in timed]
+    gemm_ms = statistics.mean(gemm_samples)
+
+    def pct(v):
+        q = sorted(v)
+        at = lambda f: q[min(len(q) - 1, int(round(f * (len(q) - 1))))]
+        return {"p10": at(0.1), "p50": at(0.5), "p90": at(0.9), "n": len(q)}
     status = moe.get_device_status(dev)
 
     # ---- end-to-end: pinned host input -> device -> layer -> pinned host output
@@ -463,11 +474,14 @@ def run_ours(args, cfg):
                 else "fallback 1.9 PFLOP/s" + (" x 2" if cfg.mx else "")}
     tr = profiled_traffic(cfg.name)
     roof.update({"traffic": tr, "kernel": "grouped_gemm_kernel (both projections, one launch)",
-                 "kernel_ms": gemm_ms, "algorithmic_bytes": gbytes, "active_experts": active})
+                 "kernel_ms": gemm_ms, "kernel_ms_pct": pct(gemm_samples), "algorithmic_bytes": gbytes,
+                 "active_experts": active})
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_total / K,
+        "step_ms_pct": {**pct(step_samples), "note": "single steps bracketed by events (every 8th timed step)"},
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": ("w4a8 (weights e2m1 + e8m0/32, activations e4m3 + e8m0/32)" if cfg.w4
                                        else "mxfp8 (e4m3 + e8m0/32)" if cfg.mx else "bf16"), "data": "synthetic",
         "config": workload_config(cfg), "roofline": roof,
@@ -526,9 +540,9 @@ def run_ep_routing(args, cfg):
     cnt_d = torch.from_numpy(cnt).to(dev)
     N = int(cnt.sum())
 
-    def step():
-        rt = moe.init_routing_v2(ids, cfg.E, 0, El, x=x)
-        moe.re_routing(cnt_d, rt["expanded_x"][:N], N)
+    def step(xx=x, ii=ids):
+        rt = moe.init_routing_v2(ii, cfg.E, 0, El, x=xx)
+        return moe.re_routing(cnt_d, rt["expanded_x"][:N], N)[2]
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -543,6 +557,27 @@ def run_ep_routing(args, cfg):
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     ms = s0.elapsed_time(s1)
+    # end to end: this rank's inputs (x and the top-k ids) from pinned host memory,
+    # the expert offsets of the re-routed rows back to the host
+    x_host, ids_host = x.cpu().pin_memory(), ids.cpu().pin_memory()
+    off_host = torch.empty(El + 1, dtype=torch.int32).pin_memory()
+    x_dev, ids_dev = torch.empty_like(x), torch.empty_like(ids)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        ids_dev.copy_(ids_host, non_blocking=True)
+        off_host.copy_(step(x_dev, ids_dev), non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
     hbm, _, kind = measured_peaks()
     nbytes = 3 * N * cfg.H * 2
     achieved = nbytes * args.steps / (ms / 1e3) / 1e9
@@ -554,6 +589,8 @@ def run_ep_routing(args, cfg):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "peak_source": kind, "traffic": None, "algorithmic_bytes": nbytes,
                          "kernel": "routing + gather + re-routing, whole step"},
+            "e2e": {"value": cfg.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": x.numel() * 2 + ids.numel() * 4, "d2h_bytes_per_step": (El + 1) * 4},
             "gpu_launches": 6 * args.steps, "clocks": clocks}
     print(json.dumps(line), flush=True)
     return 0
