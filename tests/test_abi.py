@@ -84,3 +84,22 @@ def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         B.gating_topk_softmax(torch.zeros(2, 4), 2)
+
+
+def test_out_of_range_shapes_rejected_before_device_use(L):
+    """Empty and out-of-range shapes fail host validation (MOE_ERR_UNSUPPORTED_SHAPE = 2)
+    with fake, aligned pointers that are never dereferenced."""
+    f = ctypes.c_void_p(0x10000)
+    for T, H, E, k, I in [(0, 256, 8, 2, 128),      # no tokens
+                          (16, 256, 8, 9, 128),     # k > E
+                          (16, 256, 300, 2, 128),   # E > 256
+                          (16, 256, 64, 33, 128),   # k > 32
+                          (16, 200, 8, 2, 128)]:    # H % 128 != 0
+        assert L.moe_forward(f, f, None, f, f, T, H, E, k, I, f, None, None, f, 1 << 30, None) == 2
+        assert L.moe_forward_workspace_size(T, H, E, k, I) == 0
+        assert L.moe_forward_mx_workspace_size(T, H, E, k, I) == 0
+        assert L.moe_forward_w4a8_workspace_size(T, H, E, k, I) == 0
+    assert L.moe_grouped_matmul_mx_workspace_size(8, 0, 256, 128, 1) == 0     # no rows
+    assert L.moe_grouped_matmul_mx_workspace_size(300, 16, 256, 128, 1) == 0  # E > 256
+    assert L.moe_grouped_matmul_mx_workspace_size(8, 16, 200, 128, 0) == 0    # K % 128 != 0
+    assert L.moe_packed_weight_bytes_mx4(8, 256, 128, 0) == 8 * 256 * 128     # 2I x H codes / 2

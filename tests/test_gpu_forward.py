@@ -83,6 +83,14 @@ def test_forward_single_expert_is_dense_mlp(layers):
     _check_forward(cfg, inp, layer)
 
 
+@pytest.mark.parametrize("T,E,k", [(40, 256, 32),    # the largest expert count and top-k
+                                   (33, 4, 4),       # k = E: every token visits every expert
+                                   (700, 256, 8)])   # 256 experts, multi-CTA routing (P > 4096)
+def test_forward_limits(layers, T, E, k):
+    cfg, inp, layer = layers("tiny", T=T, E=E, k=k, H=256, I=128)
+    _check_forward(cfg, inp, layer)
+
+
 @pytest.mark.parametrize("T", [64, 300])
 def test_forward_with_gpu_router(layers, T):
     cfg, inp, layer = layers("qwen3_30b_a3b_decode", T=T)

@@ -143,6 +143,15 @@ def test_forward_mx_small(cuda_dev, T, E, k, H, I):
     _check_mx_forward(cfg, inp, layer)
 
 
+@pytest.mark.parametrize("T,E,k", [(40, 256, 32), (700, 256, 8)])
+def test_forward_mx_limits(cuda_dev, T, E, k):
+    """256 experts (the routing tables' size) with the largest top-k, and with enough
+    pairs for the multi-CTA routing and the wide block-scaled tiles."""
+    cfg = W.with_shape(W.CONFIGS["mxfp8_prefill"], T=T, E=E, k=k, H=256, I=128)
+    inp, layer = _mx_layer(cfg)
+    _check_mx_forward(cfg, inp, layer)
+
+
 def test_forward_mx_decode_tiles_skewed(cuda_dev):
     """Few pairs per expert on average (the narrow-tile shape) but Zipf-skewed, so the
     busiest expert spans several 32-token tiles and every 32-row group of a scale atom."""
