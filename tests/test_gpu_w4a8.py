@@ -107,7 +107,8 @@ def _check_w4_forward(cfg, inp, layer, sample=None):
 
 
 @pytest.mark.parametrize("T,E,k,H,I", [(64, 8, 2, 256, 128), (300, 4, 2, 256, 256), (1, 8, 8, 512, 128),
-                                       (200, 16, 4, 512, 384)])
+                                       (200, 16, 4, 512, 384),
+                                       (64, 16, 2, 256, 128)])
 def test_forward_w4a8_small(cuda_dev, T, E, k, H, I):
     cfg = W.with_shape(W.CONFIGS["w4a8_prefill"], T=T, E=E, k=k, H=H, I=I)
     inp, layer = _w4_layer(cfg)
@@ -125,6 +126,19 @@ def test_forward_w4a8_decode_tiles_skewed(cuda_dev):
     _, y = O.add_rmsnorm(to_np(inp["x"]), to_np(inp["r"]), to_np(inp["norm_w"]), cfg.eps)
     ids, _ = O.gating_topk_softmax(O.router_logits_f32(y, to_np(inp["Wg"])), cfg.k)
     assert np.bincount(ids.ravel(), minlength=cfg.E).max() > 128   # two atoms, all groups
+
+
+def test_forward_w4a8_few_pairs_skewed(cuda_dev):
+    """At most 8 pairs per expert on average with a Zipf-skewed router, so one expert
+    spans several narrow token blocks while most have one or two tokens."""
+    cfg = W.with_shape(W.CONFIGS["w4a8_decode"], T=128, E=16, k=1, H=256, I=128, router="zipf",
+                       zipf_s=2.0)
+    inp, layer = _w4_layer(cfg)
+    assert cfg.T * cfg.k <= 8 * cfg.E
+    _check_w4_forward(cfg, inp, layer)
+    _, y = O.add_rmsnorm(to_np(inp["x"]), to_np(inp["r"]), to_np(inp["norm_w"]), cfg.eps)
+    ids, _ = O.gating_topk_softmax(O.router_logits_f32(y, to_np(inp["Wg"])), cfg.k)
+    assert np.bincount(ids.ravel(), minlength=cfg.E).max() > 48
 
 
 def test_w4a8_differs_from_mxfp8(cuda_dev):
