@@ -40,6 +40,10 @@ constexpr int kBM = 128;         // weight rows per tile (MMA M)
 constexpr int kBK = 64;          // K per stage: one 128-byte swizzle row of bf16
 constexpr int kThreads = 256;
 constexpr int kMaxE = 256;
+// A CTA's units are decoded once in the prologue into shared memory, so a unit
+// boundary costs each role one shared-memory load instead of a binary search and
+// divisions; a longer list is decoded on the fly.
+constexpr int kMaxUnits = 512;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
 constexpr int kEpiBytes = 4 * 32 * 32 * 2;  // per epilogue warp: 32 tokens x 32 bf16
 
@@ -73,7 +77,9 @@ struct Layout {
   static constexpr int kNumBars = 2 * STAGES + 5;            // full, empty, tfull[2], tempty[2], fin
   static constexpr int kMisc = kBar + kNumBars * 8;          // tmem addr, abort flag
   static constexpr int kTables = kMisc + 16;                 // off, uoff0, uoff1 (kMaxE+1 each), scan tmp
-  static constexpr int kEnd = kTables + (3 * (kMaxE + 1) + 8) * 4;
+  static constexpr int kUnits = kTables + ((3 * (kMaxE + 1) + 8) * 4 + 7) / 8 * 8;
+  static constexpr int kEnd = kUnits + kMaxUnits * 8;
+  static_assert(kUnits % 8 == 0, "unit list alignment");
   static constexpr int kSmemBytes = kEnd + 1024;             // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -114,6 +120,25 @@ __device__ __forceinline__ Unit decode_unit(int u, const Tables& tb) {
   r.row0 = tb.off[lo] + b * BN;
   r.rows = min(BN, tb.off[lo + 1] - r.row0);
   return r;
+}
+
+// A unit in two words: row0; ph | e << 1 | mb << 10 | rows << 19 | ks << 28 (e < 512,
+// mb < 512, rows <= 256 and ks < 16 hold for every shape the entry points accept).
+__device__ __forceinline__ uint2 pack_unit(const Unit& t) {
+  return make_uint2(static_cast<uint32_t>(t.row0),
+                    static_cast<uint32_t>(t.ph) | (static_cast<uint32_t>(t.e) << 1) |
+                        (static_cast<uint32_t>(t.mb) << 10) | (static_cast<uint32_t>(t.rows) << 19) |
+                        (static_cast<uint32_t>(t.ks) << 28));
+}
+__device__ __forceinline__ Unit unpack_unit(uint2 w) {
+  Unit t;
+  t.row0 = static_cast<int>(w.x);
+  t.ph = static_cast<int>(w.y & 1u);
+  t.e = static_cast<int>((w.y >> 1) & 511u);
+  t.mb = static_cast<int>((w.y >> 10) & 511u);
+  t.rows = static_cast<int>((w.y >> 19) & 511u);
+  t.ks = static_cast<int>(w.y >> 28);
+  return t;
 }
 
 __device__ __forceinline__ bool wait_counter(const int* p, int need, const volatile int* abort) {
@@ -158,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_uoff0 = s_off + (kMaxE + 1);
   int* s_uoff1 = s_uoff0 + (kMaxE + 1);
   int* s_tmp = s_uoff1 + (kMaxE + 1);
+  uint2* s_units = reinterpret_cast<uint2*>(smem + L::kUnits);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = args.E;
@@ -228,6 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tb.ksplit[1] = args.ksplit[1];
   tb.E = E;
   const int total = s_uoff0[E] + s_uoff1[E];
+  const int my_units =
+      (int)blockIdx.x < total ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const bool use_list = my_units <= kMaxUnits;   // the same in every thread of the CTA
+  if (use_list) {
+    for (int i = tid; i < my_units; i += kThreads)
+      s_units[i] = pack_unit(decode_unit<BN>((int)blockIdx.x + i * (int)gridDim.x, tb));
+    __syncthreads();
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -241,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t par = 0;
       uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit t = decode_unit<BN>(u, tb);
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<BN>(u, tb);
         if (t.ph == 1 && args.done != nullptr) {
           const int m = s_off[t.e + 1] - s_off[t.e];
           const int need = ((m + BN - 1) / BN) * (args.MW[0] / kBM) * args.ksplit[0];
@@ -312,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t par = 0, apar = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit t = decode_unit<BN>(u, tb);
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<BN>(u, tb);
         const int n = (t.rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(kBM, n);
         if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort)) {
@@ -360,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* s_flag = s_tmp;             // broadcast of the elected wait's result
     int acc = 0;
     uint32_t apar = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit t = decode_unit<BN>(u, tb);
+    for (int u = blockIdx.x, ui = 0; u < total; u += gridDim.x, ++ui) {
+      const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<BN>(u, tb);
       if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort) ? 1 : 0;
       named_bar_sync(1, 128);
       const int ok = s_flag[0];

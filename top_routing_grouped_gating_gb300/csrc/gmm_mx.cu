@@ -37,6 +37,10 @@ constexpr int kBM = 128;
 constexpr int kBK = 128;                          // fp8 elements per stage (128 bytes)
 constexpr int kThreads = 256;
 constexpr int kMaxE = 256;
+// A CTA's units are decoded once in the prologue into shared memory, so a unit
+// boundary costs each role one shared-memory load instead of a binary search and
+// divisions; a longer list is decoded on the fly.
+constexpr int kMaxUnits = 512;
 constexpr int kABytes = kBM * kBK;                // 16 KB
 constexpr int kSfBytes = 512;                     // one scale atom
 constexpr int kEpiBytes = (4 * 16 * 33 + 2 * 32 * 33) * 4;  // SwiGLU exchange + h tile
@@ -79,7 +83,9 @@ struct MxShape {
   static constexpr int kNumBars = kStages + 2 * (kStages / kGroup) + 6;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTables = kMisc + 16;
-  static constexpr int kEnd = kTables + (4 * (kMaxE + 1) + 8) * 4;
+  static constexpr int kUnits = kTables + (4 * (kMaxE + 1) + 8) * 4;
+  static constexpr int kEnd = kUnits + kMaxUnits * 8;
+  static_assert(kUnits % 8 == 0, "unit list alignment");
   static constexpr int kSmemBytes = kEnd + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kColsUsed <= 512, "tensor memory budget");
@@ -162,6 +168,24 @@ __device__ __forceinline__ Unit decode_unit(int u, const Tables& tb) {
   return r;
 }
 
+// A unit in two words: row0; ph | e << 1 | mb << 10 | rows << 20 (e < 512 and
+// mb < 1024 hold for every shape the entry points accept; rows <= 160).
+__device__ __forceinline__ uint2 pack_unit(const Unit& t) {
+  return make_uint2(static_cast<uint32_t>(t.row0),
+                    static_cast<uint32_t>(t.ph) | (static_cast<uint32_t>(t.e) << 1) |
+                        (static_cast<uint32_t>(t.mb) << 10) | (static_cast<uint32_t>(t.rows) << 20));
+}
+__device__ __forceinline__ Unit unpack_unit(uint2 w) {
+  Unit t;
+  t.row0 = static_cast<int>(w.x);
+  t.ph = static_cast<int>(w.y & 1u);
+  t.e = static_cast<int>((w.y >> 1) & 511u);
+  t.mb = static_cast<int>((w.y >> 10) & 1023u);
+  t.rows = static_cast<int>(w.y >> 20);
+  t.nb = 0;
+  return t;
+}
+
 __device__ __forceinline__ bool wait_counter(const int* p, int need, const volatile int* abort) {
   if (ld_acquire_gpu(p) >= need) return true;
   const unsigned long long t0 = globaltimer();
@@ -231,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_uoff0 = s_poff + (kMaxE + 1);
   int* s_uoff1 = s_uoff0 + (kMaxE + 1);
   int* s_tmp = s_uoff1 + (kMaxE + 1);
+  uint2* s_units = reinterpret_cast<uint2*>(smem + L::kUnits);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = args.E;
@@ -307,6 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tb.uoff[1] = s_uoff1;
   tb.E = E;
   const int total = s_uoff0[E] + s_uoff1[E];
+  const int my_units =
+      (int)blockIdx.x < total ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const bool use_list = my_units <= kMaxUnits;   // the same in every thread of the CTA
+  if (use_list) {
+    for (int i = tid; i < my_units; i += kThreads)
+      s_units[i] = pack_unit(decode_unit<kBN, kAbsorb>((int)blockIdx.x + i * (int)gridDim.x, tb));
+    __syncthreads();
+  }
 
   // Each tcgen05 / TMA instruction costs its issuing thread tens of clocks, so the
   // per-stage issue work is spread over four single-thread roles: weight loads
@@ -335,8 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t par = 0;
     uint32_t issued_mask = 0, issued_par = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit t = decode_unit<kBN, kAbsorb>(u, tb);
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kBN, kAbsorb>(u, tb);
       if (!weights && t.ph == 1 && args.done != nullptr) {
         // the down projection's activations are h of this expert's gate/up units
         const int m = s_off[t.e + 1] - s_off[t.e];
@@ -428,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, done_stages = 0;
     uint32_t par = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit t = decode_unit<kBN, kAbsorb>(u, tb);
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kBN, kAbsorb>(u, tb);
       const int nk = args.K[t.ph] / kBK;
       const bool tail = kAbsorb > 0 && t.rows > kBN;
       for (int kb = 0; kb < nk; ++kb) {
@@ -462,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, acc = 0, done_stages = 0;
     uint32_t par = 0, apar = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit t = decode_unit<kBN, kAbsorb>(u, tb);
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kBN, kAbsorb>(u, tb);
       const int n = (t.rows + 15) & ~15;
       const uint32_t idesc0 = idesc_mxf8_f32(kBM, n, 0, 0) | (args.a_fp4[t.ph] ? (5u << 7) : 0u);
       if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort)) {
@@ -512,8 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* s_flag = s_tmp;
     int acc = 0;
     uint32_t apar = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit t = decode_unit<kBN, kAbsorb>(u, tb);
+    for (int u = blockIdx.x, ui = 0; u < total; u += gridDim.x, ++ui) {
+      const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kBN, kAbsorb>(u, tb);
       if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort) ? 1 : 0;
       named_bar_sync(1, 128);
       const int ok = s_flag[0];
