@@ -27,6 +27,7 @@
 // bf16 tiles in the 128-byte-swizzled K-major layout TMA writes; TMEM holds two
 // 128 x BN fp32 accumulators so the epilogue of one unit overlaps the MMAs of the
 // next.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -157,6 +158,80 @@ __device__ __forceinline__ bool wait_counter(const int* p, int need, const volat
 __device__ __forceinline__ uint16_t f2bf(float f) {
   __nv_bfloat16 b = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// Drains one accumulator (this warp's 32 TMEM lanes, t.rows token columns) into
+// the unit's output: SwiGLU to bf16 h (epi 0), bf16 (epi 1) or fp32 split-K
+// partials (epi 2).  Warp q of the epilogue group owns TMEM lanes 32q..32q+31.
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& args, const Unit& t,
+                                              uint32_t tbase, uint8_t* sEpi, int q,
+                                              int lane) {
+  uint16_t* out = args.out[t.ph];
+  const int ld = args.ld[t.ph];
+  if (args.epi[t.ph] == 2) {
+    // fp32 split-K partial: part[ks][row][col], col = weight row of this lane
+    const int col = t.mb * kBM + q * 32 + lane;
+    float* part = args.out_f32[t.ph] + (size_t)t.ks * args.rows_total[t.ph] * ld;
+    for (int c0 = 0; c0 < t.rows; c0 += 32) {
+      float v[32];
+      tmem_ld_32x32b_x32(tbase + c0, v);
+      if (col < args.mvalid[t.ph]) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < t.rows) part[(size_t)(t.row0 + c0 + j) * ld + col] = v[j];
+      }
+    }
+  } else if (args.epi[t.ph] == 0) {
+    // Each 32-lane TMEM quarter holds 16 gate rows (lanes 0-15) and the 16
+    // matching up rows (lanes 16-31).  One shuffle across the half-warps pairs
+    // them: lanes 0-15 finish tokens 0-15 of the chunk, lanes 16-31 tokens 16-31,
+    // for feature t.mb*64 + q*16 + (lane % 16).
+    uint16_t* hw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 16;  // [32 tok][16] bf16
+    const bool lo = lane < 16;
+    const int f = lane & 15;
+    for (int c0 = 0; c0 < t.rows; c0 += 32) {
+      float v[32];
+      tmem_ld_32x32b_x32(tbase + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float send = lo ? v[16 + j] : v[j];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+        const float g = lo ? v[j] : recv;
+        const float up = lo ? recv : v[16 + j];
+        const float h = g / (1.0f + __expf(-g)) * up;
+        hw[(lo ? j : 16 + j) * 16 + f] = f2bf(h);
+      }
+      __syncwarp();
+      if (c0 + lane < t.rows) {
+        const uint4* src = reinterpret_cast<const uint4*>(hw + lane * 16);
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)(t.row0 + c0 + lane) * ld +
+                                              t.mb * 64 + q * 16);
+        dst[0] = src[0];
+        dst[1] = src[1];
+      }
+      __syncwarp();
+    }
+  } else {
+    uint16_t* tbw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 32;  // [32 tok][32] bf16
+    for (int c0 = 0; c0 < t.rows; c0 += 32) {
+      float v[32];
+      tmem_ld_32x32b_x32(tbase + c0, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) tbw[j * 32 + lane] = f2bf(v[j]);
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int idx = lane + 32 * it;
+        const int j = idx >> 2, c = idx & 3;
+        if (c0 + j < t.rows) {
+          const uint4 val = *reinterpret_cast<const uint4*>(tbw + j * 32 + c * 8);
+          *reinterpret_cast<uint4*>(out + (size_t)(t.row0 + c0 + j) * ld + t.mb * kBM +
+                                    q * 32 + c * 8) = val;
+        }
+      }
+      __syncwarp();
+    }
+  }
 }
 
 template <int BN, int STAGES, int BOX>
@@ -410,72 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      uint16_t* out = args.out[t.ph];
-      const int ld = args.ld[t.ph];
-      if (args.epi[t.ph] == 2) {
-        // fp32 split-K partial: part[ks][row][col], col = weight row of this lane
-        const int col = t.mb * kBM + q * 32 + lane;
-        float* part = args.out_f32[t.ph] + (size_t)t.ks * args.rows_total[t.ph] * ld;
-        for (int c0 = 0; c0 < t.rows; c0 += 32) {
-          float v[32];
-          tmem_ld_32x32b_x32(tbase + c0, v);
-          if (col < args.mvalid[t.ph]) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (c0 + j < t.rows) part[(size_t)(t.row0 + c0 + j) * ld + col] = v[j];
-          }
-        }
-      } else if (args.epi[t.ph] == 0) {
-        // Each 32-lane TMEM quarter holds 16 gate rows (lanes 0-15) and the 16
-        // matching up rows (lanes 16-31).  One shuffle across the half-warps pairs
-        // them: lanes 0-15 finish tokens 0-15 of the chunk, lanes 16-31 tokens 16-31,
-        // for feature t.mb*64 + q*16 + (lane % 16).
-        uint16_t* hw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 16;  // [32 tok][16] bf16
-        const bool lo = lane < 16;
-        const int f = lane & 15;
-        for (int c0 = 0; c0 < t.rows; c0 += 32) {
-          float v[32];
-          tmem_ld_32x32b_x32(tbase + c0, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float send = lo ? v[16 + j] : v[j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float g = lo ? v[j] : recv;
-            const float up = lo ? recv : v[16 + j];
-            const float h = g / (1.0f + __expf(-g)) * up;
-            hw[(lo ? j : 16 + j) * 16 + f] = f2bf(h);
-          }
-          __syncwarp();
-          if (c0 + lane < t.rows) {
-            const uint4* src = reinterpret_cast<const uint4*>(hw + lane * 16);
-            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)(t.row0 + c0 + lane) * ld +
-                                                  t.mb * 64 + q * 16);
-            dst[0] = src[0];
-            dst[1] = src[1];
-          }
-          __syncwarp();
-        }
-      } else {
-        uint16_t* tbw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 32;  // [32 tok][32] bf16
-        for (int c0 = 0; c0 < t.rows; c0 += 32) {
-          float v[32];
-          tmem_ld_32x32b_x32(tbase + c0, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) tbw[j * 32 + lane] = f2bf(v[j]);
-          __syncwarp();
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int idx = lane + 32 * it;
-            const int j = idx >> 2, c = idx & 3;
-            if (c0 + j < t.rows) {
-              const uint4 val = *reinterpret_cast<const uint4*>(tbw + j * 32 + c * 8);
-              *reinterpret_cast<uint4*>(out + (size_t)(t.row0 + c0 + j) * ld + t.mb * kBM +
-                                        q * 32 + c * 8) = val;
-            }
-          }
-          __syncwarp();
-        }
-      }
+      epilogue_tile(args, t, tbase, sEpi, q, lane);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -495,6 +505,362 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// ------------------------------------------------------------ CTA pairs --
+// Prefill variant on pairs of SMs (a cluster of two CTAs).  A pair unit is
+// (phase, expert, 256-row weight block, token block of up to 256 rows): one
+// tcgen05.mma.cta_group::2 of M = 256 covers both CTAs' 128-row weight blocks
+// (CTA r holds block 2*pb + r of A) and the token block's N columns, of which
+// CTA r holds rows [r*N/2, (r+1)*N/2) of B.  Each CTA's TMEM receives the full
+// 128 x N accumulator of its own weight block, so the epilogue is the one-CTA
+// kernel's.  Per SM and stage the ring then holds 16 KB of weights and 16 KB of
+// tokens instead of 16 + 32 KB: six stages fit where four did, and the L2 and
+// shared-memory traffic per FLOP drops by a third.
+//
+// Roles: warp 0 lane 0 of each CTA loads its own A and B halves onto its own
+// `full` barrier; in the odd CTA, warp 3 lane 0 passes each landed stage on to
+// the even CTA's `full` barrier (a relaxed remote arrive); warp 1 lane 0 of the
+// even CTA issues the MMAs and commits each stage's release and each
+// accumulator's completion to both CTAs (multicast commit); warps 4-7 of both
+// CTAs drain their accumulators and arrive on the even CTA's `tempty`.
+constexpr int kPairBN = 256;        // token rows per pair unit
+constexpr int kPairBoxS = 32;       // B box rows for units whose half is at most 32 rows
+constexpr int kPairTmemCols = 512;  // two 128 x 256 fp32 accumulators per CTA
+
+template <int STAGES>
+struct PairLayout {
+  static constexpr int kBBytes = 128 * kBK * 2;                // this CTA's <= 128 token rows
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + STAGES * kABytes;
+  static constexpr int kEpi = kB + STAGES * kBBytes;
+  static constexpr int kBar = kEpi + kEpiBytes;                // 8-byte aligned
+  static constexpr int kNumBars = 2 * STAGES + 5;              // full, empty, tfull[2], tempty[2], fin
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kTables = kMisc + 16;
+  static constexpr int kUnits = kTables + ((3 * (kMaxE + 1) + 8) * 4 + 7) / 8 * 8;
+  static constexpr int kEnd = kUnits + kMaxUnits * 8;
+  static_assert(kUnits % 8 == 0, "unit list alignment");
+  static constexpr int kSmemBytes = kEnd + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
+                             const __grid_constant__ CUtensorMap tmB0,
+                             const __grid_constant__ CUtensorMap tmA1,
+                             const __grid_constant__ CUtensorMap tmB1,
+                             const __grid_constant__ CUtensorMap tmS0,   // kPairBoxS-row B boxes
+                             const __grid_constant__ CUtensorMap tmS1, const GemmArgs args) {
+  using L = PairLayout<STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem + L::kA;
+  uint8_t* sB = smem + L::kB;
+  uint8_t* sEpi = smem + L::kEpi;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;     // waited on in the even CTA only
+  uint64_t* fin = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  int* s_off = reinterpret_cast<int*>(smem + L::kTables);
+  int* s_uoff0 = s_off + (kMaxE + 1);
+  int* s_uoff1 = s_uoff0 + (kMaxE + 1);
+  int* s_tmp = s_uoff1 + (kMaxE + 1);
+  uint2* s_units = reinterpret_cast<uint2*>(smem + L::kUnits);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = args.E;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
+  pdl_trigger();
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      // even CTA: its own producer + the odd CTA's forwarded arrival
+      mbar_init(&full[s], leader ? 2 : 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);   // four epilogue warps in each CTA
+    }
+    mbar_init(fin, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB1);
+    tma_prefetch_desc(&tmS0);
+    tma_prefetch_desc(&tmS1);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(s_tmem, kPairTmemCols);
+    tmem_relinquish_pair();
+  }
+  for (int i = tid; i <= E; i += kThreads) s_off[i] = args.offsets[i];
+  __syncthreads();
+
+  // Pair units per expert and their exclusive prefix, per phase.
+  {
+    int u[2] = {0, 0};
+    if (tid < E) {
+      const int m = s_off[tid + 1] - s_off[tid];
+      const int nb = (m + kPairBN - 1) / kPairBN;
+      u[0] = args.active[0] ? nb * (args.MW[0] / (2 * kBM)) : 0;
+      u[1] = args.active[1] ? nb * (args.MW[1] / (2 * kBM)) : 0;
+    }
+    for (int p = 0; p < 2; ++p) {
+      int inc = u[p];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) s_tmp[warp] = inc;
+      __syncthreads();
+      int pre = 0, tot = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        if (w < warp) pre += s_tmp[w];
+        tot += s_tmp[w];
+      }
+      int* dst = p ? s_uoff1 : s_uoff0;
+      if (tid < E) dst[tid] = pre + inc - u[p];
+      if (tid == 0) dst[E] = tot;
+      __syncthreads();
+    }
+  }
+  tc_fence_after_sync();
+  // both CTAs' barriers are initialised and TMEM allocated before any remote arrive
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
+  Tables tb;
+  tb.off = s_off;
+  tb.uoff[0] = s_uoff0;
+  tb.uoff[1] = s_uoff1;
+  tb.ksplit[0] = 1;
+  tb.ksplit[1] = 1;
+  tb.E = E;
+  const int total = s_uoff0[E] + s_uoff1[E];
+  const int my_units = pair < total ? (total - pair + npairs - 1) / npairs : 0;
+  const bool use_list = my_units <= kMaxUnits;   // the same in every thread of the cluster
+  if (use_list) {
+    for (int i = tid; i < my_units; i += kThreads)
+      s_units[i] = pack_unit(decode_unit<kPairBN>(pair + i * npairs, tb));
+    __syncthreads();
+  }
+  const uint32_t lead_full0 = mapa_shared(smem_u32(&full[0]), 0);
+  const uint32_t lead_tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer --
+      const uint64_t pol_w = l2_policy_evict_normal();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t par = 0;
+      uint32_t issued_mask = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
+        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kPairBN>(u, tb);
+        if (t.ph == 1 && args.done != nullptr) {
+          const int m = s_off[t.e + 1] - s_off[t.e];
+          const int need = ((m + kPairBN - 1) / kPairBN) * (args.MW[0] / kBM);
+          if (!wait_counter(args.done + t.e, need, s_abort)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        const int half = ((t.rows + 15) & ~15) >> 1;        // this CTA's B rows (N / 2)
+        const bool small = half <= kPairBoxS;
+        const CUtensorMap* ta = t.ph ? &tmA1 : &tmA0;
+        const CUtensorMap* tbm = small ? (t.ph ? &tmS1 : &tmS0) : (t.ph ? &tmB1 : &tmB0);
+        const uint32_t bytes = kABytes + (small ? kPairBoxS : 128) * kBK * 2;
+        const int arow = t.e * args.MW[t.ph] + (2 * t.mb + static_cast<int>(rank)) * kBM;
+        const int brow = t.row0 + static_cast<int>(rank) * half;
+        const int nk = args.K[t.ph] / kBK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(sA + stage * kABytes, ta, &full[stage], kb * kBK, arow, pol_w);
+          tma_load_2d(sB + stage * L::kBBytes, tbm, &full[stage], kb * kBK, brow, pol_x);
+          issued_mask |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (par << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (ok) {
+        // every stage released by the pair's MMAs: no multicast commit is still on
+        // its way to this CTA's barriers when it exits
+        for (int i = 0; i < STAGES; ++i) {
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued_mask >> s) & 1u) mbar_wait(&full[s], (issued_par >> s) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 3) {
+    if (lane == 0 && !leader) {
+      // ------------------------------------- odd CTA: stage forwarder --
+      int stage = 0;
+      uint32_t par = 0;
+      bool ok = true;
+      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
+        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kPairBN>(u, tb);
+        const int nk = args.K[t.ph] / kBK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], par, s_abort)) {
+            ok = false;
+            break;
+          }
+          // the stage's bytes are in this CTA's shared memory (observed above)
+          mbar_arrive_cluster_relaxed(lead_full0 + stage * 8);
+          if (++stage == STAGES) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------- even CTA: MMA issuer --
+      int stage = 0, acc = 0;
+      uint32_t par = 0, apar = 0;
+      bool ok = true;
+      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
+        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kPairBN>(u, tb);
+        const int n = (t.rows + 15) & ~15;
+        const uint32_t idesc = idesc_bf16_f32(2 * kBM, n);
+        // both CTAs' epilogues have drained this accumulator
+        if (!mbar_wait_cluster(&tempty[acc], apar ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairBN);
+        const int nk = args.K[t.ph] / kBK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_cluster(&full[stage], par, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_u32(sA + stage * kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * L::kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_pair_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32),
+                             idesc, (kb | kk) ? 1u : 0u);
+          tc_commit_pair(&empty[stage], 3);
+          if (++stage == STAGES) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair(&tfull[acc], 3);
+        acc ^= 1;
+        if (acc == 0) apar ^= 1u;
+      }
+      if (ok) {
+        // the odd CTA's last remote tempty arrivals land before this CTA may exit
+        for (int i = 0; i < 2; ++i) {
+          if (!mbar_wait_cluster(&tempty[acc], apar ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          acc ^= 1;
+          if (acc == 0) apar ^= 1u;
+        }
+      }
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        tc_commit_pair(fin, 1);  // drain this thread's outstanding MMAs before TMEM is freed
+        mbar_wait(fin, 0, nullptr);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue --
+    const int q = warp & 3;
+    const int et = tid - 128;
+    int* s_flag = s_tmp;
+    int acc = 0;
+    uint32_t apar = 0;
+    for (int u = pair, ui = 0; u < total; u += npairs, ++ui) {
+      Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kPairBN>(u, tb);
+      t.mb = 2 * t.mb + static_cast<int>(rank);   // this CTA's 128-row weight block
+      if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort) ? 1 : 0;
+      named_bar_sync(1, 128);
+      const int ok = s_flag[0];
+      named_bar_sync(1, 128);
+      if (!ok) {
+        if (et == 0) {
+          *s_abort = 1;
+          flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * kPairBN);
+      epilogue_tile(args, t, tbase, sEpi, q, lane);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_cluster(lead_tempty0 + acc * 8);
+      }
+      if (t.ph == 0 && args.done != nullptr) {
+        __threadfence();
+        fence_proxy_async_global();
+        named_bar_sync(1, 128);
+        if (et == 0) red_release_add_gpu(args.done + t.e, 1);
+      }
+      acc ^= 1;
+      if (acc == 0) apar ^= 1u;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, kPairTmemCols);
   }
 }
 
@@ -590,6 +956,72 @@ cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_
                             a);
 }
 
+template <int STAGES>
+cudaError_t launch_pair_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_t* offsets,
+                             int E, int P, int* done, int* status, cudaStream_t s) {
+  using L = PairLayout<STAGES>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+      err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<STAGES>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+      if (err != cudaSuccess) return err;
+      attr_set[dev] = true;
+    }
+  }
+  GemmArgs a{};
+  a.offsets = offsets;
+  a.E = E;
+  a.done = (ph0 && ph1) ? done : nullptr;
+  a.status = status;
+  CUtensorMap tm[6];
+  const GemmPhase* phs[2] = {ph0, ph1};
+  for (int p = 0; p < 2; ++p) {
+    const GemmPhase* g = phs[p] ? phs[p] : (ph0 ? ph0 : ph1);
+    a.active[p] = phs[p] != nullptr;
+    a.K[p] = g->K;
+    a.MW[p] = g->MW;
+    a.ld[p] = g->n_out;
+    a.epi[p] = g->epi;
+    a.ksplit[p] = 1;
+    a.out[p] = g->out;
+    if (!encode_tmap_2d_bf16(&tm[2 * p], g->A_weights, (uint64_t)g->K, (uint64_t)E * g->MW, kBK,
+                             kBM) ||
+        !encode_tmap_2d_bf16(&tm[2 * p + 1], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK, 128) ||
+        !encode_tmap_2d_bf16(&tm[4 + p], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK, kPairBoxS))
+      return cudaErrorInvalidValue;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_sm_count() & ~1, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = a.done != nullptr ? 1 : 0;  // co-residency for the phase dependency
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<STAGES>, tm[0], tm[1], tm[2], tm[3],
+                            tm[4], tm[5], a);
+}
+
+// The pair kernel takes plain expert GEMMs (SwiGLU or bf16 epilogue, whole K per
+// unit, B rows of length K) whose weight matrices split into 256-row blocks.
+bool pairable(const GemmPhase* g) {
+  return g == nullptr || (g->epi != 2 && (g->ksplit <= 1) && g->bseg == 0 &&
+                          (g->b_inner == 0 || g->b_inner == g->K) && g->MW % (2 * kBM) == 0);
+}
+
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
@@ -599,6 +1031,20 @@ cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
   // Thin token tiles when the mean expert load is small (decode), wide ones else.
   if ((long long)P <= 16LL * E)
     return launch_impl<32, 10, 16>(ph0, ph1, offsets, E, P, done_counter, status, s);
+  // Wide tiles on CTA pairs where the shapes allow; if the driver refuses the
+  // cooperative cluster launch on this device, the one-CTA kernel runs (remembered).
+  static std::atomic<int> pair_state[64];  // 0 unknown, 1 launched, 2 refused
+  int dev = 0;
+  if (pairable(ph0) && pairable(ph1) && device_sm_count() >= 2 && cudaGetDevice(&dev) == cudaSuccess &&
+      dev >= 0 && dev < 64 && pair_state[dev].load() != 2) {
+    const cudaError_t err = launch_pair_impl<6>(ph0, ph1, offsets, E, P, done_counter, status, s);
+    if (err == cudaSuccess || pair_state[dev].load() == 1) {
+      if (err == cudaSuccess) pair_state[dev].store(1);
+      return err;
+    }
+    (void)cudaGetLastError();
+    pair_state[dev].store(2);
+  }
   return launch_impl<256, 4, 128>(ph0, ph1, offsets, E, P, done_counter, status, s);
 }
 
