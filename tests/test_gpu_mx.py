@@ -136,7 +136,10 @@ def _check_mx_forward(cfg, inp, layer, sample=None):
     return rf
 
 
-@pytest.mark.parametrize("T,E,k,H,I", [(64, 8, 2, 256, 128), (300, 4, 2, 256, 256), (1, 8, 8, 512, 128)])
+# (600, 4, 2): about 300 rows per expert, i.e. a full 256-row token block plus a short
+# one, each block over 128 rows taking two scale atoms
+@pytest.mark.parametrize("T,E,k,H,I", [(64, 8, 2, 256, 128), (300, 4, 2, 256, 256), (1, 8, 8, 512, 128),
+                                       (600, 4, 2, 256, 128)])
 def test_forward_mx_small(cuda_dev, T, E, k, H, I):
     cfg = W.with_shape(W.CONFIGS["mxfp8_prefill"], T=T, E=E, k=k, H=H, I=I)
     inp, layer = _mx_layer(cfg)
@@ -202,6 +205,7 @@ def test_forward_mx_with_gpu_router(cuda_dev):
     (64, 8, 2, 256, 128, 1),
     (300, 4, 2, 256, 256, 0),     # wide tiles, 128-row padding, experts over 128 rows
     (300, 4, 2, 512, 128, 1),
+    (600, 4, 2, 256, 128, 0),     # a 256-row block and a short one per expert
 ])
 def test_grouped_gemms_mx_match_oracle(cuda_dev, T, E, k, H, I, fmt):
     """Standalone block-scaled GEMMs on expert-sorted MX rows.  The activations are

@@ -108,7 +108,7 @@ def _check_w4_forward(cfg, inp, layer, sample=None):
 
 @pytest.mark.parametrize("T,E,k,H,I", [(64, 8, 2, 256, 128), (300, 4, 2, 256, 256), (1, 8, 8, 512, 128),
                                        (200, 16, 4, 512, 384),
-                                       (64, 16, 2, 256, 128)])
+                                       (64, 16, 2, 256, 128), (600, 4, 2, 256, 128)])
 def test_forward_w4a8_small(cuda_dev, T, E, k, H, I):
     cfg = W.with_shape(W.CONFIGS["w4a8_prefill"], T=T, E=E, k=k, H=H, I=I)
     inp, layer = _w4_layer(cfg)

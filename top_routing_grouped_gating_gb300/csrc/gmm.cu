@@ -1031,19 +1031,21 @@ cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
   // Thin token tiles when the mean expert load is small (decode), wide ones else.
   if ((long long)P <= 16LL * E)
     return launch_impl<32, 10, 16>(ph0, ph1, offsets, E, P, done_counter, status, s);
-  // Wide tiles on CTA pairs where the shapes allow; if the driver refuses the
-  // cooperative cluster launch on this device, the one-CTA kernel runs (remembered).
+  // Wide tiles on CTA pairs where the shapes allow.  When the driver refuses the
+  // cooperative cluster launch (not every SM free for a cluster, e.g. under a
+  // profiler or next to another context), this call runs the one-CTA kernel; a
+  // device that never accepted it is not asked again.
   static std::atomic<int> pair_state[64];  // 0 unknown, 1 launched, 2 refused
   int dev = 0;
   if (pairable(ph0) && pairable(ph1) && device_sm_count() >= 2 && cudaGetDevice(&dev) == cudaSuccess &&
       dev >= 0 && dev < 64 && pair_state[dev].load() != 2) {
     const cudaError_t err = launch_pair_impl<6>(ph0, ph1, offsets, E, P, done_counter, status, s);
-    if (err == cudaSuccess || pair_state[dev].load() == 1) {
-      if (err == cudaSuccess) pair_state[dev].store(1);
+    if (err == cudaSuccess) {
+      pair_state[dev].store(1);
       return err;
     }
-    (void)cudaGetLastError();
-    pair_state[dev].store(2);
+    (void)cudaGetLastError();   // a refused launch configuration is not a sticky error
+    if (pair_state[dev].load() != 1) pair_state[dev].store(2);
   }
   return launch_impl<256, 4, 128>(ph0, ph1, offsets, E, P, done_counter, status, s);
 }
