@@ -91,6 +91,15 @@ def test_forward_limits(layers, T, E, k):
     _check_forward(cfg, inp, layer)
 
 
+def test_forward_prefill_one_cta_tiles(layers):
+    """Prefill-size token blocks with a hidden size (384) that does not split into
+    256-row weight blocks: both projections run on the one-CTA wide-tile kernel
+    instead of the CTA-pair kernel."""
+    cfg, inp, layer = layers("tiny", T=300, E=8, k=4, H=384, I=128)
+    assert cfg.T * cfg.k > 16 * cfg.E and cfg.H % 256 != 0
+    _check_forward(cfg, inp, layer)
+
+
 @pytest.mark.parametrize("T", [64, 300])
 def test_forward_with_gpu_router(layers, T):
     cfg, inp, layer = layers("qwen3_30b_a3b_decode", T=T)
