@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "routing_dev.cuh"
 
 namespace moe {
 
@@ -272,15 +273,17 @@ __global__ void __launch_bounds__(256) mx_expand_kernel(
   __shared__ int s_poff[257];
   __shared__ int s_off[257];
   const int tid = threadIdx.x, lane = tid & 31;
+  __shared__ int s_tmp[8];
   for (int i = tid; i <= E; i += blockDim.x) s_off[i] = offsets[i];
   __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int e = 0; e < E; ++e) {
-      s_poff[e] = acc;
-      acc += ((s_off[e + 1] - s_off[e] + pad - 1) / pad) * pad;
-    }
-    s_poff[E] = acc;
+  {
+    // padded expert starts: exclusive block scan of the counts rounded up to pad
+    // (E <= 256 = blockDim.x)
+    const int c = tid < E ? ((s_off[tid + 1] - s_off[tid] + pad - 1) / pad) * pad : 0;
+    int total = 0;
+    const int pre = block_excl_scan_256(c, s_tmp, &total);
+    if (tid < E) s_poff[tid] = pre;
+    if (tid == 0) s_poff[E] = total;
   }
   __syncthreads();
   const int j = (blockIdx.x * blockDim.x + tid) >> 5;
@@ -313,15 +316,17 @@ __global__ void __launch_bounds__(256) mx_pad_sorted_kernel(
   __shared__ int s_poff[257];
   __shared__ int s_off[257];
   const int tid = threadIdx.x, lane = tid & 31;
+  __shared__ int s_tmp[8];
   for (int i = tid; i <= E; i += blockDim.x) s_off[i] = offsets[i];
   __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int e = 0; e < E; ++e) {
-      s_poff[e] = acc;
-      acc += ((s_off[e + 1] - s_off[e] + pad - 1) / pad) * pad;
-    }
-    s_poff[E] = acc;
+  {
+    // padded expert starts: exclusive block scan of the counts rounded up to pad
+    // (E <= 256 = blockDim.x)
+    const int c = tid < E ? ((s_off[tid + 1] - s_off[tid] + pad - 1) / pad) * pad : 0;
+    int total = 0;
+    const int pre = block_excl_scan_256(c, s_tmp, &total);
+    if (tid < E) s_poff[tid] = pre;
+    if (tid == 0) s_poff[E] = total;
   }
   __syncthreads();
   const int p = (blockIdx.x * blockDim.x + tid) >> 5;

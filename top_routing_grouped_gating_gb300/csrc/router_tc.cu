@@ -85,20 +85,34 @@ __global__ void __launch_bounds__(256) router_pack_kernel(const float* __restric
 }
 
 // y (T, H) fp32 -> ys (T, 3H) bf16 = [y1 | y2 | y3], the exact three-piece split.
+// Grid (ceil(H / 8 / 256), min(T, 65535)): each thread splits 8 consecutive elements
+// of rows blockIdx.y, + gridDim.y, ... (two 16-byte loads, three 16-byte stores per
+// row; H % 64 == 0 on this path).
 __global__ void __launch_bounds__(256) split_f32_kernel(const float* __restrict__ y, int T, int H,
                                                         uint16_t* __restrict__ ys) {
   pdl_wait();
   pdl_trigger();
-  const size_t n = (size_t)T * H;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const size_t t = i / H, h = i % H;
-    uint16_t p[3];
-    split3(y[i], p);
-    uint16_t* row = ys + t * 3 * H;
-    row[h] = p[0];
-    row[H + h] = p[1];
-    row[2 * H + h] = p[2];
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;   // 8-element group of a row
+  if (g >= H / 8) return;
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
+    const float4* src = reinterpret_cast<const float4*>(y + (size_t)t * H) + 2 * g;
+    const float4 a = src[0], b = src[1];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t w[3][4];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      uint16_t p0[3], p1[3];
+      split3(v[i], p0);
+      split3(v[i + 1], p1);
+#pragma unroll
+      for (int s = 0; s < 3; ++s)
+        w[s][i / 2] = static_cast<uint32_t>(p0[s]) | (static_cast<uint32_t>(p1[s]) << 16);
+    }
+    uint16_t* row = ys + (size_t)t * 3 * H + 8 * g;
+#pragma unroll
+    for (int s = 0; s < 3; ++s)
+      *reinterpret_cast<uint4*>(row + (size_t)s * H) =
+          make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
   }
 }
 
@@ -148,10 +162,9 @@ cudaError_t launch_router_tc(const void* x, bool f32in, const float* Wg, int T, 
   if (err != cudaSuccess) return err;
   const uint16_t* B = static_cast<const uint16_t*>(x);
   if (f32in) {
-    const size_t n = (size_t)T * H;
-    const unsigned grid = (unsigned)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
-    err = launch_pdl(split_f32_kernel, dim3(grid), dim3(256), 0, s, static_cast<const float*>(x),
-                     T, H, ys);
+    const dim3 grid((unsigned)((H / 8 + 255) / 256), (unsigned)(T < 65535 ? T : 65535));
+    err = launch_pdl(split_f32_kernel, grid, dim3(256), 0, s, static_cast<const float*>(x), T, H,
+                     ys);
     if (err != cudaSuccess) return err;
     B = ys;
   }
