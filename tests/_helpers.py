@@ -82,3 +82,22 @@ def routing_margin_ok(logits32: np.ndarray, k: int, tol: np.ndarray) -> np.ndarr
     else:
         need = gaps[:, :k - 1]
     return np.all(need > 2 * tol[:, None], axis=1)
+
+
+def forced_topk_logits(counts, k: int, seed: int) -> np.ndarray:
+    """fp32 router logits (T, E) whose top-k picks give expert e exactly counts[e]
+    rows (T = sum(counts) / k; every count at most T, so a token's k picks are
+    distinct).  The expert ids, sorted, are dealt out in k column blocks of T, the
+    tokens are shuffled, and slot s of a token gets the logit 4 - s; all other
+    logits lie near -2."""
+    counts = np.asarray(counts, np.int64)
+    E = counts.size
+    T = int(counts.sum()) // k
+    assert T * k == counts.sum() and counts.max() <= T
+    rng = np.random.default_rng(seed)
+    flat = np.repeat(np.arange(E), counts)
+    picks = flat.reshape(k, T).T[rng.permutation(T)]
+    lg = (rng.standard_normal((T, E)) * 0.1 - 2.0).astype(np.float32)
+    for s in range(k):
+        lg[np.arange(T), picks[:, s]] = np.float32(4.0 - s)
+    return lg

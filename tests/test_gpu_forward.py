@@ -15,7 +15,8 @@ import torch
 
 import top_routing_grouped_gating_gb300 as moe
 from oracle import moe_oracle as O
-from tests._helpers import LazyExperts, assert_close_layer, routing_margin_ok, to_np
+from tests._helpers import (LazyExperts, assert_close_layer, forced_topk_logits, routing_margin_ok,
+                           to_np)
 from top_routing_grouped_gating_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -89,6 +90,30 @@ def test_forward_single_expert_is_dense_mlp(layers):
 def test_forward_limits(layers, T, E, k):
     cfg, inp, layer = layers("tiny", T=T, E=E, k=k, H=256, I=128)
     _check_forward(cfg, inp, layer)
+
+
+@pytest.mark.parametrize("counts", [
+    [256, 257, 255, 512, 513, 1, 0, 254],   # on both sides of one and two 256-row blocks
+    [1, 16, 17, 33, 255, 256, 480, 990],    # half blocks of 8, 9, 17 (thin boxes) to 128 rows
+])
+def test_forward_token_block_boundaries(layers, counts):
+    """Expert loads on both sides of the 256-row token blocks of the wide-tile GEMM
+    (and one expert with a single row, one with none), forced through designed
+    logits; also the thin boxes for units whose half block has at most 32 rows."""
+    k = 2
+    T = sum(counts) // k
+    cfg, inp, layer = layers("tiny", T=T, E=len(counts), k=k)
+    lg = forced_topk_logits(counts, k, seed=7)
+    x = inp["x"]
+    out, ids, w = layer(x, logits_override=torch.from_numpy(lg).to(x.device))
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 0
+    r_ids, r_w = O.gating_topk_softmax(lg, k)
+    np.testing.assert_array_equal(np.bincount(r_ids.ravel(), minlength=cfg.E), counts)
+    np.testing.assert_array_equal(to_np(ids), r_ids)
+    ref = O.moe_forward(to_np(x), None, LazyExperts(inp["w13"]), LazyExperts(inp["down"]), k,
+                        logits32=lg, keep_intermediates=False)
+    assert_close_layer(to_np(out), ref["out"], what="token-block boundaries")
 
 
 def test_forward_prefill_one_cta_tiles(layers):

@@ -13,7 +13,7 @@ import torch
 
 import top_routing_grouped_gating_gb300 as moe
 from oracle import moe_oracle as O
-from tests._helpers import REL_FRO_MX, LazyExperts, rel_fro, to_np
+from tests._helpers import REL_FRO_MX, LazyExperts, forced_topk_logits, rel_fro, to_np
 from top_routing_grouped_gating_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -144,6 +144,30 @@ def test_forward_mx_small(cuda_dev, T, E, k, H, I):
     cfg = W.with_shape(W.CONFIGS["mxfp8_prefill"], T=T, E=E, k=k, H=H, I=I)
     inp, layer = _mx_layer(cfg)
     _check_mx_forward(cfg, inp, layer)
+
+
+def test_forward_mx_token_block_boundaries(cuda_dev):
+    """Expert loads on both sides of the block-scaled GEMM's token blocks (128 rows, a
+    last block absorbing up to 32 more), forced through designed logits."""
+    counts = [128, 160, 161, 288, 289, 1, 0, 1021]
+    k = 2
+    cfg = W.with_shape(W.CONFIGS["mxfp8_prefill"], T=sum(counts) // k, E=len(counts), k=k, H=256,
+                       I=128)
+    inp, layer = _mx_layer(cfg)
+    lg = forced_topk_logits(counts, k, seed=11)
+    x, r = inp["x"], inp["r"]
+    out, res, ids, w = layer(x, r, logits_override=torch.from_numpy(lg).to(x.device))
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 0
+    r_ids, _ = O.gating_topk_softmax(lg, k)
+    np.testing.assert_array_equal(np.bincount(r_ids.ravel(), minlength=cfg.E), counts)
+    np.testing.assert_array_equal(to_np(ids), r_ids)
+    ref = O.moe_forward_mx(to_np(x), to_np(r), to_np(inp["norm_w"]), cfg.eps, None,
+                           LazyExperts(inp["w13"]), LazyExperts(inp["down"]), k, logits32=lg)
+    got = to_np(out)
+    assert np.all(np.isfinite(got))
+    rf = rel_fro(got, ref["out"])
+    assert rf <= REL_FRO_MX, f"relative Frobenius error {rf:.3e}"
 
 
 @pytest.mark.parametrize("T,E,k", [(40, 256, 32), (700, 256, 8)])

@@ -494,3 +494,14 @@ def test_w4a8_layer_matches_dense_composition():
             h = O.swiglu(a @ O.mx4_roundtrip(w13[e], axis=0))
             ref[t] += w[t, sl] * (O.mx_roundtrip(h) @ O.mx4_roundtrip(down[e], axis=0))[0]
     np.testing.assert_allclose(res["out"], ref, rtol=1e-11, atol=1e-12)
+
+
+def test_forced_topk_logits_give_the_requested_loads():
+    """The designed logits of the token-block boundary tests route exactly the
+    requested number of rows to each expert (checked with the oracle's gating)."""
+    from tests._helpers import forced_topk_logits
+    for counts, k in (([256, 257, 255, 512, 513, 1, 0, 254], 2), ([5, 0, 7, 3, 6], 3)):
+        lg = forced_topk_logits(counts, k, seed=3)
+        ids, w = O.gating_topk_softmax(lg, k)
+        assert np.bincount(ids.ravel(), minlength=len(counts)).tolist() == list(counts)
+        assert all(len(set(row)) == k for row in ids.tolist())
