@@ -25,7 +25,7 @@ Sources (three blog pages on Ascend CANN inference recipes; titles as printed):
   ``floor(log2(amax)) - emax_elem``) is the OCP Microscaling Formats spec v1.0;
   the pages only name "MXFP8".
 
-Readings where the pages are silent (each is listed with its reason in the design doc):
+Readings where the pages are silent (the CUDA path takes the same ones):
 top-k ranks the fp32 logits, ties go to the lower expert id, slot order is that
 ranking; weights are renormalised over the k chosen experts; pairs are numbered
 token-major (j = t*k + s) and sorted stably by expert; ``expanded_row_idx[j]`` is
