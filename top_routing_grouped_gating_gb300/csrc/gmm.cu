@@ -23,7 +23,8 @@
 //
 // Warp roles (256 threads): warp 0 lane 0 = TMA producer; warp 1 lane 0 = MMA
 // issuer; warp 2 = TMEM allocator; warps 4-7 = epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. +31).  Shared memory holds a STAGES-deep ring of (A 128x64, B BNx64)
+// 32*(w%4) .. +31).  Prefill-size token tiles run on the CTA-pair variant further
+// down (grouped_gemm_pair_kernel), which keeps these units, roles and epilogue.  Shared memory holds a STAGES-deep ring of (A 128x64, B BNx64)
 // bf16 tiles in the 128-byte-swizzled K-major layout TMA writes; TMEM holds two
 // 128 x BN fp32 accumulators so the epilogue of one unit overlaps the MMAs of the
 // next.
