@@ -216,6 +216,58 @@ def whole_job_tokens_per_s(T: int, steps: int, world: int, ms_total: float) -> f
 # ------------------------------------------------------------ CPU oracle arm --
 
 
+def pipelined_e2e_ms(dev, stream, steps, host_inputs, run, out_like, barrier=lambda: None):
+    """Milliseconds for `steps` end-to-end steps as a serving loop runs them: each
+    step's inputs go from pinned host memory to the device on one copy stream while
+    the previous step computes, and its result comes back on another while the next
+    one computes (two input slots and two result buffers; events order each slot's
+    reuse).  Every step's H2D and D2H copy is inside the timed region.
+    run(device_inputs, slot) launches one step on `stream` and returns its device
+    result, shaped like `out_like`."""
+    import torch
+    dev_in = [[torch.empty_like(h, device=dev) for h in host_inputs] for _ in range(2)]
+    host_out = [torch.empty_like(out_like, device="cpu").pin_memory() for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]       # input slot filled
+    ev_done = [torch.cuda.Event() for _ in range(2)]     # step done with its slot and result
+    ev_back = [torch.cuda.Event() for _ in range(2)]     # result copied back
+
+    def one(i):
+        b = i % 2
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(ev_done[b])                   # step i-2 no longer reads this slot
+            for d, h in zip(dev_in[b], host_inputs):
+                d.copy_(h, non_blocking=True)
+            ev_in[b].record(h2d)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_back[b])                    # step i-2's result is on the host
+        o = run(dev_in[b], b)
+        ev_done[b].record(stream)
+        o.record_stream(d2h)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev_done[b])
+            host_out[b].copy_(o, non_blocking=True)
+            ev_back[b].record(d2h)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize(dev)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e_start.record(stream)
+    h2d.wait_event(e_start)
+    d2h.wait_event(e_start)
+    for i in range(steps):
+        one(i)
+    for b in range(2):
+        stream.wait_event(ev_back[b])                    # the last results are on the host
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    return e_start.elapsed_time(e_end)
+
+
 def oracle_arrays(inp):
     """Host fp64 copies of the inputs (untimed: the oracle's inputs at rest)."""
     E = inp["w13"].shape[0]
@@ -421,56 +473,13 @@ def run_ours(args, cfg):
         return {"p10": at(0.1), "p50": at(0.5), "p90": at(0.9), "n": len(q)}
     status = moe.get_device_status(dev)
 
-    # ---- end-to-end: pinned host input -> device -> layer -> pinned host output.
-    # A serving loop overlaps the copies with the layer: step i's input goes up on
-    # one copy stream while step i-1 computes, and its result comes back on another
-    # while step i+1 computes (two input slots and two output buffer sets).  Every
-    # step's H2D and D2H copy is inside the timed region.
-    x_host = x.cpu().pin_memory()
+    # ---- end-to-end: pinned host input -> device -> layer -> pinned host output,
+    # the copies of neighbouring steps overlapping the layer calls
     has_r = cfg.mx or cfg.prenorm
-    r_host = inp["r"].cpu().pin_memory() if has_r else None
-    o_host = [torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    x_dev = [torch.empty_like(x) for _ in range(2)]
-    r_dev = [torch.empty_like(x) if has_r else None for _ in range(2)]
-    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]       # input slot filled
-    ev_done = [torch.cuda.Event() for _ in range(2)]     # layer done with the slot and its output
-    ev_back = [torch.cuda.Event() for _ in range(2)]     # output copied back
-
-    def e2e_step(i):
-        b = i % 2
-        with torch.cuda.stream(h2d):
-            h2d.wait_event(ev_done[b])                   # step i-2 no longer reads this slot
-            x_dev[b].copy_(x_host, non_blocking=True)
-            if has_r:
-                r_dev[b].copy_(r_host, non_blocking=True)
-            ev_in[b].record(h2d)
-        stream.wait_event(ev_in[b])
-        stream.wait_event(ev_back[b])                    # step i-2's output is on the host
-        o = step(x_dev[b], r_dev[b], bi=b)
-        ev_done[b].record(stream)
-        with torch.cuda.stream(d2h):
-            d2h.wait_event(ev_done[b])
-            o_host[b].copy_(o, non_blocking=True)
-            ev_back[b].record(d2h)
-
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize(dev)
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize(dev)
-    e_start.record(stream)
-    h2d.wait_event(e_start)
-    d2h.wait_event(e_start)
-    for i in range(K):
-        e2e_step(i)
-    for b in range(2):
-        stream.wait_event(ev_back[b])                    # the last results are on the host
-    e_end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end))
+    host_in = [x.cpu().pin_memory()] + ([inp["r"].cpu().pin_memory()] if has_r else [])
+    e2e_ms = max_over_ranks(pipelined_e2e_ms(
+        dev, stream, K, host_in,
+        lambda d, b: step(d[0], d[1] if has_r else None, bi=b), bufsets[0]["out"], barrier))
 
     if rank != 0:
         if ws > 1:
@@ -585,49 +594,10 @@ def run_ep_routing(args, cfg):
     ms = s0.elapsed_time(s1)
     # end to end: this rank's inputs (x and the top-k ids) from pinned host memory,
     # the expert offsets of the re-routed rows back to the host; the copies of
-    # neighbouring steps overlap on two copy streams (two input slots), as in the
-    # layer workloads
+    # neighbouring steps overlap, as in the layer workloads
     stream = torch.cuda.current_stream(dev)
-    x_host, ids_host = x.cpu().pin_memory(), ids.cpu().pin_memory()
-    off_host = [torch.empty(El + 1, dtype=torch.int32).pin_memory() for _ in range(2)]
-    x_dev = [torch.empty_like(x) for _ in range(2)]
-    ids_dev = [torch.empty_like(ids) for _ in range(2)]
-    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_done = [torch.cuda.Event() for _ in range(2)]
-    ev_back = [torch.cuda.Event() for _ in range(2)]
-
-    def e2e_step(i):
-        b = i % 2
-        with torch.cuda.stream(h2d):
-            h2d.wait_event(ev_done[b])
-            x_dev[b].copy_(x_host, non_blocking=True)
-            ids_dev[b].copy_(ids_host, non_blocking=True)
-            ev_in[b].record(h2d)
-        stream.wait_event(ev_in[b])
-        stream.wait_event(ev_back[b])
-        o = step(x_dev[b], ids_dev[b])
-        ev_done[b].record(stream)
-        o.record_stream(d2h)   # read on the copy stream after the step's stream is done with it
-        with torch.cuda.stream(d2h):
-            d2h.wait_event(ev_done[b])
-            off_host[b].copy_(o, non_blocking=True)
-            ev_back[b].record(d2h)
-
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    h2d.wait_event(e0)
-    d2h.wait_event(e0)
-    for i in range(args.steps):
-        e2e_step(i)
-    for b in range(2):
-        stream.wait_event(ev_back[b])
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = pipelined_e2e_ms(dev, stream, args.steps, [x.cpu().pin_memory(), ids.cpu().pin_memory()],
+                              lambda d, b: step(d[0], d[1]), step())
     hbm, _, kind = measured_peaks()
     nbytes = 3 * N * cfg.H * 2
     achieved = nbytes * args.steps / (ms / 1e3) / 1e9
