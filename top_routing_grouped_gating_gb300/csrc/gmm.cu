@@ -666,7 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer --
-      const uint64_t pol_w = l2_policy_evict_normal();
+      const uint64_t pol_w_reused = l2_policy_evict_normal();
+      const uint64_t pol_w_once = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t par = 0;
@@ -691,6 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int arow = t.e * args.MW[t.ph] + (2 * t.mb + static_cast<int>(rank)) * kBM;
         const int brow = t.row0 + static_cast<int>(rank) * half;
         const int nk = args.K[t.ph] / kBK;
+        // weight tiles of an expert with one token block are read once: stream them
+        const uint64_t pol_w = (s_off[t.e + 1] - s_off[t.e]) <= kPairBN ? pol_w_once : pol_w_reused;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
             ok = false;
