@@ -509,6 +509,18 @@ def run_ours(args, cfg):
     roof.update({"traffic": tr, "kernel": "grouped_gemm_kernel (both projections, one launch)",
                  "kernel_ms": gemm_ms, "kernel_ms_pct": pct(gemm_samples), "algorithmic_bytes": gbytes,
                  "active_experts": active})
+    if decode:
+        # the whole step against the same peak: every step streams at least the GEMM's bytes
+        roof["step_achieved"] = gbytes / (ms_total / K / 1e3) / 1e9
+        roof["step_frac"] = roof["step_achieved"] / hbm
+        if not cfg.mx:
+            # the library's router launch asks L2 for the front of w13 before the GEMM starts
+            # (same sizing rule as the C library), so part of the GEMM's bytes are L2 hits
+            props = torch.cuda.get_device_properties(dev)
+            l2 = getattr(props, "L2_cache_size", 0)
+            w13 = cfg.E * cfg.H * 2 * cfg.I * 2
+            roof["l2_prefetched_bytes"] = min(w13, props.multi_processor_count * 128 * cfg.H * 2 * 5 // 8,
+                                              l2 * 5 // 8)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,

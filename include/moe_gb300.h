@@ -182,7 +182,9 @@ MOE_API moe_status moe_finalize_routing(const moe_bf16* y2, const float* topk_w,
  * The full layer in one call: router -> gating (renormalised) -> init_routing ->
  * grouped GEMM + SwiGLU -> grouped GEMM -> finalize.  Both GEMMs run in one
  * persistent launch; a down-projection tile starts once every gate/up tile of its
- * expert has been written.
+ * expert has been written.  At decode sizes (T <= 64, router run) the router
+ * launch also asks L2 to prefetch the front of w13_packed (at most 5/8 of L2) while
+ * routing runs; this changes no result.
  *   x (T,H) bf16; Wg (H,E) fp32
  *   logits_override (T,E) fp32 or NULL: when given, replaces the router output
  *   w13_packed, down_packed from moe_pack_weights

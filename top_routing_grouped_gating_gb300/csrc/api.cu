@@ -27,10 +27,22 @@ struct DeviceFacts {
   bool probed = false;
   bool arch_ok = false;
   int sm_count = 0;
+  size_t l2_bytes = 0;
   int* status = nullptr;
 };
 std::mutex g_mu;
 DeviceFacts g_dev[64];
+
+// Decode forward: while the router, gating and routing run, HBM is idle, so the
+// router launch asks L2 for the front of w13.  The grouped GEMM's first wave is
+// one 128-row w13 block (K = H) per CTA of the lowest active experts; 5/8 of that
+// wave, and at most 5/8 of L2, is requested (on a GB300 about 50 MB at H = 2048
+// and 80 MB at H = 4096: the sizes that shortened the step most in a sweep; more
+// delays the routing kernels by more than the GEMM gains).
+size_t decode_l2_hint_bytes(const DeviceFacts& d, int E, int H, int I) {
+  const size_t wave = static_cast<size_t>(d.sm_count) * 128 * H * 2;
+  return std::min({moe_packed_weight_bytes(E, H, I, 0), wave * 5 / 8, d.l2_bytes * 5 / 8});
+}
 
 moe_status current_device(DeviceFacts** out) {
   int dev = -1;
@@ -43,8 +55,11 @@ moe_status current_device(DeviceFacts** out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return MOE_ERR_CUDA;
+    int l2 = 0;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return MOE_ERR_CUDA;
     d.arch_ok = (major == 10 && minor == 3);
     d.sm_count = sms;
+    d.l2_bytes = static_cast<size_t>(l2);
     if (d.arch_ok) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return MOE_ERR_CUDA;
@@ -436,7 +451,8 @@ moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_o
       MOE_CUDA(moe::launch_router_tc(x, false, Wg, T, H, E, rp, part, extra, zw, d->status,
                                      stream));
     } else {
-      MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, part, zw, stream));
+      MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, part, zw, stream, w13_packed,
+                                  decode_l2_hint_bytes(*d, E, H, I)));
     }
     MOE_CUDA(moe::launch_gating(part, rp.splits, T, E, k, 1, ids, w, fuse, d->status, stream));
   }
@@ -1035,9 +1051,11 @@ moe_status moe_forward_v2(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
       MOE_CUDA(moe::launch_router_tc(f32in ? static_cast<const void*>(y32) : x, f32in, Wg, T, H,
                                      Eg, rp, part, extra, zw, d->status, stream));
     } else if (f32in) {
-      MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, Eg, rp, part, zw, stream));
+      MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, Eg, rp, part, zw, stream, w13_packed,
+                                      decode_l2_hint_bytes(*d, E, H, I)));
     } else {
-      MOE_CUDA(moe::launch_router(x, Wg, T, H, Eg, rp, part, zw, stream));
+      MOE_CUDA(moe::launch_router(x, Wg, T, H, Eg, rp, part, zw, stream, w13_packed,
+                                  decode_l2_hint_bytes(*d, E, H, I)));
     }
     MOE_CUDA(moe::launch_gating(part, rp.splits, T, Eg, k, 1, ids, w, fuse, d->status, stream));
   }

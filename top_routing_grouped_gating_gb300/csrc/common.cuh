@@ -96,6 +96,13 @@ MOE_DEVINL void named_bar_sync(uint32_t id, uint32_t nthreads) {
 MOE_DEVINL void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
+// Asks the memory system to bring [p, p + bytes) into L2; nothing waits for it.
+// p 16-byte aligned, bytes a multiple of 16, the range inside one allocation.
+MOE_DEVINL void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
 MOE_DEVINL uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

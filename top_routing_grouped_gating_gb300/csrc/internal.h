@@ -30,14 +30,19 @@ cudaError_t launch_router_tc(const void* x, bool f32in, const float* Wg, int T, 
                              const RouterPlan& plan, float* partial, void* extra, int* zero_word,
                              int* status, cudaStream_t s);
 // partial[s][T][E] when splits > 1, else writes out directly.  zero_word (may be
-// null) is set to 0 by the launch (the fused gating/routing counter).
+// null) is set to 0 by the launch (the fused gating/routing counter).  With a
+// decode-size plan, the launch also asks L2 to prefetch [l2_hint, l2_hint +
+// l2_hint_bytes) (16-byte aligned, inside one allocation; bytes rounded down to
+// whole 32 KB chunks), for data that later kernels of the stream read.
 cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
                           const RouterPlan& plan, float* partial_or_out, int* zero_word,
-                          cudaStream_t s);
+                          cudaStream_t s, const void* l2_hint = nullptr,
+                          size_t l2_hint_bytes = 0);
 // Same with fp32 activations (the MXFP8 path routes on the fp32 normalised input).
 cudaError_t launch_router_f32(const float* x, const float* Wg, int T, int H, int E,
                               const RouterPlan& plan, float* partial_or_out, int* zero_word,
-                              cudaStream_t s);
+                              cudaStream_t s, const void* l2_hint = nullptr,
+                              size_t l2_hint_bytes = 0);
 cudaError_t launch_router_reduce(const float* partial, int splits, int T, int E, float* logits,
                                  cudaStream_t s);
 // Optional init_routing fused into the gating launch (one-CTA routing, P <= 4096):

@@ -111,13 +111,15 @@ __global__ void __launch_bounds__(256) router_kernel(const XT* __restrict__ x,
 // pays one round of load latency.  Partial sums go to partial[split][T][E].
 constexpr int kSmallRows = 128;
 constexpr int kSmallExp = 32;
+constexpr uint32_t kPrefetchChunk = 32768;
 
 template <typename XT>
 __global__ void __launch_bounds__(256) router_small_kernel(const XT* __restrict__ x,
                                                            const float* __restrict__ Wg, int T,
                                                            int H, int E,
                                                            float* __restrict__ partial,
-                                                           int* zero_word) {
+                                                           int* zero_word, const uint8_t* l2_hint,
+                                                           size_t l2_hint_chunks) {
   __shared__ float ws[kSmallRows][kSmallExp];
   pdl_wait();
   pdl_trigger();
@@ -166,6 +168,15 @@ __global__ void __launch_bounds__(256) router_small_kernel(const XT* __restrict_
     }
   }
   __syncthreads();
+  if (l2_hint_chunks != 0 && threadIdx.x < 32) {
+    // After this CTA's own loads have landed, so they do not queue behind the
+    // hint.  Chunk c goes to lane c / nblk of CTA c % nblk: the front of the
+    // range (read first) is requested first.
+    const size_t nblk = (size_t)gridDim.x * gridDim.y * gridDim.z;
+    const size_t b = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
+    for (size_t c = b + nblk * threadIdx.x; c < l2_hint_chunks; c += nblk * 32)
+      prefetch_l2_bulk(l2_hint + c * kPrefetchChunk, kPrefetchChunk);
+  }
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
   for (int h = 0; h < kSmallRows; ++h) {
@@ -313,11 +324,13 @@ RouterPlan router_plan(int T, int H, int E) {
 
 template <typename XT>
 cudaError_t launch_router_t(const XT* x, const float* Wg, int T, int H, int E,
-                            const RouterPlan& plan, float* out, int* zero_word, cudaStream_t s) {
+                            const RouterPlan& plan, float* out, int* zero_word, cudaStream_t s,
+                            const void* l2_hint = nullptr, size_t l2_hint_bytes = 0) {
   if (plan.small) {
     dim3 grid(plan.e_tiles, plan.splits, plan.t_tiles);
+    const size_t chunks = l2_hint != nullptr ? l2_hint_bytes / kPrefetchChunk : 0;
     return launch_pdl(router_small_kernel<XT>, grid, dim3(256), 0, s, x, Wg, T, H, E, out,
-                      zero_word);
+                      zero_word, static_cast<const uint8_t*>(l2_hint), chunks);
   }
   dim3 grid(plan.t_tiles, plan.e_tiles, plan.splits);
   return launch_pdl(router_kernel<XT>, grid, dim3(256), 0, s, x, Wg, T, H, E, H / plan.splits,
@@ -325,14 +338,15 @@ cudaError_t launch_router_t(const XT* x, const float* Wg, int T, int H, int E,
 }
 
 cudaError_t launch_router(const uint16_t* x, const float* Wg, int T, int H, int E,
-                          const RouterPlan& plan, float* out, int* zero_word, cudaStream_t s) {
-  return launch_router_t(x, Wg, T, H, E, plan, out, zero_word, s);
+                          const RouterPlan& plan, float* out, int* zero_word, cudaStream_t s,
+                          const void* l2_hint, size_t l2_hint_bytes) {
+  return launch_router_t(x, Wg, T, H, E, plan, out, zero_word, s, l2_hint, l2_hint_bytes);
 }
 
 cudaError_t launch_router_f32(const float* x, const float* Wg, int T, int H, int E,
-                              const RouterPlan& plan, float* out, int* zero_word,
-                              cudaStream_t s) {
-  return launch_router_t(x, Wg, T, H, E, plan, out, zero_word, s);
+                              const RouterPlan& plan, float* out, int* zero_word, cudaStream_t s,
+                              const void* l2_hint, size_t l2_hint_bytes) {
+  return launch_router_t(x, Wg, T, H, E, plan, out, zero_word, s, l2_hint, l2_hint_bytes);
 }
 
 cudaError_t launch_router_reduce(const float* partial, int splits, int T, int E, float* logits,
