@@ -34,14 +34,15 @@ std::mutex g_mu;
 DeviceFacts g_dev[64];
 
 // Decode forward: while the router, gating and routing run, HBM is idle, so the
-// router launch asks L2 for the front of w13.  The grouped GEMM's first wave is
-// one 128-row w13 block (K = H) per CTA of the lowest active experts; 5/8 of that
-// wave, and at most 5/8 of L2, is requested (on a GB300 about 50 MB at H = 2048
-// and 80 MB at H = 4096: the sizes that shortened the step most in a sweep; more
-// delays the routing kernels by more than the GEMM gains).
-size_t decode_l2_hint_bytes(const DeviceFacts& d, int E, int H, int I) {
-  const size_t wave = static_cast<size_t>(d.sm_count) * 128 * H * 2;
-  return std::min({moe_packed_weight_bytes(E, H, I, 0), wave * 5 / 8, d.l2_bytes * 5 / 8});
+// router launch asks L2 for the front of packed w13 (w13_bytes in all, row_bytes
+// per weight row of K = H).  The grouped GEMM's first wave is one 128-row w13
+// block per CTA of the lowest active experts; 5/8 of that wave, and at most 5/8 of
+// L2, is requested (bf16 on a GB300: about 50 MB at H = 2048 and 80 MB at H = 4096,
+// the sizes that shortened the step most in a sweep; more delays the routing
+// kernels by more than the GEMM gains).
+size_t decode_l2_hint_bytes(const DeviceFacts& d, size_t w13_bytes, size_t row_bytes) {
+  const size_t wave = static_cast<size_t>(d.sm_count) * 128 * row_bytes;
+  return std::min({w13_bytes, wave * 5 / 8, d.l2_bytes * 5 / 8});
 }
 
 moe_status current_device(DeviceFacts** out) {
@@ -56,7 +57,8 @@ moe_status current_device(DeviceFacts** out) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return MOE_ERR_CUDA;
     int l2 = 0;
-    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
     d.arch_ok = (major == 10 && minor == 3);
     d.sm_count = sms;
     d.l2_bytes = static_cast<size_t>(l2);
@@ -451,8 +453,8 @@ moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_o
       MOE_CUDA(moe::launch_router_tc(x, false, Wg, T, H, E, rp, part, extra, zw, d->status,
                                      stream));
     } else {
-      MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, part, zw, stream, w13_packed,
-                                  decode_l2_hint_bytes(*d, E, H, I)));
+      const size_t hint = decode_l2_hint_bytes(*d, moe_packed_weight_bytes(E, H, I, 0), 2u * H);
+      MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, part, zw, stream, w13_packed, hint));
     }
     MOE_CUDA(moe::launch_gating(part, rp.splits, T, E, k, 1, ids, w, fuse, d->status, stream));
   }
@@ -654,7 +656,10 @@ moe_status forward_mx_impl(const moe_bf16* x, const moe_bf16* r, const moe_bf16*
       MOE_CUDA(moe::launch_router_tc(y32, true, Wg, T, H, E, rp, part, extra, zw, d->status,
                                      stream));
     } else {
-      MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, E, rp, part, zw, stream));
+      // e4m3 rows are H bytes, packed e2m1 rows H / 2
+      const size_t row = w4 ? (size_t)H / 2 : (size_t)H;
+      MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, E, rp, part, zw, stream, w13_q,
+                                      decode_l2_hint_bytes(*d, row * 2 * I * E, row)));
     }
     MOE_CUDA(moe::launch_gating(part, rp.splits, T, E, k, 1, ids, w, fuse, d->status, stream));
   }
@@ -1044,6 +1049,7 @@ moe_status moe_forward_v2(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
   } else {
     const bool f32in = y32 != nullptr;
     const moe::RouterPlan rp = moe::router_plan_ex(T, H, Eg, f32in);
+    const size_t hint = decode_l2_hint_bytes(*d, moe_packed_weight_bytes(E, H, I, 0), 2u * H);
     float* part = at<float>(ws, L.router);
     int* zw = fused_routing ? fr.counter : nullptr;
     if (rp.tc) {
@@ -1052,10 +1058,9 @@ moe_status moe_forward_v2(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
                                      Eg, rp, part, extra, zw, d->status, stream));
     } else if (f32in) {
       MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, Eg, rp, part, zw, stream, w13_packed,
-                                      decode_l2_hint_bytes(*d, E, H, I)));
+                                      hint));
     } else {
-      MOE_CUDA(moe::launch_router(x, Wg, T, H, Eg, rp, part, zw, stream, w13_packed,
-                                  decode_l2_hint_bytes(*d, E, H, I)));
+      MOE_CUDA(moe::launch_router(x, Wg, T, H, Eg, rp, part, zw, stream, w13_packed, hint));
     }
     MOE_CUDA(moe::launch_gating(part, rp.splits, T, Eg, k, 1, ids, w, fuse, d->status, stream));
   }
