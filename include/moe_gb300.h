@@ -240,6 +240,7 @@ MOE_API moe_status moe_pack_weights_mx(const moe_bf16* w13, const moe_bf16* down
  * GEMM over w13 + SwiGLU, h MX-quantised along I -> block-scaled grouped GEMM over
  * down -> finalize.  Arguments as moe_forward plus r, norm_w, eps and residual_out
  * (T,H bf16 or NULL), with the packed MX weights.  H % 256 == 0, I % 128 == 0.
+ * As in moe_forward, decode sizes also ask L2 to prefetch the front of the w13 codes.
  *   ws >= moe_forward_mx_workspace_size(T,H,E,k,I) bytes. */
 MOE_API size_t moe_forward_mx_workspace_size(int T, int H, int E, int k, int I);
 MOE_API moe_status moe_forward_mx(const moe_bf16* x, const moe_bf16* r, const moe_bf16* norm_w,
