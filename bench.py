@@ -172,6 +172,17 @@ def algorithmic_gemm_bytes(cfg, active: int, pairs: int = -1) -> int:
     return weights + acts
 
 
+def l2_hint_bytes(cfg, sm_count: int, l2_bytes: int) -> int:
+    """Bytes of packed w13 that the library's decode-size router launch asks L2 to
+    prefetch (the same rule as the C library): 5/8 of the grouped GEMM's first wave
+    (one 128-row w13 block of K = H per SM), at most 5/8 of L2 and of w13.  Only the
+    CUDA-core router (T <= 64) issues it."""
+    if cfg.T > 64:
+        return 0
+    row = cfg.H // 2 if cfg.w4 else (cfg.H if cfg.mx else 2 * cfg.H)
+    return min(cfg.E * 2 * cfg.I * row, sm_count * 128 * row * 5 // 8, l2_bytes * 5 // 8)
+
+
 def gemm_flops(cfg) -> float:
     return 2.0 * cfg.T * cfg.k * 3 * cfg.H * cfg.I
 
@@ -513,14 +524,11 @@ def run_ours(args, cfg):
         # the whole step against the same peak: every step streams at least the GEMM's bytes
         roof["step_achieved"] = gbytes / (ms_total / K / 1e3) / 1e9
         roof["step_frac"] = roof["step_achieved"] / hbm
-        if not cfg.mx:
-            # the library's router launch asks L2 for the front of w13 before the GEMM starts
-            # (same sizing rule as the C library), so part of the GEMM's bytes are L2 hits
-            props = torch.cuda.get_device_properties(dev)
-            l2 = getattr(props, "L2_cache_size", 0)
-            w13 = cfg.E * cfg.H * 2 * cfg.I * 2
-            roof["l2_prefetched_bytes"] = min(w13, props.multi_processor_count * 128 * cfg.H * 2 * 5 // 8,
-                                              l2 * 5 // 8)
+        # the library's router launch asks L2 for the front of w13 before the GEMM starts,
+        # so part of the GEMM's bytes are L2 hits
+        props = torch.cuda.get_device_properties(dev)
+        roof["l2_prefetched_bytes"] = l2_hint_bytes(cfg, props.multi_processor_count,
+                                                    getattr(props, "L2_cache_size", 0))
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
