@@ -35,7 +35,11 @@ DeviceFacts g_dev[64];
 
 // Decode forward: while the router, gating and routing run, HBM is idle, so the
 // router launch asks L2 for the front of packed w13 (w13_bytes in all, row_bytes
-// per weight row of K = H).  The grouped GEMM's first wave is one 128-row w13
+// per weight row of K = H).  This is the weight prefetch of the page
+// "基于Atlas A3集群的LongCat-Flash模型推理性能优化实践" (§权重预取): weights of a
+// memory-bound operator are pulled from HBM into L2 while an operator that needs
+// little bandwidth runs, at most bandwidth x the time available, and less if the
+// overlapped operator slows down.  The grouped GEMM's first wave is one 128-row w13
 // block per CTA of the lowest active experts; 5/8 of that wave, and at most 5/8 of
 // L2, is requested (bf16 on a GB300: about 50 MB at H = 2048 and 80 MB at H = 4096,
 // the sizes that shortened the step most in a sweep; more delays the routing

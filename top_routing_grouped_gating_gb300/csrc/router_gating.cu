@@ -169,8 +169,9 @@ __global__ void __launch_bounds__(256) router_small_kernel(const XT* __restrict_
   }
   __syncthreads();
   if (l2_hint_chunks != 0 && threadIdx.x < 32) {
-    // After this CTA's own loads have landed, so they do not queue behind the
-    // hint.  Chunk c goes to lane c / nblk of CTA c % nblk: the front of the
+    // Weight prefetch into L2 (page "基于Atlas A3集群的LongCat-Flash模型推理性能优化
+    // 实践", §权重预取).  Issued after this CTA's own loads have landed, so they do
+    // not queue behind the hint.  Chunk c goes to lane c / nblk of CTA c % nblk: the front of the
     // range (read first) is requested first.
     const size_t nblk = (size_t)gridDim.x * gridDim.y * gridDim.z;
     const size_t b = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
