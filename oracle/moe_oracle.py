@@ -205,13 +205,16 @@ def expert_mlp(a: np.ndarray, w13_e: np.ndarray, down_e: np.ndarray, return_h: b
 
 def moe_forward(x: np.ndarray, Wg: np.ndarray, w13: Sequence[np.ndarray], down: Sequence[np.ndarray],
                 k: int, logits32: Optional[np.ndarray] = None, renormalize: bool = True,
-                keep_intermediates: bool = True) -> Dict[str, np.ndarray]:
+                keep_intermediates: bool = True, expert_map=map) -> Dict[str, np.ndarray]:
     """The MoE layer: router -> gating -> init_routing -> per-expert MLP on the
     expert-sorted rows -> finalize (un-permute, weighted sum over the k slots).
 
     ``w13[e]`` / ``down[e]`` may be any array-likes (converted to fp64 one expert at a
     time, so fp32 copies of large bf16 weights are enough).  ``logits32`` replaces
     the router output (the fp32 logits the GPU is fed in routing-exact checks).
+    ``expert_map(f, experts)`` runs the per-expert MLPs (default: the builtin
+    ``map``; a thread pool's ``map`` gives the same values, since each expert's
+    rows are computed on their own and written to their own slice).
 
     [Q3MoE §高效排序和token路由, §高性能专家计算, §计算分解]
     """
@@ -228,15 +231,17 @@ def moe_forward(x: np.ndarray, Wg: np.ndarray, w13: Sequence[np.ndarray], down: 
     sri = rt["sorted_row_idx"]
     h_all = np.zeros((P, I), np.float64) if keep_intermediates else None
     y_all = np.zeros((P, H), np.float64)
-    for e in range(E):
+
+    def one_expert(e):
         lo, hi = int(offs[e]), int(offs[e + 1])
-        if hi == lo:
-            continue
         tokens = sri[lo:hi] // k
         y, h = expert_mlp(x[tokens], w13[e], down[e], return_h=True)
         y_all[lo:hi] = y
         if keep_intermediates:
             h_all[lo:hi] = h
+
+    for _ in expert_map(one_expert, [e for e in range(E) if offs[e + 1] > offs[e]]):
+        pass
     out = np.zeros((T, H), np.float64)
     eri = rt["expanded_row_idx"]
     for t in range(T):
@@ -366,13 +371,14 @@ def mx_roundtrip(y: np.ndarray, axis: int = -1) -> np.ndarray:
 
 def moe_forward_mx(x: np.ndarray, r: Optional[np.ndarray], norm_w: np.ndarray, eps: float,
                    Wg: np.ndarray, w13: Sequence[np.ndarray], down: Sequence[np.ndarray], k: int,
-                   logits32: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+                   logits32: Optional[np.ndarray] = None, expert_map=map) -> Dict[str, np.ndarray]:
     """MXFP8 layer [Q3MoE §融合RMSNorm MX量化, §融合RMSNorm Cast].
 
     s = x + r; y = RMSNorm(s); the router sees the unquantised y; the experts see
     MX(y) along H, weights MX-quantised along their reduction axis (H for w13, I for
     down), and h MX-quantised along I before the down projection.  Everything is
-    then computed in fp64 on the dequantised values.
+    then computed in fp64 on the dequantised values.  ``expert_map`` as in
+    ``moe_forward``.
     """
     s, y = add_rmsnorm(x, r, norm_w, eps)
     if logits32 is None:
@@ -385,16 +391,18 @@ def moe_forward_mx(x: np.ndarray, r: Optional[np.ndarray], norm_w: np.ndarray, e
     P = T * k
     offs, sri, eri = rt["offsets"], rt["sorted_row_idx"], rt["expanded_row_idx"]
     y_all = np.zeros((P, H), np.float64)
-    for e in range(E):
+
+    def one_expert(e):
         lo, hi = int(offs[e]), int(offs[e + 1])
-        if hi == lo:
-            continue
         a = yq[sri[lo:hi] // k]
         w13q = mx_roundtrip(w13[e], axis=0)
         downq = mx_roundtrip(down[e], axis=0)
         h = swiglu(a @ w13q)
         hq = mx_roundtrip(h, axis=-1)
         y_all[lo:hi] = hq @ downq
+
+    for _ in expert_map(one_expert, [e for e in range(E) if offs[e + 1] > offs[e]]):
+        pass
     out = np.zeros((T, H), np.float64)
     for t in range(T):
         for s_ in range(k):
@@ -639,9 +647,10 @@ def mx4_roundtrip(y: np.ndarray, axis: int = -1) -> np.ndarray:
     return np.moveaxis(v.reshape(y.shape), -1, axis)
 
 
-def moe_forward_w4a8(x, r, norm_w, eps, Wg, w13, down, k, logits32=None):
+def moe_forward_w4a8(x, r, norm_w, eps, Wg, w13, down, k, logits32=None, expert_map=map):
     """The MXFP8 layer of moe_forward_mx with MXFP4 expert weights: identical except
-    that w13 (along H) and down (along I) are quantised to e2m1 + E8M0/32."""
+    that w13 (along H) and down (along I) are quantised to e2m1 + E8M0/32.
+    ``expert_map`` as in ``moe_forward``."""
     s, y = add_rmsnorm(x, r, norm_w, eps)
     if logits32 is None:
         logits32 = router_logits_f32(y, Wg)
@@ -652,12 +661,14 @@ def moe_forward_w4a8(x, r, norm_w, eps, Wg, w13, down, k, logits32=None):
     T, H = y.shape
     offs, sri, eri = rt["offsets"], rt["sorted_row_idx"], rt["expanded_row_idx"]
     y_all = np.zeros((T * k, H), np.float64)
-    for e in range(E):
+
+    def one_expert(e):
         lo, hi = int(offs[e]), int(offs[e + 1])
-        if hi == lo:
-            continue
         h = swiglu(yq[sri[lo:hi] // k] @ mx4_roundtrip(w13[e], axis=0))
         y_all[lo:hi] = mx_roundtrip(h) @ mx4_roundtrip(down[e], axis=0)
+
+    for _ in expert_map(one_expert, [e for e in range(E) if offs[e + 1] > offs[e]]):
+        pass
     out = np.zeros((T, H), np.float64)
     for t in range(T):
         for s_ in range(k):

@@ -475,6 +475,41 @@ def test_mx4_scale_rule_and_error_bound():
     np.testing.assert_allclose(np.abs(deq[sat]), 6 * scale[sat])
 
 
+def _mx4_block_brute_force(col):
+    """One 32-element block quantised to MXFP4 element by element: the shared
+    exponent from frexp of the block's largest magnitude minus the e2m1 emax (2),
+    then each element the nearest e2m1 magnitude (saturating at 6), sign kept."""
+    import math
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    amax = max(abs(float(v)) for v in col)
+    if amax == 0.0:
+        return [0.0] * len(col)
+    X = math.frexp(amax)[1] - 1 - 2
+    out = []
+    for v in col:
+        a = min(abs(float(v)) / 2.0 ** X, 6.0)
+        q = min(grid, key=lambda g: abs(a - g))
+        out.append(math.copysign(q * 2.0 ** X, float(v)))
+    return out
+
+
+def test_mx4_roundtrip_axis():
+    """mx4_roundtrip along axis 0 of a non-square matrix (the weight layout: blocks
+    run down the reduction axis) equals an element-by-element brute force on each
+    column's 32-row blocks; the other axis (5 columns) has no 32-blocks and raises,
+    and on a 64 x 96 matrix the two axes give different results."""
+    rng = np.random.default_rng(21)
+    w = rng.standard_normal((64, 5)) * np.exp2(rng.integers(-6, 6, size=(1, 5)))
+    got = O.mx4_roundtrip(w, axis=0)
+    ref = np.array([[v for b in range(2) for v in _mx4_block_brute_force(w[32 * b:32 * (b + 1), c])]
+                    for c in range(5)]).T
+    np.testing.assert_array_equal(got, ref)
+    with pytest.raises(ValueError):
+        O.mx4_roundtrip(w, axis=-1)
+    w2 = rng.standard_normal((64, 96))
+    assert not np.array_equal(O.mx4_roundtrip(w2, axis=0), O.mx4_roundtrip(w2, axis=1))
+
+
 def test_w4a8_layer_matches_dense_composition():
     rng = np.random.default_rng(5)
     T, H, E, k, I = 5, 64, 4, 2, 32
@@ -494,6 +529,27 @@ def test_w4a8_layer_matches_dense_composition():
             h = O.swiglu(a @ O.mx4_roundtrip(w13[e], axis=0))
             ref[t] += w[t, sl] * (O.mx_roundtrip(h) @ O.mx4_roundtrip(down[e], axis=0))[0]
     np.testing.assert_allclose(res["out"], ref, rtol=1e-11, atol=1e-12)
+
+
+def test_expert_map_thread_pool_gives_identical_results():
+    """The per-expert loop run on a thread pool (as the full-size GPU parity tests
+    do) writes the same values as the serial loop, for the three layer oracles."""
+    from concurrent.futures import ThreadPoolExecutor
+    rng = np.random.default_rng(8)
+    T, H, E, k, I = 9, 64, 6, 2, 32
+    x, r = rng.standard_normal((T, H)), rng.standard_normal((T, H))
+    nw = 1 + 0.1 * rng.standard_normal(H)
+    Wg = rng.standard_normal((H, E)) * 0.3
+    w13 = [rng.standard_normal((H, 2 * I)) * 0.2 for _ in range(E)]
+    down = [rng.standard_normal((I, H)) * 0.2 for _ in range(E)]
+    with ThreadPoolExecutor(4) as ex:
+        a = O.moe_forward(x, Wg, w13, down, k, expert_map=ex.map)
+        b = O.moe_forward_mx(x, r, nw, 1e-6, Wg, w13, down, k, expert_map=ex.map)
+        c = O.moe_forward_w4a8(x, r, nw, 1e-6, Wg, w13, down, k, expert_map=ex.map)
+    np.testing.assert_array_equal(a["out"], O.moe_forward(x, Wg, w13, down, k)["out"])
+    np.testing.assert_array_equal(a["h"], O.moe_forward(x, Wg, w13, down, k)["h"])
+    np.testing.assert_array_equal(b["out"], O.moe_forward_mx(x, r, nw, 1e-6, Wg, w13, down, k)["out"])
+    np.testing.assert_array_equal(c["out"], O.moe_forward_w4a8(x, r, nw, 1e-6, Wg, w13, down, k)["out"])
 
 
 def test_forced_topk_logits_give_the_requested_loads():
