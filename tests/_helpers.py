@@ -1,4 +1,7 @@
 """Test helpers: tensor conversion, tolerance checks, lazy per-expert weight access."""
+import os
+import threading
+
 import numpy as np
 import pytest
 import torch
@@ -42,22 +45,40 @@ def assert_close_layer(got, ref, rel=REL_FRO, max_abs_frac=MAX_ABS_FRAC, what="o
 
 class LazyExperts:
     """Indexable view of a (E, a, b) torch weight tensor: w[e] -> fp32 numpy array,
-    converted one expert at a time (the oracle widens it to fp64)."""
+    converted one expert at a time (the oracle widens it to fp64).  Safe to index
+    from several threads (the oracle's per-expert loop on a thread pool)."""
 
     def __init__(self, w: torch.Tensor):
         self.w = w
         self._cache = {}
+        self._lock = threading.Lock()
 
     def __len__(self):
         return self.w.shape[0]
 
     def __getitem__(self, e):
         e = int(e)
-        if e not in self._cache:
-            if len(self._cache) > 16:
-                self._cache.clear()
-            self._cache[e] = self.w[e].float().cpu().numpy()
-        return self._cache[e]
+        with self._lock:
+            v = self._cache.get(e)
+            if v is None:
+                if len(self._cache) >= 32:
+                    self._cache.pop(next(iter(self._cache)))
+                v = self._cache[e] = self.w[e].float().cpu().numpy()
+            return v
+
+
+def oracle_threads() -> int:
+    """Host threads for the oracle's per-expert loop in the full-size tests."""
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def expert_coverage(ids: np.ndarray, rows: np.ndarray, E: int):
+    """(experts hit by the compared tokens, experts active in the whole batch)."""
+    active = np.unique(ids.ravel())
+    active = active[active < E]
+    hit = np.unique(ids[rows].ravel())
+    hit = hit[hit < E]
+    return int(hit.size), int(active.size)
 
 
 @pytest.fixture(scope="session")

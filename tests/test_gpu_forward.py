@@ -3,20 +3,22 @@ CPU oracle on the seeded workloads, at their full sizes.
 
 Routing is checked bit-exactly by feeding both sides the oracle's fp32 logits
 (logits_override), so the comparison of outputs cannot be masked by near-tie
-routing flips of the fp32 router.  Where the oracle would take minutes at full
-size, every token is still computed on the GPU and a seeded sample of tokens is
-checked (tokens are independent in this layer).  A separate test runs the GPU
-router and compares the tokens whose routing margin is larger than the router's
-error bound.
+routing flips of the fp32 router.  Every configuration, the two prefill layers
+(4096 and 8192 tokens) included, is compared on every token, so every active
+expert and every expert's last token block is checked; the oracle's per-expert
+loop runs on a host thread pool there.  A separate test runs the GPU router and
+compares the tokens whose routing margin is larger than the router's error bound.
 """
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
 
 import top_routing_grouped_gating_gb300 as moe
 from oracle import moe_oracle as O
-from tests._helpers import (LazyExperts, assert_close_layer, forced_topk_logits, routing_margin_ok,
-                           to_np)
+from tests._helpers import (LazyExperts, assert_close_layer, expert_coverage, forced_topk_logits,
+                           oracle_threads, routing_margin_ok, to_np)
 from top_routing_grouped_gating_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -41,7 +43,7 @@ def layers(cuda_dev):
     return get
 
 
-def _check_forward(cfg, inp, layer, sample=None):
+def _check_forward(cfg, inp, layer, sample=None, threads=1):
     x, Wg = inp["x"], inp["Wg"]
     xn = to_np(x)
     lg32 = O.router_logits_f32(xn, to_np(Wg))
@@ -52,8 +54,12 @@ def _check_forward(cfg, inp, layer, sample=None):
     np.testing.assert_array_equal(to_np(ids), r_ids)
     np.testing.assert_allclose(to_np(w), r_w, rtol=2e-6, atol=1e-7)
     rows = np.arange(cfg.T) if sample is None else sample
-    ref = O.moe_forward(xn[rows], None, LazyExperts(inp["w13"]), LazyExperts(inp["down"]), cfg.k,
-                        logits32=lg32[rows], keep_intermediates=False)
+    with ThreadPoolExecutor(threads) as pool:
+        ref = O.moe_forward(xn[rows], None, LazyExperts(inp["w13"]), LazyExperts(inp["down"]), cfg.k,
+                            logits32=lg32[rows], keep_intermediates=False,
+                            expert_map=pool.map if threads > 1 else map)
+    hit, active = expert_coverage(r_ids, rows, cfg.E)
+    print(f"{cfg.name}: {len(rows)}/{cfg.T} tokens compared, {hit}/{active} active experts covered")
     return assert_close_layer(to_np(out)[rows], ref["out"], what=cfg.name)
 
 
@@ -63,14 +69,13 @@ def test_forward_full_oracle(layers, name):
     _check_forward(cfg, inp, layer)
 
 
-@pytest.mark.parametrize("name,nsample", [("qwen3_30b_a3b_prefill_zipf", 96),
-                                          ("qwen3_235b_a22b_prefill", 48)])
-def test_forward_prefill_sampled(layers, name, nsample):
+@pytest.mark.parametrize("name", ["qwen3_30b_a3b_prefill_zipf", "qwen3_235b_a22b_prefill"])
+def test_forward_prefill_full_oracle(layers, name):
+    """The prefill layers at full size (4096 tokens, Zipf-skewed loads; 8192 tokens,
+    uniform) against the oracle on every token: every active expert, every token
+    block of the CTA-pair GEMM and every expert's last, partial block."""
     cfg, inp, layer = layers(name)
-    rng = np.random.default_rng(0)
-    sample = np.sort(rng.choice(cfg.T, nsample, replace=False))
-    sample[0], sample[-1] = 0, cfg.T - 1
-    _check_forward(cfg, inp, layer, sample=np.unique(sample))
+    _check_forward(cfg, inp, layer, threads=oracle_threads())
 
 
 @pytest.mark.parametrize("T", [1, 3, 17, 100])

@@ -7,13 +7,16 @@ dequantised values, since the oracle's fp64 normalisation can sit on the other
 side of a rounding boundary.  The layer output must stay within relative
 Frobenius error 4e-2 of the oracle run on dequantised inputs.
 """
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
 
 import top_routing_grouped_gating_gb300 as moe
 from oracle import moe_oracle as O
-from tests._helpers import REL_FRO_MX, LazyExperts, forced_topk_logits, rel_fro, to_np
+from tests._helpers import (REL_FRO_MX, LazyExperts, expert_coverage, forced_topk_logits, oracle_threads,
+                           rel_fro, to_np)
 from top_routing_grouped_gating_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -116,7 +119,7 @@ def _mx_layer(cfg, device="cuda"):
     return inp, layer
 
 
-def _check_mx_forward(cfg, inp, layer, sample=None):
+def _check_mx_forward(cfg, inp, layer, sample=None, threads=1):
     x, r = inp["x"], inp["r"]
     xn, rn, wn = to_np(x), to_np(r), to_np(inp["norm_w"])
     _, y = O.add_rmsnorm(xn, rn, wn, cfg.eps)
@@ -127,8 +130,12 @@ def _check_mx_forward(cfg, inp, layer, sample=None):
     r_ids, r_w = O.gating_topk_softmax(lg32, cfg.k)
     np.testing.assert_array_equal(to_np(ids), r_ids)
     rows = np.arange(cfg.T) if sample is None else sample
-    ref = O.moe_forward_mx(xn[rows], rn[rows], wn, cfg.eps, None, LazyExperts(inp["w13"]),
-                           LazyExperts(inp["down"]), cfg.k, logits32=lg32[rows])
+    with ThreadPoolExecutor(threads) as pool:
+        ref = O.moe_forward_mx(xn[rows], rn[rows], wn, cfg.eps, None, LazyExperts(inp["w13"]),
+                               LazyExperts(inp["down"]), cfg.k, logits32=lg32[rows],
+                               expert_map=pool.map if threads > 1 else map)
+    hit, active = expert_coverage(r_ids, rows, cfg.E)
+    print(f"{cfg.name}: {len(rows)}/{cfg.T} tokens compared, {hit}/{active} active experts covered")
     got = to_np(out)[rows]
     assert np.all(np.isfinite(got))
     rf = rel_fro(got, ref["out"])
@@ -192,11 +199,13 @@ def test_forward_mx_decode_tiles_skewed(cuda_dev):
     assert np.bincount(ids.ravel(), minlength=cfg.E).max() > 128   # two atoms, all groups
 
 
-def test_forward_mx_full_size_sampled(cuda_dev):
+def test_forward_mx_full_size(cuda_dev):
+    """The MXFP8 prefill layer at full size (4096 tokens, 128 experts, H = 4096,
+    I = 1536) against the oracle on every token, so every expert and every token
+    block of the block-scaled GEMM is compared."""
     cfg = W.CONFIGS["mxfp8_prefill"]
     inp, layer = _mx_layer(cfg)
-    sample = np.array([0, 1777, cfg.T - 1])
-    _check_mx_forward(cfg, inp, layer, sample=sample)
+    _check_mx_forward(cfg, inp, layer, threads=oracle_threads())
     a = layer(inp["x"], inp["r"])[0].clone()
     b = layer(inp["x"], inp["r"])[0]
     assert torch.equal(a, b)

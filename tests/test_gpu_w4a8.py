@@ -6,13 +6,15 @@ bf16 weights, and the e2m1 codes, their nibble packing and the E8M0 scale atoms
 must match exactly.  The layer output is held to the MXFP8 layer's relative
 Frobenius bound against ``moe_forward_w4a8`` run on the same dequantised values.
 """
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
 
 import top_routing_grouped_gating_gb300 as moe
 from oracle import moe_oracle as O
-from tests._helpers import REL_FRO_MX, LazyExperts, rel_fro, to_np
+from tests._helpers import REL_FRO_MX, LazyExperts, expert_coverage, oracle_threads, rel_fro, to_np
 from tests.test_gpu_mx import _unpack_w13
 from top_routing_grouped_gating_gb300 import workloads as W
 
@@ -86,7 +88,7 @@ def _w4_layer(cfg, device="cuda"):
     return inp, layer
 
 
-def _check_w4_forward(cfg, inp, layer, sample=None):
+def _check_w4_forward(cfg, inp, layer, sample=None, threads=1):
     x, r = inp["x"], inp["r"]
     xn, rn, wn = to_np(x), to_np(r), to_np(inp["norm_w"])
     _, y = O.add_rmsnorm(xn, rn, wn, cfg.eps)
@@ -97,8 +99,12 @@ def _check_w4_forward(cfg, inp, layer, sample=None):
     r_ids, _ = O.gating_topk_softmax(lg32, cfg.k)
     np.testing.assert_array_equal(to_np(ids), r_ids)
     rows = np.arange(cfg.T) if sample is None else sample
-    ref = O.moe_forward_w4a8(xn[rows], rn[rows], wn, cfg.eps, None, LazyExperts(inp["w13"]),
-                             LazyExperts(inp["down"]), cfg.k, logits32=lg32[rows])
+    with ThreadPoolExecutor(threads) as pool:
+        ref = O.moe_forward_w4a8(xn[rows], rn[rows], wn, cfg.eps, None, LazyExperts(inp["w13"]),
+                                 LazyExperts(inp["down"]), cfg.k, logits32=lg32[rows],
+                                 expert_map=pool.map if threads > 1 else map)
+    hit, active = expert_coverage(r_ids, rows, cfg.E)
+    print(f"{cfg.name}: {len(rows)}/{cfg.T} tokens compared, {hit}/{active} active experts covered")
     got = to_np(out)[rows]
     assert np.all(np.isfinite(got))
     rf = rel_fro(got, ref["out"])
@@ -155,10 +161,11 @@ def test_w4a8_differs_from_mxfp8(cuda_dev):
     assert e4 < 0.5 * e8
 
 
-def test_forward_w4a8_full_size_sampled(cuda_dev):
+def test_forward_w4a8_full_size(cuda_dev):
+    """The W4A8 prefill layer at full size against the oracle on every token."""
     cfg = W.CONFIGS["w4a8_prefill"]
     inp, layer = _w4_layer(cfg)
-    _check_w4_forward(cfg, inp, layer, sample=np.array([0, 2049, cfg.T - 1]))
+    _check_w4_forward(cfg, inp, layer, threads=oracle_threads())
     a = layer(inp["x"], inp["r"])[0].clone()
     b = layer(inp["x"], inp["r"])[0]
     assert torch.equal(a, b)
@@ -167,7 +174,7 @@ def test_forward_w4a8_full_size_sampled(cuda_dev):
 def test_forward_w4a8_decode_full_size(cuda_dev):
     cfg = W.CONFIGS["w4a8_decode"]
     inp, layer = _w4_layer(cfg)
-    _check_w4_forward(cfg, inp, layer, sample=np.arange(0, cfg.T, 7))
+    _check_w4_forward(cfg, inp, layer, threads=oracle_threads())
 
 
 def test_w4a8_rejects_unaligned_codes(cuda_dev):
