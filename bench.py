@@ -2,22 +2,38 @@
 """Benchmark of the MoE-layer forward on GB300 (one JSON line on stdout, rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload NAME|all] [--no-cpu-baseline]
 
 A step is one ``moe_forward`` call (router -> gating -> init_routing -> grouped GEMM
-+ SwiGLU -> grouped GEMM -> finalize) over one batch of T tokens of the workload,
-with inputs and packed weights resident in HBM.  The default workload is the
-Qwen3-30B-A3B-shaped decode layer (T=32, H=2048, E=128, k=8, I=768): its active
-expert weights (~1 GB) are far larger than L2, so no L2 flush is needed between
-steps.  Timing uses CUDA events on the launching stream, bracketed by a barrier
-and a device synchronize, max over ranks.
++ SwiGLU -> grouped GEMM -> finalize; the MXFP8 layer adds the fused add + RMSNorm +
+MX quantisation in front) over one batch of T tokens of the workload, with inputs
+and packed weights resident in HBM.
+
+With no ``--workload`` (``all``) the five measured layer shapes run one after the
+other, each in its own timed region: Qwen3-30B-A3B decode (T=32), Qwen3-30B-A3B
+prefill with a Zipf-skewed router (T=4096), Qwen3-235B-A22B decode (T=64), the MXFP8
+prefill (T=4096, H=4096) and, last, the largest, Qwen3-235B-A22B prefill (T=8192,
+H=4096, E=128, k=8, I=1536).  The printed line is that last workload's; it carries
+every workload's result under ``"workloads"``.  Each workload's full line also goes
+to stderr.
+
+Timing per workload: W untimed warm-up steps; then the headline timed region of K
+steps with CUDA events only at its two ends (no event between steps, since an
+event between two kernels costs their programmatic launch overlap), bracketed by a
+barrier and a device synchronize, max over ranks; then a second, separate pass of
+K steps with events around every step and around every grouped-GEMM launch, which
+gives the per-step percentiles and the GEMM time behind the roofline; then the
+end-to-end pass through pinned host buffers.  Every workload streams more weight
+bytes per step than the 129 MB L2 holds (the active experts' weights), so no L2
+flush is needed between steps.
 
 Multi-GPU: tokens are independent, so N GPUs run N replicas of the layer on their
 own batches with no collective on the data path (weak scaling); torch.distributed
 is used only for the barrier and the max-over-ranks of the elapsed time.
 
 ``--impl reference`` times the CPU fp64 oracle (the test oracle under ``oracle/``,
-unmodified) on the host cores, on a bounded sample of tokens per step.
+unmodified) on the host cores, on the same bounded token sample as the
+``cpu_baseline`` field of the GPU arm.
 """
 from __future__ import annotations
 
@@ -40,15 +56,22 @@ FALLBACK_BF16_TFLOPS = 1900.0
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# The measured layer shapes, the largest (the headline) last.
+SUITE = ("qwen3_30b_a3b_decode", "qwen3_30b_a3b_prefill_zipf", "qwen3_235b_a22b_decode",
+         "mxfp8_prefill", "qwen3_235b_a22b_prefill")
+HEADLINE = SUITE[-1]
+# Tokens per oracle call in the CPU baseline (both arms): the whole batch of a
+# decode workload, a slice of this many consecutive tokens of a prefill batch.
+ORACLE_SAMPLE_TOKENS = 64
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen3_30b_a3b_decode")
+    ap.add_argument("--workload", default="all", help="a workload name, or 'all' (the five measured shapes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the cpu_baseline sample")
@@ -117,7 +140,6 @@ class ClockSampler:
     def __init__(self, dev_index: int):
         import torch
         self.proc = None
-        self.lines = []
         sel = []
         try:
             props = torch.cuda.get_device_properties(dev_index)
@@ -158,18 +180,40 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def algorithmic_gemm_bytes(cfg, active: int, pairs: int = -1) -> int:
-    """Bytes one grouped-GEMM launch must move: the active experts' w13 and down
-    weights, the expert-sorted activations in, h out and back in, y2 out (for the
-    token-expert pairs routed to real experts)."""
+# ------------------------------------------------------ algorithmic work ---
+
+
+def gemm_weight_bytes(cfg, active: int) -> int:
+    """The active experts' w13 and down weights as the grouped GEMM reads them: bf16,
+    or e4m3 codes (e2m1: half a byte) plus one E8M0 byte per 32 elements."""
+    if cfg.mx:
+        return active * 3 * cfg.H * cfg.I * (17 if cfg.w4 else 33) // 32
+    return active * 3 * cfg.H * cfg.I * 2
+
+
+def gemm_implementation_bytes(cfg, pairs: int = -1) -> int:
+    """The grouped GEMM's intermediate traffic (not credited to the roofline): the
+    expert-sorted activations read, h written and read back, y2 written, for the
+    token-expert pairs routed to real experts."""
     P = cfg.T * cfg.k if pairs < 0 else pairs
-    if cfg.mx:  # e4m3 (e2m1: half a byte) codes plus one E8M0 byte per 32 elements; y2 stays bf16
-        weights = active * 3 * cfg.H * cfg.I * (17 if cfg.w4 else 33) // 32
-        acts = P * cfg.H * 33 // 32 + 2 * P * cfg.I * 33 // 32 + P * cfg.H * 2
-        return weights + acts
-    weights = active * 3 * cfg.H * cfg.I * 2
-    acts = P * cfg.H * 2 + 2 * P * cfg.I * 2 + P * cfg.H * 2
-    return weights + acts
+    if cfg.mx:
+        return P * cfg.H * 33 // 32 + 2 * P * cfg.I * 33 // 32 + P * cfg.H * 2
+    return P * cfg.H * 2 + 2 * P * cfg.I * 2 + P * cfg.H * 2
+
+
+def layer_algorithmic_bytes(cfg, active: int) -> int:
+    """Bytes the whole layer call must move at the least: the active experts' weights,
+    the router weights W_g (fp32), the input x (and the residual r with the norm
+    weight for the normed layers) read, the output (and residual_out) written, the
+    top-k ids and weights written."""
+    T, H, P = cfg.T, cfg.H, cfg.T * cfg.k
+    normed = cfg.mx or cfg.prenorm
+    b = gemm_weight_bytes(cfg, active)
+    b += H * (cfg.E + cfg.Z) * 4
+    b += T * H * 2 * (2 if normed else 1) + (H * 2 if normed else 0)
+    b += T * H * 2 * (2 if normed else 1)
+    b += P * 4 * 2
+    return b
 
 
 def l2_hint_bytes(cfg, sm_count: int, l2_bytes: int) -> int:
@@ -185,6 +229,29 @@ def l2_hint_bytes(cfg, sm_count: int, l2_bytes: int) -> int:
 
 def gemm_flops(cfg) -> float:
     return 2.0 * cfg.T * cfg.k * 3 * cfg.H * cfg.I
+
+
+def is_decode(cfg) -> bool:
+    """Decode-size (HBM-bound) layer: at most 16 token-expert pairs per expert."""
+    return cfg.T * cfg.k <= 16 * cfg.E
+
+
+def hbm_roofline(weight_bytes: int, layer_bytes: int, l2_prefetched: int, kernel_ms: float,
+                 step_ms: float, peak_gbs: float) -> dict:
+    """HBM roofline of a decode-size layer.  The grouped GEMM's own HBM rate counts the
+    weight bytes it pulled from HBM itself, i.e. net of those the router launch had
+    already asked L2 for; the whole step counts the layer's algorithmic bytes."""
+    achieved = (weight_bytes - l2_prefetched) / (kernel_ms / 1e3) / 1e9
+    step = layer_bytes / (step_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
+            "frac": achieved / peak_gbs, "step_achieved": step, "step_frac": step / peak_gbs}
+
+
+def tensor_roofline(flops: float, kernel_ms: float, step_ms: float, peak_tflops: float) -> dict:
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    step = flops / (step_ms / 1e3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+            "frac": achieved / peak_tflops, "step_achieved": step, "step_frac": step / peak_tflops}
 
 
 def launches_per_step(cfg, router: bool = True) -> int:
@@ -224,7 +291,10 @@ def whole_job_tokens_per_s(T: int, steps: int, world: int, ms_total: float) -> f
     return T * steps * world / (ms_total / 1e3)
 
 
-# ------------------------------------------------------------ CPU oracle arm --
+def percentiles(v):
+    q = sorted(v)
+    at = lambda f: q[min(len(q) - 1, int(round(f * (len(q) - 1))))]
+    return {"p10": at(0.1), "p50": at(0.5), "p90": at(0.9), "n": len(q)}
 
 
 def pipelined_e2e_ms(dev, stream, steps, host_inputs, run, out_like, barrier=lambda: None):
@@ -279,11 +349,36 @@ def pipelined_e2e_ms(dev, stream, steps, host_inputs, run, out_like, barrier=lam
     return e_start.elapsed_time(e_end)
 
 
-def oracle_arrays(inp):
-    """Host fp64 copies of the inputs (untimed: the oracle's inputs at rest)."""
+# ------------------------------------------------------------ CPU oracle ---
+
+
+def oracle_sample_tokens(cfg) -> int:
+    """Tokens per oracle call in the CPU baseline: the whole batch of a decode
+    workload, a slice of consecutive tokens of a prefill batch."""
+    return min(cfg.T, ORACLE_SAMPLE_TOKENS)
+
+
+def host_memory_bytes() -> int:
+    try:
+        return os.sysconf("SC_PHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        return 0
+
+
+def oracle_weight_dtype(cfg) -> str:
+    """fp64 host copies of the expert weights when they take at most a quarter of
+    the host memory, else fp32 (the oracle then widens one expert at a time)."""
+    fp64_bytes = cfg.E * 3 * cfg.H * cfg.I * 8
+    return "float64" if 4 * fp64_bytes <= host_memory_bytes() else "float32"
+
+
+def oracle_arrays(inp, cfg):
+    """Host copies of the inputs (untimed: the oracle's inputs at rest)."""
+    import torch
+    wt = torch.float64 if oracle_weight_dtype(cfg) == "float64" else torch.float32
     E = inp["w13"].shape[0]
-    arr = {"w13": [inp["w13"][e].double().cpu().numpy() for e in range(E)],
-           "down": [inp["down"][e].double().cpu().numpy() for e in range(E)]}
+    arr = {"w13": [inp["w13"][e].cpu().to(wt).numpy() for e in range(E)],
+           "down": [inp["down"][e].cpu().to(wt).numpy() for e in range(E)]}
     for key in ("x", "Wg", "r", "norm_w"):
         if key in inp:
             arr[key] = inp[key].double().cpu().numpy()
@@ -303,55 +398,61 @@ def oracle_step(O, arrays, cfg, rows):
         O.moe_forward(a["x"][rows], a["Wg"], a["w13"], a["down"], cfg.k, keep_intermediates=False)
 
 
+def oracle_sample_rows(cfg, i: int):
+    """The i-th sample: consecutive tokens of the batch (wrapping around)."""
+    n = oracle_sample_tokens(cfg)
+    return [(i * n + j) % cfg.T for j in range(n)]
+
+
+def oracle_sample_text(cfg, calls: int, seconds: float) -> str:
+    n = oracle_sample_tokens(cfg)
+    what = "the whole batch" if n == cfg.T else f"a slice of {n} consecutive tokens of the {cfg.T}-token batch"
+    held = ("pre-widened to fp64" if oracle_weight_dtype(cfg) == "float64"
+            else "held in fp32 (widened to fp64 by the oracle, one expert at a time)")
+    return (f"{calls} oracle calls of {n} tokens each ({what}) over {seconds:.1f} s; numpy fp64 oracle "
+            f"as committed, weights {held} in host memory")
+
+
 def time_oracle(O, arrays, cfg, target_s):
     """Tokens/s of the oracle on consecutive token samples until ~target_s of CPU time."""
-    n = 0
+    oracle_step(O, arrays, cfg, oracle_sample_rows(cfg, 0))   # first touch of the arrays, untimed
+    calls = 0
     t0 = time.perf_counter()
-    start = 0
-    while time.perf_counter() - t0 < target_s:
-        rows = [(start + i) % cfg.T for i in range(min(cfg.T, 4))]
-        oracle_step(O, arrays, cfg, rows)
-        n += len(rows)
-        start += len(rows)
+    while time.perf_counter() - t0 < target_s or calls == 0:
+        oracle_step(O, arrays, cfg, oracle_sample_rows(cfg, calls + 1))
+        calls += 1
     dt = time.perf_counter() - t0
-    return n / dt, n, dt
+    return calls * oracle_sample_tokens(cfg) / dt, calls, dt
 
 
 def run_reference(args, cfg):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    import numpy as np
     import torch
     from oracle import moe_oracle as O
     from top_routing_grouped_gating_gb300 import workloads as W
 
     gen_dev = "cuda" if torch.cuda.is_available() else "cpu"   # same values as the GPU arm
     inp = W.make_inputs(cfg, device=gen_dev)
-    arrays = oracle_arrays(inp)
+    arrays = oracle_arrays(inp, cfg)
     del inp
-    # size each step's token sample so the whole K+W run stays within a few minutes
-    t0 = time.perf_counter()
-    oracle_step(O, arrays, cfg, [0])
-    per_tok = max(time.perf_counter() - t0, 1e-4)
-    budget = 150.0 / max(args.steps + args.warmup, 1)
-    ntok = int(max(1, min(cfg.T, budget // per_tok)))
+    if gen_dev == "cuda":
+        torch.cuda.empty_cache()
     for i in range(args.warmup):
-        oracle_step(O, arrays, cfg, [(i * ntok + j) % cfg.T for j in range(ntok)])
+        oracle_step(O, arrays, cfg, oracle_sample_rows(cfg, i))
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle_step(O, arrays, cfg, [(i * ntok + j) % cfg.T for j in range(ntok)])
+        oracle_step(O, arrays, cfg, oracle_sample_rows(cfg, args.warmup + i))
     dt = time.perf_counter() - t0
-    value = ntok * args.steps / dt
-    cores = blas_threads()
+    value = oracle_sample_tokens(cfg) * args.steps / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(cfg),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{ntok} token(s) of the workload per step, numpy fp64 oracle, "
-                                   f"weights pre-widened to fp64 in host memory"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": oracle_sample_text(cfg, args.steps, dt)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -365,6 +466,8 @@ def workload_config(cfg):
         extra["zero_computation_experts"] = cfg.Z
     if cfg.prenorm:
         extra["fused_add_rmsnorm_cast"] = True
+    if cfg.mx:
+        extra["fused_add_rmsnorm_mxquant"] = True
     return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, **extra,
             "router": cfg.router, "seed": cfg.seed, "parallelism": "replicas (token batches), no collective",
             "l2": "inputs larger than L2: the active experts' weights streamed per step exceed the 129 MB L2"}
@@ -373,61 +476,59 @@ def workload_config(cfg):
 # ------------------------------------------------------------------- ours ---
 
 
-def run_ours(args, cfg):
-    import numpy as np
+def make_layer(moe, cfg, inp):
+    """The layer object and a step(x, r, slot) closure over two output buffer sets."""
     import torch
-
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-
-    from top_routing_grouped_gating_gb300 import build as B
-    B.build()
-    import top_routing_grouped_gating_gb300 as moe
-    from top_routing_grouped_gating_gb300 import workloads as W
-
-    inp = W.make_inputs(cfg, device=f"cuda:{local}")
     x = inp["x"]
-    stream = torch.cuda.current_stream(dev)
     if cfg.mx:
         cls = moe.MoELayerW4A8 if cfg.w4 else moe.MoELayerMX
         layer = cls(inp["Wg"], inp["w13"], inp["down"], inp["norm_w"], cfg.k, cfg.eps)
-        r = inp["r"]
-        out, res, ids, w = layer(x, r)
+        out, res, ids, w = layer(x, inp["r"])
         bufs = dict(out=out, residual_out=res, topk_ids=ids, topk_w=w)
-
-        def step(xx, rr=r, bi=0):
-            return layer(xx, rr, **bufsets[bi])[0]
     elif cfg.prenorm or cfg.Z:
         layer = moe.MoELayerV2(inp["Wg"], inp["w13"], inp["down"], cfg.k, Z=cfg.Z,
                                norm_w=inp["norm_w"] if cfg.prenorm else None, eps=cfg.eps)
-        r = inp["r"] if cfg.prenorm else None
-        out, res, ids, w = layer(x, r)
+        out, res, ids, w = layer(x, inp["r"] if cfg.prenorm else None)
         bufs = dict(out=out, residual_out=res, topk_ids=ids, topk_w=w)
-
-        def step(xx, rr=r, bi=0):
-            return layer(xx, rr, **bufsets[bi])[0]
     else:
         layer = moe.MoELayer(inp["Wg"], inp["w13"], inp["down"], cfg.k)
         out, ids, w = layer(x)
         bufs = dict(out=out, topk_ids=ids, topk_w=w)
-
-        def step(xx, rr=None, bi=0):
-            return layer(xx, **bufsets[bi])[0]
     # a second set of output buffers for the double-buffered end-to-end loop
     bufsets = [bufs, {key: (torch.empty_like(v) if v is not None else None) for key, v in bufs.items()}]
+    has_r = cfg.mx or cfg.prenorm
+
+    def step(xx, rr=None, bi=0):
+        if has_r:
+            return layer(xx, rr, **bufsets[bi])[0]
+        return layer(xx, **bufsets[bi])[0]
+    return layer, step, bufsets, ids
+
+
+def measure(args, cfg, dev, cpu_baseline: bool):
+    """One workload: warm-up, the headline timed region, the instrumented pass, the
+    end-to-end pass (and the CPU baseline when asked).  Returns rank 0's JSON line
+    (None on other ranks)."""
+    import torch
+    import top_routing_grouped_gating_gb300 as moe
+    from top_routing_grouped_gating_gb300 import workloads as W
+
+    ws, rank, local = dist_env()
+    inp = W.make_inputs(cfg, device=f"cuda:{local}")
+    x = inp["x"]
+    r = inp.get("r") if (cfg.mx or cfg.prenorm) else None
+    stream = torch.cuda.current_stream(dev)
+    layer, step, bufsets, ids = make_layer(moe, cfg, inp)
     torch.cuda.synchronize(dev)
     counts = torch.bincount(ids.flatten().long(), minlength=cfg.E + cfg.Z)[:cfg.E]
     active = int((counts > 0).sum())
     routed_pairs = int(counts.sum())
-    if args.no_cpu_baseline:
-        # the packed copies are all the layer uses; drop the logical weights
-        del inp["w13"], inp["down"]
-        torch.cuda.empty_cache()
+    host_w = None
+    if cpu_baseline and rank == 0:
+        host_w = {k_: v.cpu() for k_, v in inp.items()}   # bf16/fp32 host copies, widened later
+    # the packed copies are all the layer uses; drop the logical weights
+    del inp["w13"], inp["down"]
+    torch.cuda.empty_cache()
 
     def barrier():
         rank_barrier(ws)
@@ -435,105 +536,100 @@ def run_ours(args, cfg):
     def max_over_ranks(v: float) -> float:
         return reduce_max_over_ranks(v, ws, dev)
 
+    K = args.steps
     # ---- warm-up
     for _ in range(max(args.warmup, 3)):
-        step(x)
+        step(x, r)
     torch.cuda.synchronize(dev)
 
-    # ---- timed region (device-resident inputs), grouped-GEMM events on every step
-    K = args.steps
-    # grouped-GEMM events on every GEMM_EVERY-th step of the timed region (an event
-    # pair between two kernels costs their programmatic launch overlap)
-    GEMM_EVERY = max(1, min(32, K // 8))
-    timed = list(range(0, K, GEMM_EVERY))
-    gb = {i: torch.cuda.Event(enable_timing=True) for i in timed}
-    ge = {i: torch.cuda.Event(enable_timing=True) for i in timed}
-    sb = {i: torch.cuda.Event(enable_timing=True) for i in timed}   # whole-step events, same steps
-    se = {i: torch.cuda.Event(enable_timing=True) for i in timed}
+    # ---- headline timed region: events only at its two ends
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
     barrier()
     torch.cuda.synchronize(dev)
     t_start.record(stream)
-    for i in range(K):
-        if i in gb:
-            # torch only reports elapsed_time for events it recorded itself; record
-            # both here first, the library then re-records them around the GEMM
-            gb[i].record(stream)
-            ge[i].record(stream)
-            moe.set_gemm_events(gb[i], ge[i])
-            sb[i].record(stream)
-        step(x)
-        if i in gb:
-            se[i].record(stream)
-            moe.set_gemm_events(None, None)
+    for _ in range(K):
+        step(x, r)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clocks = sampler.stop()
-    moe.set_gemm_events(None, None)
     ms_total = max_over_ranks(t_start.elapsed_time(t_end))
-    gemm_samples = [gb[i].elapsed_time(ge[i]) for i in timed]
-    step_samples = [sb[i].elapsed_time(se[i]) for i in timed]
-    gemm_ms = statistics.mean(gemm_samples)
 
-    def pct(v):
-        q = sorted(v)
-        at = lambda f: q[min(len(q) - 1, int(round(f * (len(q) - 1))))]
-        return {"p10": at(0.1), "p50": at(0.5), "p90": at(0.9), "n": len(q)}
+    # ---- instrumented pass: events around every step and every grouped-GEMM launch
+    n_inst = max(K, 8)
+    gb = [torch.cuda.Event(enable_timing=True) for _ in range(n_inst)]
+    ge = [torch.cuda.Event(enable_timing=True) for _ in range(n_inst)]
+    sb = [torch.cuda.Event(enable_timing=True) for _ in range(n_inst)]
+    se = [torch.cuda.Event(enable_timing=True) for _ in range(n_inst)]
+    torch.cuda.synchronize(dev)
+    for i in range(n_inst):
+        # torch only reports elapsed_time for events it recorded itself; record
+        # both here first, the library then re-records them around the GEMM
+        gb[i].record(stream)
+        ge[i].record(stream)
+        moe.set_gemm_events(gb[i], ge[i])
+        sb[i].record(stream)
+        step(x, r)
+        se[i].record(stream)
+    moe.set_gemm_events(None, None)
+    torch.cuda.synchronize(dev)
+    gemm_samples = [gb[i].elapsed_time(ge[i]) for i in range(n_inst)]
+    step_samples = [sb[i].elapsed_time(se[i]) for i in range(n_inst)]
+    gemm_ms = statistics.mean(gemm_samples)
     status = moe.get_device_status(dev)
 
     # ---- end-to-end: pinned host input -> device -> layer -> pinned host output,
     # the copies of neighbouring steps overlapping the layer calls
-    has_r = cfg.mx or cfg.prenorm
-    host_in = [x.cpu().pin_memory()] + ([inp["r"].cpu().pin_memory()] if has_r else [])
+    has_r = r is not None
+    host_in = [x.cpu().pin_memory()] + ([r.cpu().pin_memory()] if has_r else [])
     e2e_ms = max_over_ranks(pipelined_e2e_ms(
         dev, stream, K, host_in,
         lambda d, b: step(d[0], d[1] if has_r else None, bi=b), bufsets[0]["out"], barrier))
 
     if rank != 0:
-        if ws > 1:
-            torch.distributed.destroy_process_group()
-        return 0
+        del layer, bufsets
+        torch.cuda.empty_cache()
+        return None
 
     hbm, bf16, peak_kind = measured_peaks()
     value = whole_job_tokens_per_s(cfg.T, K, ws, ms_total)
-    decode = cfg.T * cfg.k <= 16 * cfg.E
-    gbytes = algorithmic_gemm_bytes(cfg, active, routed_pairs)
-    if cfg.mx:
-        bf16 = bf16 * 2.0   # MXFP8 dense peak: measured bf16 x the nominal fp8/bf16 ratio (4.5/2.25)
-    if decode:
-        achieved = gbytes / (gemm_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                else "fallback 6.8 TB/s"}
-    else:
-        achieved = gemm_flops(cfg) / (gemm_ms / 1e3) / 1e12
-        # e2m1 x e4m3 runs in the same f8f6f4 MMA kind, at the fp8 rate
-        src = "bf16_tflops x 2 (nominal MXFP8/bf16 ratio)" if cfg.mx else "bf16_tflops"
-        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                "frac": achieved / bf16,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json {src})" if peak_kind == "measured"
-                else "fallback 1.9 PFLOP/s" + (" x 2" if cfg.mx else "")}
-    tr = profiled_traffic(cfg.name)
-    roof.update({"traffic": tr, "kernel": "grouped_gemm_kernel (both projections, one launch)",
-                 "kernel_ms": gemm_ms, "kernel_ms_pct": pct(gemm_samples), "algorithmic_bytes": gbytes,
-                 "active_experts": active})
-    if decode:
-        # the whole step against the same peak: every step streams at least the GEMM's bytes
-        roof["step_achieved"] = gbytes / (ms_total / K / 1e3) / 1e9
-        roof["step_frac"] = roof["step_achieved"] / hbm
-        # the library's router launch asks L2 for the front of w13 before the GEMM starts,
-        # so part of the GEMM's bytes are L2 hits
+    step_ms = ms_total / K
+    wbytes = gemm_weight_bytes(cfg, active)
+    lbytes = layer_algorithmic_bytes(cfg, active)
+    if is_decode(cfg):
         props = torch.cuda.get_device_properties(dev)
-        roof["l2_prefetched_bytes"] = l2_hint_bytes(cfg, props.multi_processor_count,
-                                                    getattr(props, "L2_cache_size", 0))
+        l2pf = l2_hint_bytes(cfg, props.multi_processor_count, getattr(props, "L2_cache_size", 0))
+        roof = hbm_roofline(wbytes, lbytes, l2pf, gemm_ms, step_ms, hbm)
+        roof["peak_source"] = (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                               else "fallback 6.8 TB/s")
+        roof["l2_prefetched_bytes"] = l2pf
+        roof["note"] = ("frac: the grouped GEMM's weight bytes net of those the router launch asked L2 "
+                        "for, over its mean launch time; step_frac: the layer's algorithmic bytes over "
+                        "the headline step time")
+    else:
+        peak = bf16 * 2.0 if cfg.mx else bf16   # e2m1/e4m3 run in kind::mxf8f6f4 at the fp8 rate
+        roof = tensor_roofline(gemm_flops(cfg), gemm_ms, step_ms, peak)
+        src = "bf16_tflops x 2 (nominal MXFP8/bf16 ratio)" if cfg.mx else "bf16_tflops"
+        roof["peak_source"] = (f"{peak_kind} (MEASURED_PEAKS.json {src})" if peak_kind == "measured"
+                               else "fallback 1.9 PFLOP/s" + (" x 2" if cfg.mx else ""))
+        roof["note"] = ("frac: the grouped GEMMs' 2*P*3*H*I FLOPs over the GEMM launch's mean time; "
+                        "step_frac: the same FLOPs over the headline step time")
+    roof.update({"traffic": profiled_traffic(cfg.name),
+                 "kernel": "grouped_gemm_mx_kernel" if cfg.mx else
+                           ("grouped_gemm_kernel" if is_decode(cfg) else "grouped_gemm_pair_kernel")
+                           + " (both projections, one launch)",
+                 "kernel_ms": gemm_ms, "kernel_ms_pct": percentiles(gemm_samples),
+                 "algorithmic_bytes": lbytes, "gemm_weight_bytes": wbytes,
+                 "implementation_bytes": gemm_implementation_bytes(cfg, routed_pairs),
+                 "active_experts": active})
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_total / K,
-        "step_ms_pct": {**pct(step_samples), "note": "single steps bracketed by events (every GEMM_EVERY-th timed step, at most every 32nd)"},
+        "warmup": args.warmup, "ms_per_step": step_ms,
+        "step_ms_pct": {**percentiles(step_samples),
+                        "note": "single steps bracketed by events, in a separate pass after the timed region"},
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": ("w4a8 (weights e2m1 + e8m0/32, activations e4m3 + e8m0/32)" if cfg.w4
                                        else "mxfp8 (e4m3 + e8m0/32)" if cfg.mx else "bf16"), "data": "synthetic",
@@ -547,15 +643,58 @@ def run_ours(args, cfg):
         "clocks": clocks,
         "device_status": status,
     }
+    del layer, bufsets
+    torch.cuda.empty_cache()
 
-    if not args.no_cpu_baseline:
+    if host_w is not None:
         from oracle import moe_oracle as O
-        arrays = oracle_arrays({k_: v.cpu() for k_, v in inp.items()})
-        v_cpu, ntok, dt = time_oracle(O, arrays, cfg, args.cpu_seconds)
+        arrays = oracle_arrays(host_w, cfg)
+        del host_w
+        v_cpu, calls, dt = time_oracle(O, arrays, cfg, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                                "sample": f"{ntok} tokens of the workload in batches of 4 over {dt:.1f} s, "
-                                          f"numpy fp64 oracle, weights pre-widened to fp64 in host memory"}
-    print(json.dumps(line), flush=True)
+                                "sample": oracle_sample_text(cfg, calls, dt)}
+    return line
+
+
+def summary(line: dict) -> dict:
+    """The compact per-workload record carried by the headline line."""
+    roof = line["roofline"]
+    return {"value": line["value"], "unit": line["unit"], "ms_per_step": line["ms_per_step"],
+            "bound": roof["bound"], "frac": roof["frac"], "step_frac": roof["step_frac"],
+            "kernel_ms": roof["kernel_ms"], "e2e": line["e2e"]["value"], "dtype": line["dtype"],
+            "clocks": line["clocks"], "device_status": line["device_status"]}
+
+
+def run_ours(args, names):
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from top_routing_grouped_gating_gb300 import build as B
+    B.build()
+    from top_routing_grouped_gating_gb300 import workloads as W
+
+    lines = {}
+    for name in names:
+        cfg = W.CONFIGS[name]
+        # the oracle baseline is timed for the printed workload only
+        line = measure(args, cfg, dev, cpu_baseline=(not args.no_cpu_baseline and name == names[-1]))
+        if line is not None:
+            lines[name] = line
+            if len(names) > 1:
+                print(json.dumps(line), file=sys.stderr, flush=True)
+    if rank == 0:
+        head = dict(lines[names[-1]])
+        if len(names) > 1:
+            head["workloads"] = {n: summary(l) for n, l in lines.items()}
+            head["gpu_launches_all_workloads"] = sum(l["gpu_launches"] for l in lines.values())
+        print(json.dumps(head), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
@@ -641,14 +780,16 @@ def run_ep_routing(args, cfg):
 def main(argv=None):
     args = parse_args(argv)
     from top_routing_grouped_gating_gb300 import workloads as W
-    if args.workload not in W.CONFIGS:
-        raise SystemExit(f"unknown workload {args.workload}; one of {sorted(W.CONFIGS)}")
-    cfg = W.CONFIGS[args.workload]
-    if cfg.ep_ranks:
-        return run_ep_routing(args, cfg)
+    names = list(SUITE) if args.workload == "all" else [args.workload]
+    for n in names:
+        if n not in W.CONFIGS:
+            raise SystemExit(f"unknown workload {n}; 'all' or one of {sorted(W.CONFIGS)}")
+    if len(names) == 1 and W.CONFIGS[names[0]].ep_ranks:
+        return run_ep_routing(args, W.CONFIGS[names[0]])
     if args.impl == "reference":
-        return run_reference(args, cfg)
-    return run_ours(args, cfg)
+        # the oracle on the printed (headline) workload
+        return run_reference(args, W.CONFIGS[names[-1]])
+    return run_ours(args, names)
 
 
 if __name__ == "__main__":

@@ -18,33 +18,87 @@ from top_routing_grouped_gating_gb300 import workloads as W  # noqa: E402
 MB = 1 << 20
 
 
-def test_algorithmic_bytes_30b_decode():
+def test_gemm_weight_and_implementation_bytes_30b_decode():
     cfg = W.CONFIGS["qwen3_30b_a3b_decode"]
     # 112 active experts x (w13 2048x1536 + down 768x2048) bf16 = 112 x 9,437,184 B
-    weights = 112 * 9_437_184
-    # P = 256 pairs: x rows 256x2048 bf16 in, h 256x768 out and in, y2 256x2048 out
-    acts = 1_048_576 + 2 * 393_216 + 1_048_576
-    assert bench.algorithmic_gemm_bytes(cfg, 112) == weights + acts == 1_059_848_192
+    assert bench.gemm_weight_bytes(cfg, 112) == 112 * 9_437_184 == 1_056_964_608
+    # P = 256 pairs: x rows 256x2048 bf16 in (1 MiB), h 256x768 out and in (2 x 384 KiB),
+    # y2 256x2048 out (1 MiB); reported apart, not credited
+    assert bench.gemm_implementation_bytes(cfg) == 1_048_576 + 2 * 393_216 + 1_048_576 == 2_883_584
 
 
-def test_algorithmic_bytes_mxfp8_and_w4a8():
+def test_layer_algorithmic_bytes_30b_decode():
+    cfg = W.CONFIGS["qwen3_30b_a3b_decode"]
+    # weights 1,056,964,608 + W_g 2048x128 fp32 (1 MiB) + x and out 32x2048 bf16 (128 KiB each)
+    # + top-k ids and weights 256 x (4 + 4) B
+    assert bench.layer_algorithmic_bytes(cfg, 112) == 1_056_964_608 + 1_048_576 + 2 * 131_072 + 2048
+
+
+def test_layer_algorithmic_bytes_mxfp8_prefill():
+    cfg = W.CONFIGS["mxfp8_prefill"]
+    # e4m3 codes + one E8M0 byte per 32: 3*4096*1536 = 18,874,368 elements per expert x 33/32
+    weights = 128 * 19_464_192
+    wg = 4096 * 128 * 4
+    # x and r in, out and residual_out written: four 4096x4096 bf16 tensors; norm weight 4096 bf16
+    acts = 4 * 33_554_432 + 8192
+    ids = 32768 * 8
+    assert bench.layer_algorithmic_bytes(cfg, 128) == weights + wg + acts + ids
+
+
+def test_gemm_bytes_mxfp8_and_w4a8():
     mx = W.CONFIGS["mxfp8_decode"]
-    # e4m3 codes + one E8M0 byte per 32: 3*4096*1536 elements per expert x 33/32
     per_expert = 3 * 4096 * 1536 * 33 // 32
+    assert bench.gemm_weight_bytes(mx, 100) == 100 * per_expert
     P = 64 * 8
-    acts = P * 4096 * 33 // 32 + 2 * P * 1536 * 33 // 32 + P * 4096 * 2
-    assert bench.algorithmic_gemm_bytes(mx, 100) == 100 * per_expert + acts
+    assert bench.gemm_implementation_bytes(mx) == P * 4096 * 33 // 32 + 2 * P * 1536 * 33 // 32 + P * 4096 * 2
     w4 = W.CONFIGS["w4a8_decode"]
     # e2m1: half a byte per code, plus the same scale bytes: 17/32 of a byte per element
-    assert bench.algorithmic_gemm_bytes(w4, 100) == 100 * (3 * 4096 * 1536 * 17 // 32) + acts
+    assert bench.gemm_weight_bytes(w4, 100) == 100 * (3 * 4096 * 1536 * 17 // 32)
 
 
-def test_algorithmic_bytes_count_only_routed_pairs():
+def test_implementation_bytes_count_only_routed_pairs():
     cfg = W.CONFIGS["zero_experts_decode"]
-    full = bench.algorithmic_gemm_bytes(cfg, 100)
-    fewer = bench.algorithmic_gemm_bytes(cfg, 100, pairs=200)
+    full = bench.gemm_implementation_bytes(cfg)
+    fewer = bench.gemm_implementation_bytes(cfg, pairs=200)
     # 56 pairs fewer, each H*2 in + 2*I*2 for h + H*2 out = 4096 + 3072 + 4096 bytes
     assert full - fewer == 56 * (4096 + 3072 + 4096)
+
+
+def test_hbm_roofline_nets_out_the_l2_hint():
+    # 1.0e9 weight bytes of which 0.2e9 were asked into L2 by the router launch, a 0.1 ms
+    # GEMM: 0.8e9 B / 1e-4 s = 8000 GB/s; 1.2e9 layer bytes in a 0.2 ms step: 6000 GB/s
+    r = bench.hbm_roofline(1_000_000_000, 1_200_000_000, 200_000_000, 0.1, 0.2, 8000.0)
+    assert r["achieved"] == pytest.approx(8000.0)
+    assert r["frac"] == pytest.approx(1.0)
+    assert r["step_achieved"] == pytest.approx(6000.0)
+    assert r["step_frac"] == pytest.approx(0.75)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+
+
+def test_tensor_roofline():
+    # 2.0e12 FLOP in a 1 ms GEMM inside a 1.25 ms step against a 2500 TFLOP/s peak
+    r = bench.tensor_roofline(2.0e12, 1.0, 1.25, 2500.0)
+    assert r["achieved"] == pytest.approx(2000.0)
+    assert r["frac"] == pytest.approx(0.8)
+    assert r["step_frac"] == pytest.approx(0.64)
+
+
+def test_oracle_sample_is_the_same_in_both_arms():
+    # decode: the whole batch per oracle call; prefill: 64 consecutive tokens, wrapping
+    assert bench.oracle_sample_tokens(W.CONFIGS["qwen3_30b_a3b_decode"]) == 32
+    assert bench.oracle_sample_tokens(W.CONFIGS["qwen3_235b_a22b_decode"]) == 64
+    pre = W.CONFIGS["qwen3_235b_a22b_prefill"]
+    assert bench.oracle_sample_tokens(pre) == 64
+    assert bench.oracle_sample_rows(pre, 0) == list(range(64))
+    assert bench.oracle_sample_rows(pre, 1) == list(range(64, 128))
+    assert bench.oracle_sample_rows(pre, 128) == list(range(64))          # 128 x 64 = 8192 wraps to 0
+    assert bench.oracle_sample_rows(W.CONFIGS["qwen3_30b_a3b_decode"], 3) == list(range(32))
+
+
+def test_suite_ends_with_the_largest_workload():
+    sizes = [W.CONFIGS[n].T * W.CONFIGS[n].H * W.CONFIGS[n].I for n in bench.SUITE]
+    assert bench.HEADLINE == "qwen3_235b_a22b_prefill" == bench.SUITE[-1]
+    assert sizes[-1] == max(sizes)
 
 
 def test_gemm_flops():
