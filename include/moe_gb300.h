@@ -27,8 +27,12 @@
  *    Matrix pointers must be 16-byte aligned.
  *  - Shapes: 1 <= T; H % 128 == 0; I % 64 == 0; 1 <= E <= 256; 1 <= k <= min(E, 32);
  *    T*k < 2^31.  Other shapes return MOE_ERR_UNSUPPORTED_SHAPE.
- *  - The library runs only on compute capability 10.3 (GB300, sm_103a); other
- *    devices return MOE_ERR_UNSUPPORTED_ARCH.
+ *  - The library runs only on compute capability 10.3 (GB300, sm_103a) and on
+ *    device indices 0..63; other devices return MOE_ERR_UNSUPPORTED_ARCH.
+ *  - Per-device facts (SM count, the status word's address, kernel attributes)
+ *    are looked up on the first call on each device and kept.  They belong to the
+ *    device's primary context: the library assumes that context is not destroyed
+ *    (cudaDeviceReset) while it stays loaded.
  *  - Token-expert pairs are numbered token-major: pair j = t*k + s is slot s of
  *    token t.  P = T*k.
  */
@@ -55,7 +59,7 @@ typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,       /* null / misaligned pointer, negative size */
   MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set above */
-  MOE_ERR_UNSUPPORTED_ARCH = 3,  /* current device is not sm_103 */
+  MOE_ERR_UNSUPPORTED_ARCH = 3,  /* current device is not sm_103, or its index is >= 64 */
   MOE_ERR_WORKSPACE = 4,         /* ws too small or misaligned */
   MOE_ERR_CUDA = 5               /* a CUDA runtime call or launch failed */
 } moe_status;
@@ -409,6 +413,21 @@ MOE_API moe_status moe_init_routing_noalloc(const moe_bf16* x, const int32_t* to
  * owned by the caller; pass NULL, NULL to stop.
  */
 MOE_API moe_status moe_set_gemm_events(void* ev_begin, void* ev_end);
+
+/* ------------------------------------------------------------- test hook --
+ * Test aid, not part of the page's operator set: makes the bounded device waits of
+ * the one-CTA grouped GEMM (the decode-size tiles) run out on purpose, so that the
+ * timeout path can be checked without a fault.  With stage >= 0, every later launch
+ * of that kernel (from any host thread) bounds each of its waits by `wait_ns`
+ * (1 us .. 2 s, else MOE_ERR_INVALID_ARG), and in every CTA the TMA producer stops
+ * before its stage-th pipeline stage: it issues no copy for that stage or any later
+ * one.  The MMA thread's wait for that stage then runs out, the CTA's roles unwind
+ * (MMAs and copies already issued complete first, TMEM is freed), the launch
+ * returns, and MOE_DEV_WAIT_TIMEOUT is set in the status word; the layer's outputs
+ * of that call are invalid.  stage < 0 switches the hook off and restores the
+ * library-wide limit (2 s).  The CTA-pair and block-scaled GEMMs ignore it.
+ */
+MOE_API moe_status moe_debug_set_gemm_stall(int stage, long long wait_ns);
 
 #ifdef __cplusplus
 }

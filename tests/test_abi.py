@@ -103,3 +103,10 @@ def test_out_of_range_shapes_rejected_before_device_use(L):
     assert L.moe_grouped_matmul_mx_workspace_size(300, 16, 256, 128, 1) == 0  # E > 256
     assert L.moe_grouped_matmul_mx_workspace_size(8, 16, 200, 128, 0) == 0    # K % 128 != 0
     assert L.moe_packed_weight_bytes_mx4(8, 256, 128, 0) == 8 * 256 * 128     # 2I x H codes / 2
+
+
+def test_gemm_stall_hook_validates_on_the_host(L):
+    # host-only: sets or clears the hook state, touches no device
+    assert L.moe_debug_set_gemm_stall(3, 10) == 1               # wait limit below 1 us
+    assert L.moe_debug_set_gemm_stall(3, 3_000_000_000) == 1    # above the 2 s library limit
+    assert L.moe_debug_set_gemm_stall(-1, 0) == 0               # off

@@ -40,5 +40,6 @@ from ._binding import (  # noqa: F401
     pack_weights,
     router_logits,
     set_gemm_events,
+    debug_set_gemm_stall,
 )
 from .workloads import CONFIGS, MoEConfig, make_inputs  # noqa: F401

@@ -43,6 +43,7 @@ _SIGS = {
     "moe_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
                              _vp, _vp, _c_size, _vp]),
     "moe_set_gemm_events": (_c_int, [_vp, _vp]),
+    "moe_debug_set_gemm_stall": (_c_int, [_c_int, ctypes.c_longlong]),
     "moe_add_rmsnorm_cast": (_c_int, [_vp, _vp, _vp, _c_float, _c_int, _c_int, _vp, _vp, _vp, _vp]),
     "moe_init_routing_v2_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
     "moe_init_routing_v2": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp,
@@ -314,6 +315,14 @@ def set_gemm_events(ev_begin: Optional[torch.cuda.Event], ev_end: Optional[torch
     b = None if ev_begin is None else ev_begin.cuda_event
     e = None if ev_end is None else ev_end.cuda_event
     _check("moe_set_gemm_events", lib().moe_set_gemm_events(b, e))
+
+
+def debug_set_gemm_stall(stage: int, wait_ns: int = 2_000_000) -> None:
+    """Test hook: later launches of the decode-size grouped GEMM stop feeding their
+    pipeline at ``stage`` and bound every device wait by ``wait_ns``, so the timeout
+    path runs (the call's outputs are invalid; the status word gets the timeout
+    bit).  ``stage < 0`` switches it off."""
+    _check("moe_debug_set_gemm_stall", lib().moe_debug_set_gemm_stall(int(stage), int(wait_ns)))
 
 
 def get_device_status(device=None) -> int:

@@ -51,7 +51,8 @@ size_t decode_l2_hint_bytes(const DeviceFacts& d, size_t w13_bytes, size_t row_b
 
 moe_status current_device(DeviceFacts** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED_ARCH;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceFacts& d = g_dev[dev];
   if (!d.probed) {
@@ -217,7 +218,8 @@ const char* moe_status_string(int status) {
     case MOE_OK: return "ok";
     case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size)";
     case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
-    case MOE_ERR_UNSUPPORTED_ARCH: return "unsupported device: compute capability 10.3 required";
+    case MOE_ERR_UNSUPPORTED_ARCH:
+      return "unsupported device: compute capability 10.3 and a device index below 64 required";
     case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
     case MOE_ERR_CUDA: return "CUDA runtime error";
     default: return "unknown status";
@@ -1094,6 +1096,12 @@ moe_status moe_forward_v2(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
   MOE_CUDA(moe::launch_grouped_gemm(&g1, &g2, offsets, E, P, T, done, d->status, stream));
   if (t_gemm_ev_end) MOE_CUDA(cudaEventRecord(t_gemm_ev_end, stream));
   MOE_CUDA(moe::launch_finalize_v2(y2, w, eri, ids, expert_in, T, k, H, E, Eg, out, stream));
+  return MOE_OK;
+}
+
+moe_status moe_debug_set_gemm_stall(int stage, long long wait_ns) {
+  if (stage >= 0 && (wait_ns < 1000 || wait_ns > 2000000000LL)) return MOE_ERR_INVALID_ARG;
+  moe::set_gemm_stall(stage, static_cast<unsigned long long>(wait_ns));
   return MOE_OK;
 }
 

@@ -73,8 +73,9 @@ MOE_DEVINL bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// if the time limit passed or *abort became non-zero (another role gave up).
-MOE_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+// if the time limit (limit_ns) passed or *abort became non-zero (another role gave up).
+MOE_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                          unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
@@ -82,7 +83,7 @@ MOE_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* ab
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 63u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
   }
 }

@@ -66,6 +66,12 @@ struct GemmArgs {
   float* out_f32[2];
   int* done;        // per-expert count of finished phase-0 units, or null
   int* status;
+  // Test hook of the one-CTA kernel (moe_debug_set_gemm_stall): a producer that
+  // reaches its stall_stage-th stage issues nothing more and waits for another role
+  // to give up; every wait of the launch is bounded by wait_ns.  stall_stage < 0:
+  // off (the normal case); wait_ns is then the library-wide limit.
+  int stall_stage;
+  unsigned long long wait_ns;
 };
 
 template <int BN, int STAGES, int BOX>
@@ -143,7 +149,8 @@ __device__ __forceinline__ Unit unpack_unit(uint2 w) {
   return t;
 }
 
-__device__ __forceinline__ bool wait_counter(const int* p, int need, const volatile int* abort) {
+__device__ __forceinline__ bool wait_counter(const int* p, int need, const volatile int* abort,
+                                             unsigned long long limit_ns = kWaitLimitNs) {
   if (ld_acquire_gpu(p) >= need) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
@@ -151,7 +158,7 @@ __device__ __forceinline__ bool wait_counter(const int* p, int need, const volat
     if (ld_acquire_gpu(p) >= need) return true;
     if ((i & 15u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
   }
 }
@@ -347,16 +354,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // of its expert, so keep them cacheable
       const uint64_t pol_w = BN <= 32 ? l2_policy_evict_first() : l2_policy_evict_normal();
       const uint64_t pol_x = l2_policy_evict_last();
+      const unsigned long long wait_ns = args.wait_ns;
       int stage = 0;
       uint32_t par = 0;
       uint32_t issued_mask = 0, issued_par = 0;
-      bool ok = true;
-      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      int nissued = 0;
+      bool ok = true, stalled = false;
+      for (int u = blockIdx.x, ui = 0; u < total && ok && !stalled; u += gridDim.x, ++ui) {
         const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<BN>(u, tb);
         if (t.ph == 1 && args.done != nullptr) {
           const int m = s_off[t.e + 1] - s_off[t.e];
           const int need = ((m + BN - 1) / BN) * (args.MW[0] / kBM) * args.ksplit[0];
-          if (!wait_counter(args.done + t.e, need, s_abort)) {
+          if (!wait_counter(args.done + t.e, need, s_abort, wait_ns)) {
             ok = false;
             break;
           }
@@ -371,7 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bseg = args.bseg[t.ph];
         const uint32_t bmap = args.bmap[t.ph];
         for (int kb = t.ks * nks; kb < (t.ks + 1) * nks; ++kb) {
-          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+          if (nissued == args.stall_stage) {
+            // test hook: nothing is issued for this stage or after it; the MMA
+            // thread's wait for it runs out (nothing of this CTA is in flight then)
+            stalled = true;
+            break;
+          }
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort, wait_ns)) {
             ok = false;
             break;
           }
@@ -388,17 +403,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         t.row0 + j * BOX, pol_x);
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (par << stage);
+          ++nissued;
           if (++stage == STAGES) {
             stage = 0;
             par ^= 1u;
           }
         }
       }
+      if (stalled) {
+        // wait (bounded) for the role whose wait ran out to raise the abort flag
+        const unsigned long long t0 = globaltimer();
+        while (!*s_abort && globaltimer() - t0 < 4 * wait_ns) __nanosleep(256);
+        ok = false;
+      }
       if (ok) {
         // producer tail: wait until the MMA unit has released every stage, so no
         // commit-arrive is still in flight when the CTA exits
         for (int i = 0; i < STAGES; ++i) {
-          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort, wait_ns)) {
             ok = false;
             break;
           }
@@ -419,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // -------------------------------------------------------- MMA issuer --
+      const unsigned long long wait_ns = args.wait_ns;
       int stage = 0, acc = 0;
       uint32_t par = 0, apar = 0;
       bool ok = true;
@@ -426,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<BN>(u, tb);
         const int n = (t.rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(kBM, n);
-        if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort)) {
+        if (!mbar_wait(&tempty[acc], apar ^ 1u, s_abort, wait_ns)) {
           ok = false;
           break;
         }
@@ -434,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
         const int nk = args.K[t.ph] / kBK / args.ksplit[t.ph];
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&full[stage], par, s_abort)) {
+          if (!mbar_wait(&full[stage], par, s_abort, wait_ns)) {
             ok = false;
             break;
           }
@@ -472,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t apar = 0;
     for (int u = blockIdx.x, ui = 0; u < total; u += gridDim.x, ++ui) {
       const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<BN>(u, tb);
-      if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort) ? 1 : 0;
+      if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort, args.wait_ns) ? 1 : 0;
       named_bar_sync(1, 128);
       const int ok = s_flag[0];
       named_bar_sync(1, 128);
@@ -899,6 +922,10 @@ __global__ void pack_down_kernel(const uint16_t* __restrict__ down, int H, int I
     out[((size_t)e * H + n0 + i) * I + i0 + tx] = tile[tx][i];
 }
 
+// Test hook state (moe_debug_set_gemm_stall); read at each one-CTA launch.
+std::atomic<int> g_stall_stage{-1};
+std::atomic<unsigned long long> g_stall_wait_ns{kWaitLimitNs};
+
 template <int BN, int STAGES, int BOX>
 cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_t* offsets, int E,
                         int P, int* done, int* status, cudaStream_t s) {
@@ -923,6 +950,8 @@ cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_
   a.E = E;
   a.done = (ph0 && ph1) ? done : nullptr;
   a.status = status;
+  a.stall_stage = g_stall_stage.load();
+  a.wait_ns = a.stall_stage >= 0 ? g_stall_wait_ns.load() : kWaitLimitNs;
   CUtensorMap tm[4];
   const GemmPhase* phs[2] = {ph0, ph1};
   for (int p = 0; p < 2; ++p) {
@@ -984,6 +1013,8 @@ cudaError_t launch_pair_impl(const GemmPhase* ph0, const GemmPhase* ph1, const i
   a.E = E;
   a.done = (ph0 && ph1) ? done : nullptr;
   a.status = status;
+  a.stall_stage = -1;
+  a.wait_ns = kWaitLimitNs;
   CUtensorMap tm[6];
   const GemmPhase* phs[2] = {ph0, ph1};
   for (int p = 0; p < 2; ++p) {
@@ -1027,6 +1058,11 @@ bool pairable(const GemmPhase* g) {
 }
 
 }  // namespace
+
+void set_gemm_stall(int stage, unsigned long long wait_ns) {
+  g_stall_wait_ns.store(stage >= 0 ? wait_ns : kWaitLimitNs);
+  g_stall_stage.store(stage >= 0 ? stage : -1);
+}
 
 cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
                                 const int32_t* offsets, int E, int P, int max_rows_hint,

@@ -109,6 +109,8 @@ struct GemmPhase {
 cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
                                 const int32_t* offsets, int E, int P, int max_rows_hint,
                                 int* done_counter, int* status, cudaStream_t s);
+// Test hook of the one-CTA grouped GEMM (moe_debug_set_gemm_stall); stage < 0: off.
+void set_gemm_stall(int stage, unsigned long long wait_ns);
 cudaError_t launch_pack_w13(const uint16_t* w13, int E, int H, int I, uint16_t* out,
                             cudaStream_t s);
 cudaError_t launch_pack_down(const uint16_t* down, int E, int H, int I, uint16_t* out,

@@ -10,7 +10,10 @@
 // Set-up: the first call on each device (with that device current) looks up the
 // array's device address with cudaGetSymbolAddress and caches it; in host code
 // the array's name is only a host-side stand-in and must never be passed to a
-// kernel.  Make that first call before any stream capture on the device.
+// kernel.  Make that first call before any stream capture on the device.  The
+// cached address belongs to the device's primary context: like the library's other
+// per-device state, it assumes that context is not destroyed (cudaDeviceReset)
+// while the library stays loaded.  Device indices 0..63 are supported.
 //
 // Sharing: every call on a device uses the same array, which keeps whatever the
 // last call left in it.  Calls that can overlap on the GPU (different streams
@@ -39,7 +42,8 @@ int32_t* g_scratch_addr[64] = {};
 // Device address of g_routing_scratch on the current device (looked up once).
 moe_status scratch_address(int32_t** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED_ARCH;
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
