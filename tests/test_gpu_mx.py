@@ -78,8 +78,10 @@ def _unpack_w13(q, sf, E, H, I):
     q = q.reshape(E, 2 * I, H)
     sf = sf.reshape(E, 2 * I // 128, H // 128, 512)
     r = np.arange(2 * I)
-    blk, wi = r // 128, r % 128
-    col = np.where(wi < 64, blk * 64 + wi, I + blk * 64 + (wi - 64))
+    # packed row 32q + i of 128-row block b: gate feature 64b + 16q + i (i < 16), else
+    # the up feature 64b + 16q + i - 16 (logical column I + that feature)
+    blk, quarter, i = r // 128, (r % 128) // 32, r % 32
+    col = blk * 64 + quarter * 16 + i % 16 + np.where(i < 16, 0, I)
     codes = np.empty((E, H, 2 * I), np.uint8)
     scales = np.empty((E, H // 32, 2 * I), np.uint8)
     b = np.arange(H // 32)
@@ -153,10 +155,15 @@ def test_forward_mx_small(cuda_dev, T, E, k, H, I):
     _check_mx_forward(cfg, inp, layer)
 
 
-def test_forward_mx_token_block_boundaries(cuda_dev):
-    """Expert loads on both sides of the block-scaled GEMM's token blocks (128 rows, a
-    last block absorbing up to 32 more), forced through designed logits."""
-    counts = [128, 160, 161, 288, 289, 1, 0, 1021]
+@pytest.mark.parametrize("counts", [
+    [128, 160, 161, 288, 289, 1, 0, 1021],   # one-CTA blocks: 128 rows, the last absorbing 32
+    [256, 257, 272, 288, 289, 544, 545, 17],  # CTA-pair units: 256 rows, the last absorbing 32
+])
+def test_forward_mx_token_block_boundaries(cuda_dev, counts):
+    """Expert loads on both sides of the block-scaled GEMM's token blocks, forced
+    through designed logits: the CTA-pair kernel's 256-row units (an expert's last
+    unit takes up to 32 more rows through a second MMA of N = 32), and the 128-row
+    blocks of the one-CTA layout."""
     k = 2
     cfg = W.with_shape(W.CONFIGS["mxfp8_prefill"], T=sum(counts) // k, E=len(counts), k=k, H=256,
                        I=128)

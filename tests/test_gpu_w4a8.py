@@ -121,6 +121,30 @@ def test_forward_w4a8_small(cuda_dev, T, E, k, H, I):
     _check_w4_forward(cfg, inp, layer)
 
 
+def test_forward_w4a8_token_block_boundaries(cuda_dev):
+    """MXFP4 weights through the CTA-pair kernel with expert loads on both sides of its
+    256-row units and of the 32 absorbed rows, forced through designed logits."""
+    from tests._helpers import forced_topk_logits
+    counts = [256, 257, 288, 289, 31, 0, 545, 130]
+    k = 2
+    cfg = W.with_shape(W.CONFIGS["w4a8_prefill"], T=sum(counts) // k, E=len(counts), k=k, H=256, I=128)
+    inp, layer = _w4_layer(cfg)
+    lg = forced_topk_logits(counts, k, seed=13)
+    x, r = inp["x"], inp["r"]
+    out, res, ids, w = layer(x, r, logits_override=torch.from_numpy(lg).to(x.device))
+    torch.cuda.synchronize()
+    assert moe.get_device_status() == 0
+    r_ids, _ = O.gating_topk_softmax(lg, k)
+    np.testing.assert_array_equal(np.bincount(r_ids.ravel(), minlength=cfg.E), counts)
+    np.testing.assert_array_equal(to_np(ids), r_ids)
+    ref = O.moe_forward_w4a8(to_np(x), to_np(r), to_np(inp["norm_w"]), cfg.eps, None,
+                             LazyExperts(inp["w13"]), LazyExperts(inp["down"]), k, logits32=lg)
+    got = to_np(out)
+    assert np.all(np.isfinite(got))
+    rf = rel_fro(got, ref["out"])
+    assert rf <= REL_FRO_MX, f"relative Frobenius error {rf:.3e}"
+
+
 def test_forward_w4a8_decode_tiles_skewed(cuda_dev):
     """Narrow-tile shape with a Zipf-skewed router: one expert spans several 32-token
     tiles, so all four 32-row groups of the activation scale atoms are used."""

@@ -24,6 +24,7 @@
 //    atoms that the down projection then reads.
 #include <cuda_fp8.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -43,7 +44,10 @@ constexpr int kMaxE = 256;
 constexpr int kMaxUnits = 512;
 constexpr int kABytes = kBM * kBK;                // 16 KB
 constexpr int kSfBytes = 512;                     // one scale atom
-constexpr int kEpiBytes = (4 * 16 * 33 + 2 * 32 * 33) * 4;  // SwiGLU exchange + h tile
+// epilogue shared memory: four 32 x 32 bf16 transpose tiles (down projection), which
+// also hold the two warp pairs' block-maximum swap areas of the gate/up projection
+constexpr int kEpiBytes = 4 * 32 * 32 * 2;
+static_assert(kEpiBytes >= 2 * 128 * 4, "block-maximum swap areas");
 
 // Tile shape: kBN tokens per unit, kStages pipeline stages, B boxes of kBoxRows rows.
 // With kAbsorb > 0 an expert's last token block takes up to kAbsorb rows beyond kBN
@@ -217,6 +221,66 @@ __device__ __forceinline__ uint8_t mx_code(float v, int X) {
   const float f = v * __uint_as_float(static_cast<uint32_t>(a + 127) << 23) *
                   __uint_as_float(static_cast<uint32_t>(nx - a + 127) << 23);
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3));
+}
+
+// One 32-token chunk of a gate/up accumulator: SwiGLU, then MX quantisation of h
+// along I into the down projection's activation layout.  The warp reads TMEM lane
+// quarter q of the CTA's 128-row weight block mb (whose features are mb * 64 ..
+// mb * 64 + 63): lanes 0-15 hold the gate rows of features 16q .. 16q + 15 of the
+// block and lanes 16-31 their up rows, v[j] being token c0 + j.  One shuffle pairs
+// gate and up, so lanes 0-15 finish tokens c0 .. c0 + 15 and lanes 16-31 tokens
+// c0 + 16 .. c0 + 31, each for feature 16q + (lane & 15).  An MX block (32 features)
+// spans quarters q and q ^ 1: each half-warp takes its 16 per-token maxima over its
+// 16 lanes by a butterfly (16 values halved over lane offsets 8, 4, 2, 1, after which
+// lane t holds token c0 + t's maximum), the two warps swap them through xs (a
+// [2 slots][2 warps][32] float area of the warp pair, the slot alternating with the
+// pair's chunk count) after a named barrier of the pair, and every lane then writes
+// its code byte of each of its 16 token rows; the even warp of the pair writes the
+// scale bytes.
+template <int kPad>
+__device__ __forceinline__ void swiglu_mx_chunk(const MxArgs& args, const float (&v)[32], int row0,
+                                                int c0, int rows, int mb, int q, int lane,
+                                                float* xs, int slot, uint32_t bar_id) {
+  const bool lo = lane < 16;
+  float h[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float send = lo ? v[16 + j] : v[j];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+    const float g = lo ? v[j] : recv;
+    const float up = lo ? recv : v[16 + j];
+    h[j] = g / (1.0f + __expf(-g)) * up;
+  }
+  float m[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m[j] = fabsf(h[j]);
+#pragma unroll
+  for (int o = 8, n = 16; o >= 1; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float send = upper ? m[k] : m[k + n / 2];
+      const float keep = upper ? m[k + n / 2] : m[k];
+      m[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+  xs[(slot * 2 + (q & 1)) * 32 + lane] = m[0];
+  named_bar_sync(bar_id, 64);
+  const int Xmine = mx_exponent(fmaxf(m[0], xs[(slot * 2 + ((q & 1) ^ 1)) * 32 + lane]));
+  const int ld = args.ld[0];
+  if ((q & 1) == 0 && c0 + lane < rows) {
+    const int prow = row0 + c0 + lane;
+    const int kbq = (mb & 1) * 2 + (q >> 1);   // 32-feature block within the 128-feature step
+    uint8_t* atom = args.h_sf + ((size_t)(prow / kPad) * (ld / 128) + mb / 2) * kSfBytes;
+    atom[(prow & 31) * 16 + ((prow % kPad) >> 5) * 4 + kbq] = static_cast<uint8_t>(Xmine + 127);
+  }
+  uint8_t* hcol = args.hq + mb * 64 + 16 * q + (lane & 15);
+  const int tb0 = c0 + (lo ? 0 : 16);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int X = __shfl_sync(0xffffffffu, Xmine, (lane & 16) + j);
+    if (tb0 + j < rows) hcol[(size_t)(row0 + tb0 + j) * ld] = mx_code(h[j], X);
+  }
 }
 
 template <class S>
@@ -543,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int et = tid - 128;
     int* s_flag = s_tmp;
-    int acc = 0;
+    int acc = 0, nchunk = 0;
     uint32_t apar = 0;
     for (int u = blockIdx.x, ui = 0; u < total; u += gridDim.x, ++ui) {
       const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kBN, kAbsorb>(u, tb);
@@ -562,65 +626,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * kAccStride);
       if (t.ph == 0) {
-        // SwiGLU, then MX quantisation of h along I.  Warps q and q+2 hold the gate
-        // and up rows of the same 32 features (one scale block, p = q & 1).  The pair
-        // swaps half a chunk through shared memory, so the gate warp finishes tokens
-        // 0-15 and the up warp tokens 16-31; h goes to a padded [token][feature]
-        // tile, and two lanes per token then quantise 16 features each (block
-        // maximum by one shuffle).
-        float* xb = reinterpret_cast<float*>(sEpi);          // [4 warps][16 tok][33]
-        float* hb = xb + 4 * 16 * 33;                        // [2 blocks][32 tok][33]
-        const int ld = args.ld[0];
-        const int ksteps = ld / 128;
-        const int ks = t.mb / 2;                 // 128-feature step of the down projection
-        const int pblk = q & 1;                  // feature block of this warp pair
-        const int kbq = (t.mb & 1) * 2 + pblk;   // its 32-feature block within step ks
-        const bool gate = q < 2;
-        const uint32_t bar_id = 2 + pblk;
-        float* mine = xb + q * 16 * 33;
-        const float* other = xb + (q ^ 2) * 16 * 33;
-        float* hrow = hb + pblk * 32 * 33;
+        // SwiGLU and MX quantisation of h, a 32-token chunk at a time; warps q and q ^ 1
+        // (the two halves of one 32-feature MX block) swap block maxima through xs
+        float* xs = reinterpret_cast<float*>(sEpi) + (q >> 1) * 128;
         for (int c0 = 0; c0 < t.rows; c0 += 32) {
           float v[32];
           tmem_ld_32x32b_x32(tbase + c0, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) mine[j * 33 + lane] = gate ? v[16 + j] : v[j];
-          named_bar_sync(bar_id, 64);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float g = gate ? v[j] : other[j * 33 + lane];
-            const float up = gate ? other[j * 33 + lane] : v[16 + j];
-            hrow[((gate ? 0 : 16) + j) * 33 + lane] = g / (1.0f + __expf(-g)) * up;
-          }
-          named_bar_sync(bar_id, 64);
-          const int tok = (gate ? 0 : 16) + (lane >> 1);
-          const int half = lane & 1;
-          float hv[16];
-          float amax = 0.f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            hv[i] = hrow[tok * 33 + 16 * half + i];
-            amax = fmaxf(amax, fabsf(hv[i]));
-          }
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-          const int X = mx_exponent(amax);
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            w[i] = static_cast<uint32_t>(mx_code(hv[4 * i], X)) |
-                   (static_cast<uint32_t>(mx_code(hv[4 * i + 1], X)) << 8) |
-                   (static_cast<uint32_t>(mx_code(hv[4 * i + 2], X)) << 16) |
-                   (static_cast<uint32_t>(mx_code(hv[4 * i + 3], X)) << 24);
-          if (c0 + tok < t.rows) {
-            const int prow = t.row0 + c0 + tok;
-            *reinterpret_cast<uint4*>(args.hq + (size_t)prow * ld + t.mb * 64 + 32 * pblk +
-                                      16 * half) = make_uint4(w[0], w[1], w[2], w[3]);
-            if (half == 0) {
-              uint8_t* atom = args.h_sf + ((size_t)(prow / kPad) * ksteps + ks) * kSfBytes;
-              atom[(prow & 31) * 16 + ((prow % kPad) >> 5) * 4 + kbq] = static_cast<uint8_t>(X + 127);
-            }
-          }
-          named_bar_sync(bar_id, 64);
+          swiglu_mx_chunk<kPad>(args, v, t.row0, c0, t.rows, t.mb, q, lane, xs, nchunk & 1,
+                                2 + (q >> 1));
+          ++nchunk;
         }
       } else {
         uint16_t* tbw = reinterpret_cast<uint16_t*>(sEpi) + q * 32 * 32;
@@ -663,6 +677,531 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------- CTA pairs --
+// Prefill on pairs of SMs (clusters of two CTAs) with 256-token units.  One
+// tcgen05.mma.cta_group::2 of M = 256 covers both CTAs' 128-row weight blocks (CTA r
+// holds block 2 * pb + r of A) and up to 256 tokens, of which CTA r holds rows
+// [r * N/2, (r + 1) * N/2) of B; each CTA's TMEM receives the 128 x N fp32 accumulator
+// of its own weight block.  Per SM an instruction then does 128 x 256 x 32, twice the
+// one-CTA kernel's 128 x 128 x 32, for the same issue work and for half the shared-
+// memory operand traffic per FLOP (the bounds of the one-CTA kernel).  An expert's last
+// unit absorbs up to 32 rows beyond 256 through a second MMA of N = 32 per K step
+// (each CTA holding 16 of those rows), writing accumulator columns 256..287, so that
+// experts of 257..288 rows need no second, nearly empty unit.
+//
+// TMEM: one accumulator of 288 columns and five 16-column scale slots (SFA, then the
+// B scale atoms of rows 0-127, 128-255 and the absorbed rows) do not leave room for a
+// second accumulator, so the MMAs of a unit wait until both CTAs' epilogues have read
+// the previous one.  Eight epilogue warps (two per TMEM lane quarter, each taking
+// every other 32-token chunk) keep that drain short.
+//
+// Roles (384 threads): warp 0 lane 0 loads the weight tile and its scale atom, warp 2
+// lane 0 the token rows (this CTA's half) and the token block's B scale atoms (in both
+// CTAs); in the even CTA warp 3 lane 0 copies each stage's scale atoms into both
+// CTAs' TMEM (tcgen05.cp.cta_group::2, each CTA from its own shared memory) and warp 1
+// lane 0 issues the MMAs; in the odd CTA warp 3 lane 0 passes each landed stage on to
+// the even CTA's `full` barrier (a relaxed remote arrive).  Stage release and
+// accumulator completion are committed to both CTAs (multicast); the accumulator's
+// `tempty` barrier lives in the even CTA and counts the epilogue warps of both.
+struct PairMx {
+  static constexpr int kBN = 256;                  // tokens of a unit's main MMA
+  static constexpr int kTail = 32;                 // rows the last unit of an expert absorbs
+  static constexpr int kMaxRows = kBN + kTail;
+  static constexpr int kPad = 128;                 // row padding of the expert blocks
+  static constexpr int kStages = 5;
+  static constexpr int kEpiGroups = 3;             // epilogue warps per TMEM lane quarter
+  static constexpr int kEpiWarps = 4 * kEpiGroups;
+  static constexpr int kThreads = 32 * (4 + kEpiWarps);
+  static constexpr int kChunks = (kMaxRows / 32 + kEpiGroups - 1) / kEpiGroups;  // per warp
+  static constexpr int kBBytes = (kBN / 2) * kBK;  // this CTA's half of the main token block
+  static constexpr int kTBytes = (kTail / 2) * kBK;// this CTA's half of the absorbed rows
+  static constexpr int kSfAtoms = 4;               // SFA, SFB rows 0-127, 128-255, absorbed
+  static constexpr int kSfStageCols = 4 * kSfAtoms;
+  static constexpr int kSfCol = kMaxRows;          // scale slots follow the accumulator
+  static constexpr int kTmemCols = 512;
+  static constexpr int kEpiGroupBytes = 2 * 128 * 4;          // block-maximum swaps, phase 0
+  static constexpr int kTileBytes = 32 * 32 * 2;              // bf16 transpose, phase 1
+  static constexpr int kEpiBytes = kEpiGroups * kEpiGroupBytes > kEpiWarps * kTileBytes
+                                       ? kEpiGroups * kEpiGroupBytes
+                                       : kEpiWarps * kTileBytes;
+  static constexpr int kMaxUnits = 256;
+  // registers: 65536 / 512 at launch; the epilogue warpgroups hold kChunks x 32 values
+  static constexpr int kLaunchRegs = 128;
+  static constexpr int kRoleRegs = 56, kEpiRegs = 152;
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + kStages * kABytes;
+  static constexpr int kT = kB + kStages * kBBytes;
+  static constexpr int kSf = kT + kStages * kTBytes;
+  static constexpr int kEpi = kSf + kStages * kSfAtoms * kSfBytes;
+  static constexpr int kBar = kEpi + kEpiBytes;
+  static constexpr int kNumBars = 3 * kStages + 4;  // full, empty, sfready; tfull, tempty, fin, fin_sf
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kTables = kMisc + 16;
+  static constexpr int kUnits = kTables + (4 * (kMaxE + 1) + 16) * 4;  // scan scratch: 16 warps
+  static constexpr int kEnd = kUnits + kMaxUnits * 8;
+  static constexpr int kSmemBytes = kEnd + 1024;
+  static_assert(kBar % 8 == 0 && kUnits % 8 == 0, "barrier and unit list alignment");
+  static_assert(kB % 1024 == 0 && kT % 1024 == 0 && kBBytes % 1024 == 0 && kTBytes % 1024 == 0,
+                "swizzle atoms");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kSfCol + kSfStageCols * kStages <= kTmemCols, "tensor memory budget");
+  static_assert(kThreads * kLaunchRegs <= 65536, "launch registers");
+  static_assert(128 * kRoleRegs + 32 * kEpiWarps * kEpiRegs <= kThreads * kLaunchRegs,
+                "register split within the launch's registers");
+  static_assert(kChunks * kEpiGroups * 32 >= kMaxRows, "chunks cover a unit");
+};
+static_assert(token_blocks<256, 32>(256) == 1 && token_blocks<256, 32>(288) == 1 &&
+                  token_blocks<256, 32>(289) == 2 && token_blocks<256, 32>(544) == 2 &&
+                  token_blocks<256, 32>(545) == 3,
+              "pair token blocks");
+
+// The 32-token chunks an epilogue warp reads: chunk i holds the tokens
+// c0 = 32 * (g + kEpiGroups * i) of the warp's 32 TMEM lanes (quarter q).
+constexpr int kPairChunks = PairMx::kChunks;
+
+// The epilogue's work on the chunks it has read (the accumulator is free again by
+// then).  Phase 0 applies SwiGLU and MX-quantises h along I.  Warps q and q + 2 of a
+// group hold the gate and up rows of the same 32 features (lanes); they swap half of
+// each chunk through shared memory, so the gate warp finishes tokens 0-15 of the
+// chunk and the up warp tokens 16-31, each lane one feature.  Each token's block
+// maximum over the warp's 32 lanes comes from a butterfly (16 values halved over
+// lane offsets 16, 8, 4, 2, then combined over offset 1: lanes 2t and 2t + 1 end
+// with token t's maximum), the scale exponent is broadcast back, and every lane
+// writes its code byte of each token row (32 consecutive bytes per token).  Phase 1
+// writes y in bf16 through a 32 x 32 transpose.
+__device__ __forceinline__ void pair_epilogue(const MxArgs& args, const Unit& t,
+                                              float (&acc)[kPairChunks][32], uint8_t* sEpi,
+                                              int q, int g, int lane, int& nchunk) {
+  constexpr int kPad = PairMx::kPad, kG = PairMx::kEpiGroups;
+  if (t.ph == 0) {
+    float* xs = reinterpret_cast<float*>(sEpi) + (g * 2 + (q >> 1)) * 128;
+#pragma unroll
+    for (int i = 0; i < kPairChunks; ++i) {
+      const int c0 = 32 * (g + kG * i);
+      if (c0 >= t.rows) break;
+      swiglu_mx_chunk<kPad>(args, acc[i], t.row0, c0, t.rows, t.mb, q, lane, xs, nchunk & 1,
+                            2 + (q >> 1) + 2 * g);
+      ++nchunk;
+    }
+  } else {
+    uint16_t* tile = reinterpret_cast<uint16_t*>(sEpi) + (g * 4 + q) * 32 * 32;
+    const int ld = args.ld[1];
+#pragma unroll
+    for (int i = 0; i < kPairChunks; ++i) {
+      const int c0 = 32 * (g + kG * i);
+      if (c0 >= t.rows) break;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) tile[j * 32 + lane] = f2bf(acc[i][j]);
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int idx = lane + 32 * it;
+        const int j = idx >> 2, c = idx & 3;
+        if (c0 + j < t.rows) {
+          const uint4 val = *reinterpret_cast<const uint4*>(tile + j * 32 + c * 8);
+          *reinterpret_cast<uint4*>(args.y + (size_t)(t.row0 + c0 + j) * ld + t.mb * kBM +
+                                    q * 32 + c * 8) = val;
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// Pair unit u: phase, expert, the pair's 256-row weight block (mb; the units per
+// expert are counted in 256-row blocks), token block of up to 256 + 32 rows.
+__device__ __forceinline__ Unit decode_pair_unit(int u, const Tables& tb) {
+  return decode_unit<PairMx::kBN, PairMx::kTail>(u, tb);
+}
+
+__global__ void __launch_bounds__(PairMx::kThreads, 1)
+    grouped_gemm_mx_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
+                                const __grid_constant__ CUtensorMap tmB0,
+                                const __grid_constant__ CUtensorMap tmA1,
+                                const __grid_constant__ CUtensorMap tmB1,
+                                const __grid_constant__ CUtensorMap tmX0,   // 16-row tail boxes
+                                const __grid_constant__ CUtensorMap tmX1, const MxArgs args) {
+  using S = PairMx;
+  constexpr int kStages = S::kStages, kSfAtoms = S::kSfAtoms, kSfStageCols = S::kSfStageCols;
+  constexpr int kSfCol = S::kSfCol, kBN = S::kBN, kTail = S::kTail, kPad = S::kPad;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem + S::kA;
+  uint8_t* sB = smem + S::kB;
+  uint8_t* sT = smem + S::kT;
+  uint8_t* sSF = smem + S::kSf;
+  uint8_t* sEpi = smem + S::kEpi;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBar);
+  uint64_t* empty = full + kStages;
+  uint64_t* sfready = empty + kStages;   // used in the even CTA only
+  uint64_t* tfull = sfready + kStages;
+  uint64_t* tempty = tfull + 1;          // waited on in the even CTA only
+  uint64_t* fin = tempty + 1;
+  uint64_t* fin_sf = fin + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S::kMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::kMisc + 4);
+  int* s_off = reinterpret_cast<int*>(smem + S::kTables);
+  int* s_poff = s_off + (kMaxE + 1);
+  int* s_uoff0 = s_poff + (kMaxE + 1);
+  int* s_uoff1 = s_uoff0 + (kMaxE + 1);
+  int* s_tmp = s_uoff1 + (kMaxE + 1);
+  uint2* s_units = reinterpret_cast<uint2*>(smem + S::kUnits);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = args.E;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
+  pdl_trigger();
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      // even CTA: its two producers + the odd CTA's forwarded arrival
+      mbar_init(&full[s], leader ? 3 : 2);
+      mbar_init(&empty[s], 1);
+      mbar_init(&sfready[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * S::kEpiWarps);   // the epilogue warps of both CTAs
+    mbar_init(fin, 1);
+    mbar_init(fin_sf, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB1);
+    tma_prefetch_desc(&tmX0);
+    tma_prefetch_desc(&tmX1);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(s_tmem, S::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  for (int i = tid; i <= E; i += S::kThreads) s_off[i] = args.offsets[i];
+  __syncthreads();
+
+  // pair units per expert (per phase) and the 128-row padded offsets, by block scans
+  {
+    int v[3] = {0, 0, 0};
+    if (tid < E) {
+      const int m = s_off[tid + 1] - s_off[tid];
+      const int nb = token_blocks<kBN, kTail>(m);
+      v[0] = args.active[0] ? nb * (args.MW[0] / (2 * kBM)) : 0;
+      v[1] = args.active[1] ? nb * (args.MW[1] / (2 * kBM)) : 0;
+      v[2] = ((m + kPad - 1) / kPad) * kPad;
+    }
+    int* dsts[3] = {s_uoff0, s_uoff1, s_poff};
+    for (int p = 0; p < 3; ++p) {
+      int inc = v[p];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) s_tmp[warp] = inc;
+      __syncthreads();
+      int pre = 0, tot = 0;
+      for (int w = 0; w < S::kThreads / 32; ++w) {
+        if (w < warp) pre += s_tmp[w];
+        tot += s_tmp[w];
+      }
+      if (tid < E) dsts[p][tid] = pre + inc - v[p];
+      if (tid == 0) dsts[p][E] = tot;
+      __syncthreads();
+    }
+  }
+  tc_fence_after_sync();
+  // both CTAs' barriers are initialised and TMEM allocated before any remote arrive
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
+  Tables tb;
+  tb.off = s_off;
+  tb.poff = s_poff;
+  tb.uoff[0] = s_uoff0;
+  tb.uoff[1] = s_uoff1;
+  tb.E = E;
+  const int total = s_uoff0[E] + s_uoff1[E];
+  const int my_units = pair < total ? (total - pair + npairs - 1) / npairs : 0;
+  const bool use_list = my_units <= S::kMaxUnits;   // the same in every thread of the cluster
+  if (use_list) {
+    for (int i = tid; i < my_units; i += S::kThreads)
+      s_units[i] = pack_unit(decode_pair_unit(pair + i * npairs, tb));
+    __syncthreads();
+  }
+  const uint32_t lead_full0 = mapa_shared(smem_u32(&full[0]), 0);
+  const uint32_t lead_tempty = mapa_shared(smem_u32(tempty), 0);
+  // Registers: the role warpgroup needs few, the epilogue warpgroups hold up to
+  // kPairChunks x 32 accumulator values each (kRoleRegs and kEpiRegs share out the
+  // launch's kThreads x kLaunchRegs); each warpgroup's setmaxnreg opens its branch.
+  if (warp < 4) {
+    setmaxnreg_dec<S::kRoleRegs>();
+    if ((warp == 0 || warp == 2) && lane == 0) {
+      // ------------------------------------------------------ TMA producers --
+      const bool weights = warp == 0;
+      const uint64_t pol_w = l2_policy_evict_normal();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t par = 0;
+      uint32_t issued_mask = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
+        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_pair_unit(u, tb);
+        if (!weights && t.ph == 1 && args.done != nullptr) {
+          // the down projection's activations are h of this expert's gate/up units
+          const int m = s_off[t.e + 1] - s_off[t.e];
+          const int need = token_blocks<kBN, kTail>(m) * (args.MW[0] / kBM);
+          if (!wait_counter(args.done + t.e, need, s_abort)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        const int nk = args.K[t.ph] / kBK;
+        const int mb = 2 * t.mb + static_cast<int>(rank);      // this CTA's 128-row block
+        const bool tail = t.rows > kBN;
+        const int nmain = tail ? kBN : ((t.rows + 15) & ~15);
+        const int half = nmain >> 1;
+        const int nsfb = nmain > 128 ? 2 : 1;
+        const uint32_t abytes = args.a_fp4[t.ph] ? kABytes / 2 : kABytes;
+        const uint32_t bytes = weights ? abytes + kSfBytes
+                                       : S::kBBytes + nsfb * kSfBytes + (tail ? S::kTBytes + kSfBytes : 0);
+        const int arow = t.e * args.MW[t.ph] + mb * kBM;
+        const int atile0 = (t.e * (args.MW[t.ph] / kBM) + mb) * nk;
+        const uint8_t* sfsrc =
+            weights ? args.a_sf[t.ph] + ((size_t)(t.e * (args.MW[t.ph] / kBM) + mb) * nk) * kSfBytes
+                    : args.b_sf[t.ph] + ((size_t)(t.row0 / kPad) * nk) * kSfBytes;
+        const int hrow0 = t.row0 + static_cast<int>(rank) * half;
+        const int trow0 = t.row0 + kBN + static_cast<int>(rank) * (kTail / 2);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          uint8_t* sf = sSF + stage * kSfAtoms * kSfBytes;
+          if (weights) {
+            if (args.a_fp4[t.ph])  // tile-major e2m1: tile (e, mb, kb) is rows [128 * tile, +128)
+              tma_load_2d(sA + stage * kABytes, t.ph ? &tmA1 : &tmA0, &full[stage], 0,
+                          (atile0 + kb) * kBM, pol_w);
+            else
+              tma_load_2d(sA + stage * kABytes, t.ph ? &tmA1 : &tmA0, &full[stage], kb * kBK, arow,
+                          pol_w);
+            bulk_load_1d(sf, sfsrc + (size_t)kb * kSfBytes, kSfBytes, &full[stage], pol_w);
+          } else {
+            tma_load_2d(sB + stage * S::kBBytes, t.ph ? &tmB1 : &tmB0, &full[stage], kb * kBK, hrow0,
+                        pol_x);
+            // the token block's B scales, in both CTAs (each CTA's MMA scales all N columns)
+            bulk_load_1d(sf + kSfBytes, sfsrc + (size_t)kb * kSfBytes, kSfBytes, &full[stage], pol_x);
+            if (nsfb == 2)
+              bulk_load_1d(sf + 2 * kSfBytes, sfsrc + ((size_t)nk + kb) * kSfBytes, kSfBytes,
+                           &full[stage], pol_x);
+            if (tail) {
+              tma_load_2d(sT + stage * S::kTBytes, t.ph ? &tmX1 : &tmX0, &full[stage], kb * kBK,
+                          trow0, pol_x);
+              bulk_load_1d(sf + 3 * kSfBytes, sfsrc + ((size_t)2 * nk + kb) * kSfBytes, kSfBytes,
+                           &full[stage], pol_x);
+            }
+          }
+          issued_mask |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (par << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (ok && weights) {
+        // every stage released by the pair's MMAs (their multicast commits have landed)
+        for (int i = 0; i < kStages; ++i) {
+          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        // let this thread's copies land before the CTA can exit (bounded waits)
+        for (int s2 = 0; s2 < kStages; ++s2)
+          if ((issued_mask >> s2) & 1u) mbar_wait(&full[s2], (issued_par >> s2) & 1u, nullptr);
+      }
+    } else if (warp == 3 && lane == 0) {
+      // ------------ even CTA: scale copier; odd CTA: forwarder of its landed stages --
+      int stage = 0;
+      uint32_t par = 0;
+      bool ok = true;
+      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
+        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_pair_unit(u, tb);
+        const int nk = args.K[t.ph] / kBK;
+        const bool tail = t.rows > kBN;
+        const bool two = tail || t.rows > 128;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (leader) {
+            if (!mbar_wait_cluster(&full[stage], par, s_abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * kSfStageCols);
+            const uint32_t sf_s = smem_u32(sSF + stage * kSfAtoms * kSfBytes);
+            tc_cp_pair_32x128b_warpx4(sfa_t, smem_desc_noswz(sf_s, 128));
+            tc_cp_pair_32x128b_warpx4(sfa_t + 4, smem_desc_noswz(sf_s + kSfBytes, 128));
+            if (two) tc_cp_pair_32x128b_warpx4(sfa_t + 8, smem_desc_noswz(sf_s + 2 * kSfBytes, 128));
+            if (tail)
+              tc_cp_pair_32x128b_warpx4(sfa_t + 12, smem_desc_noswz(sf_s + 3 * kSfBytes, 128));
+            tc_commit_pair(&sfready[stage], 1);
+          } else {
+            if (!mbar_wait(&full[stage], par, s_abort)) {
+              ok = false;
+              break;
+            }
+            // this stage's bytes are in this CTA's shared memory (observed above)
+            mbar_arrive_cluster_relaxed(lead_full0 + stage * 8);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        if (leader) {
+          tc_commit_pair(fin_sf, 1);
+          mbar_wait(fin_sf, 0, nullptr);
+        }
+      }
+    } else if (warp == 1 && lane == 0 && leader) {
+      // ----------------------------------------------- even CTA: MMA issuer --
+      int stage = 0;
+      uint32_t par = 0, apar = 0;
+      bool ok = true;
+      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
+        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_pair_unit(u, tb);
+        const bool tail = t.rows > kBN;
+        const int nmain = tail ? kBN : ((t.rows + 15) & ~15);
+        const uint32_t fp4 = args.a_fp4[t.ph] ? (5u << 7) : 0u;
+        const uint32_t idesc_main = idesc_mxf8_f32(2 * kBM, nmain, 0, 0) | fp4;
+        const uint32_t idesc_tail = idesc_mxf8_f32(2 * kBM, kTail, 0, 0) | fp4;
+        // both CTAs' epilogues have read the previous unit's accumulator
+        if (!mbar_wait_cluster(tempty, apar ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base;
+        const int nk = args.K[t.ph] / kBK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&sfready[stage], par, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(kSfCol + stage * kSfStageCols);
+          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * kABytes));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * S::kBBytes));
+  #pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)   // +32 bytes along K = +2 in the start field
+            tc_mma_pair_mxf8(d, adesc + 2 * kk, bdesc + 2 * kk, idesc_main | idesc_sf_ids(kk, kk),
+                             sfa_t, sfa_t + 4, (kb | kk) ? 1u : 0u);
+          if (tail) {
+            const uint64_t tdesc = smem_desc_sw128(smem_u32(sT + stage * S::kTBytes));
+  #pragma unroll
+            for (int kk = 0; kk < kBK / 32; ++kk)
+              tc_mma_pair_mxf8(d + kBN, adesc + 2 * kk, tdesc + 2 * kk,
+                               idesc_tail | idesc_sf_ids(kk, kk), sfa_t, sfa_t + 12,
+                               (kb | kk) ? 1u : 0u);
+          }
+          tc_commit_pair(&empty[stage], 3);
+          if (++stage == kStages) {
+            stage = 0;
+            par ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair(tfull, 3);
+        apar ^= 1u;
+      }
+      // the last unit's epilogues (the odd CTA's arrivals are remote) finish before exit
+      if (ok && !mbar_wait_cluster(tempty, apar ^ 1u, s_abort)) ok = false;
+      if (!ok) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        tc_commit_pair(fin, 1);
+        mbar_wait(fin, 0, nullptr);
+      }
+    }
+  } else {
+    setmaxnreg_inc<S::kEpiRegs>();
+    // ------------------------------------------------------------ epilogue --
+    const int q = warp & 3;                  // TMEM lane quarter
+    const int g = (warp - 4) >> 2;           // chunk group: 32-token chunks g, g + 3, ...
+    const int et = tid - 128;
+    int* s_flag = s_tmp;
+    int nchunk = 0;                          // gate/up chunks so far (the xs slot parity)
+    uint32_t apar = 0;
+    for (int u = pair, ui = 0; u < total; u += npairs, ++ui) {
+      Unit t = use_list ? unpack_unit(s_units[ui]) : decode_pair_unit(u, tb);
+      t.mb = 2 * t.mb + static_cast<int>(rank);
+      if (et == 0) s_flag[0] = mbar_wait(tfull, apar, s_abort) ? 1 : 0;
+      named_bar_sync(1, 32 * S::kEpiWarps);
+      const int ok = s_flag[0];
+      named_bar_sync(1, 32 * S::kEpiWarps);
+      if (!ok) {
+        if (et == 0) {
+          *s_abort = 1;
+          flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after_sync();
+      // read this warp's chunks into registers, then hand the accumulator back to the
+      // MMA thread before working on them
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      float acc[kPairChunks][32];
+#pragma unroll
+      for (int i = 0; i < kPairChunks; ++i) {
+        const int c0 = 32 * (g + S::kEpiGroups * i);
+        if (c0 < t.rows) tmem_ld_32x32b_x32_nowait(tbase + c0, acc[i]);
+      }
+      tmem_wait_ld();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty);
+        else mbar_arrive_cluster(lead_tempty);
+      }
+      pair_epilogue(args, t, acc, sEpi, q, g, lane, nchunk);
+      if (t.ph == 0 && args.done != nullptr) {
+        __threadfence();
+        fence_proxy_async_global();
+        named_bar_sync(1, 32 * S::kEpiWarps);
+        if (et == 0) red_release_add_gpu(args.done + t.e, 1);
+      }
+      apar ^= 1u;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, S::kTmemCols);
   }
 }
 
@@ -749,6 +1288,77 @@ cudaError_t launch_shape(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1, const i
                             tm[5], a);
 }
 
+cudaError_t launch_pair_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1, const int32_t* offsets,
+                           int E, int P_pad_rows, int* done, int* status, cudaStream_t s) {
+  using S = PairMx;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+      err = cudaFuncSetAttribute(grouped_gemm_mx_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+      if (err != cudaSuccess) return err;
+      attr_set[dev] = true;
+    }
+  }
+  MxArgs a{};
+  a.offsets = offsets;
+  a.E = E;
+  a.done = (ph0 && ph1) ? done : nullptr;
+  a.status = status;
+  CUtensorMap tm[6];   // A0, B0, A1, B1 (128-row boxes), then the 16-row tail boxes
+  const GemmPhaseMx* phs[2] = {ph0, ph1};
+  for (int p = 0; p < 2; ++p) {
+    const GemmPhaseMx* g = phs[p] ? phs[p] : (ph0 ? ph0 : ph1);
+    a.active[p] = phs[p] != nullptr;
+    a.K[p] = g->K;
+    a.MW[p] = g->MW;
+    a.ld[p] = g->n_out;
+    a.a_sf[p] = g->A_sf;
+    a.b_sf[p] = g->B_sf;
+    a.a_fp4[p] = g->a_fp4 ? 1 : 0;
+    const bool ok_a =
+        g->a_fp4 ? encode_tmap_2d_fp4(&tm[2 * p], g->A_q, (uint64_t)E * g->MW * (g->K / kBK))
+                 : encode_tmap_2d_u8(&tm[2 * p], g->A_q, (uint64_t)g->K, (uint64_t)E * g->MW, kBK,
+                                     kBM);
+    if (!ok_a) return cudaErrorInvalidValue;
+    if (!encode_tmap_2d_u8(&tm[2 * p + 1], g->B_q, (uint64_t)g->K, (uint64_t)P_pad_rows, kBK,
+                           S::kBN / 2) ||
+        !encode_tmap_2d_u8(&tm[4 + p], g->B_q, (uint64_t)g->K, (uint64_t)P_pad_rows, kBK,
+                           S::kTail / 2))
+      return cudaErrorInvalidValue;
+  }
+  if (ph0) {
+    a.hq = ph0->out_q;
+    a.h_sf = ph0->out_sf;
+  }
+  if (ph1) a.y = ph1->out_bf16;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_sm_count() & ~1, 1, 1);
+  cfg.blockDim = dim3(S::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = a.done != nullptr ? 1 : 0;  // co-residency for the phase dependency
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_pair_kernel, tm[0], tm[1], tm[2], tm[3], tm[4],
+                            tm[5], a);
+}
+
+// The pair kernel takes weight matrices that split into 256-row blocks.
+bool pairable_mx(const GemmPhaseMx* g) { return g == nullptr || g->MW % (2 * kBM) == 0; }
+
 }  // namespace
 
 cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1,
@@ -760,9 +1370,24 @@ cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph
     if (fp4) return launch_shape<ShapeDecodeFp4>(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
     return launch_shape<ShapeDecode>(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
   }
-  if (pad == ShapePrefill::kPad)
-    return launch_shape<ShapePrefill>(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
-  return cudaErrorInvalidValue;
+  if (pad != ShapePrefill::kPad) return cudaErrorInvalidValue;
+  // Prefill-size tiles on CTA pairs where the shapes allow.  When the driver refuses
+  // the cooperative cluster launch (not every SM free for a cluster, e.g. under a
+  // profiler or next to another context), this call runs the one-CTA kernel; a device
+  // that never accepted it is not asked again.
+  static std::atomic<int> pair_state[64];  // 0 unknown, 1 launched, 2 refused
+  int dev = 0;
+  if (pairable_mx(ph0) && pairable_mx(ph1) && device_sm_count() >= 2 &&
+      cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && pair_state[dev].load() != 2) {
+    const cudaError_t err = launch_pair_mx(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
+    if (err == cudaSuccess) {
+      pair_state[dev].store(1);
+      return err;
+    }
+    (void)cudaGetLastError();   // a refused launch configuration is not a sticky error
+    if (pair_state[dev].load() != 1) pair_state[dev].store(2);
+  }
+  return launch_shape<ShapePrefill>(ph0, ph1, offsets, E, P_pad_rows, done, status, s);
 }
 
 }  // namespace moe

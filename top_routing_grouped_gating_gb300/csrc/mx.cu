@@ -159,8 +159,11 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const float* __restric
 }
 
 // MX pre-quantisation of logical weights W (E, K, Ncols) along K into K-major fp8
-// rows of the packed order (row_of -> logical column) plus scale atoms.  Tile:
-// 128 K values x 32 packed rows per CTA (32 x 8 threads).
+// rows of the packed order plus scale atoms.  w13's packed order is the bf16
+// packing's: in 128-row block b, the 32-row quarter q holds the 16 gate rows of
+// features 64b + 16q .. 64b + 16q + 15 and then their 16 up rows, so that one TMEM
+// lane quarter of the GEMM accumulator pairs them within a warp.  Tile: 128 K values
+// x 32 packed rows per CTA (32 x 8 threads).
 template <bool kW13>
 __global__ void __launch_bounds__(256) pack_mx_kernel(const uint16_t* __restrict__ w, int K,
                                                       int ncols, int I, uint8_t* __restrict__ q,
@@ -168,17 +171,13 @@ __global__ void __launch_bounds__(256) pack_mx_kernel(const uint16_t* __restrict
   __shared__ float tile[128][33];
   const int k0 = blockIdx.x * 128, r0 = blockIdx.y * 32, e = blockIdx.z;
   const int tx = threadIdx.x, ty = threadIdx.y;
-  int col0;
-  if (kW13) {
-    const int blk = r0 / 128, within = r0 % 128;
-    col0 = within < 64 ? blk * 64 + within : I + blk * 64 + (within - 64);
-  } else {
-    col0 = r0;
-  }
+  // this thread's logical column: for w13, packed row 32q + i of 128-row block b holds
+  // gate feature 64b + 16q + i (i < 16) or the matching up feature (i >= 16)
+  const int col = kW13 ? (r0 / 128) * 64 + ((r0 % 128) / 32) * 16 + (tx & 15) + (tx < 16 ? 0 : I)
+                       : r0 + tx;
   for (int i = ty; i < 128; i += 8)
-    tile[i][tx] = __uint_as_float(static_cast<uint32_t>(
-                                      w[((size_t)e * K + k0 + i) * ncols + col0 + tx])
-                                  << 16);
+    tile[i][tx] =
+        __uint_as_float(static_cast<uint32_t>(w[((size_t)e * K + k0 + i) * ncols + col]) << 16);
   __syncthreads();
   const int rows_total = ncols;  // packed rows per expert
   const int ksteps = K / 128;
@@ -214,17 +213,13 @@ __global__ void __launch_bounds__(256) pack_mx4_kernel(const uint16_t* __restric
   __shared__ float tile[128][33];
   const int k0 = blockIdx.x * 128, r0 = blockIdx.y * 32, e = blockIdx.z;
   const int tx = threadIdx.x, ty = threadIdx.y;
-  int col0;
-  if (kW13) {
-    const int blk = r0 / 128, within = r0 % 128;
-    col0 = within < 64 ? blk * 64 + within : I + blk * 64 + (within - 64);
-  } else {
-    col0 = r0;
-  }
+  // this thread's logical column: for w13, packed row 32q + i of 128-row block b holds
+  // gate feature 64b + 16q + i (i < 16) or the matching up feature (i >= 16)
+  const int col = kW13 ? (r0 / 128) * 64 + ((r0 % 128) / 32) * 16 + (tx & 15) + (tx < 16 ? 0 : I)
+                       : r0 + tx;
   for (int i = ty; i < 128; i += 8)
-    tile[i][tx] = __uint_as_float(static_cast<uint32_t>(
-                                      w[((size_t)e * K + k0 + i) * ncols + col0 + tx])
-                                  << 16);
+    tile[i][tx] =
+        __uint_as_float(static_cast<uint32_t>(w[((size_t)e * K + k0 + i) * ncols + col]) << 16);
   __syncthreads();
   const int rows_total = ncols;
   const int ksteps = K / 128;
