@@ -711,7 +711,7 @@ struct PairMx {
   static constexpr int kTail = 32;                 // rows the last unit of an expert absorbs
   static constexpr int kMaxRows = kBN + kTail;
   static constexpr int kPad = 128;                 // row padding of the expert blocks
-  static constexpr int kStages = 5;
+  static constexpr int kStages = 6;
   static constexpr int kEpiGroups = 3;             // epilogue warps per TMEM lane quarter
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kThreads = 32 * (4 + kEpiWarps);
@@ -723,10 +723,7 @@ struct PairMx {
   static constexpr int kSfCol = kMaxRows;          // scale slots follow the accumulator
   static constexpr int kTmemCols = 512;
   static constexpr int kEpiGroupBytes = 2 * 128 * 4;          // block-maximum swaps, phase 0
-  static constexpr int kTileBytes = 32 * 32 * 2;              // bf16 transpose, phase 1
-  static constexpr int kEpiBytes = kEpiGroups * kEpiGroupBytes > kEpiWarps * kTileBytes
-                                       ? kEpiGroups * kEpiGroupBytes
-                                       : kEpiWarps * kTileBytes;
+  static constexpr int kEpiBytes = kEpiGroups * kEpiGroupBytes;
   static constexpr int kMaxUnits = 256;
   // registers: 65536 / 512 at launch; the epilogue warpgroups hold kChunks x 32 values
   static constexpr int kLaunchRegs = 128;
@@ -787,26 +784,24 @@ __device__ __forceinline__ void pair_epilogue(const MxArgs& args, const Unit& t,
       ++nchunk;
     }
   } else {
-    uint16_t* tile = reinterpret_cast<uint16_t*>(sEpi) + (g * 4 + q) * 32 * 32;
+    // lane l holds output feature q * 32 + l of the CTA's weight block for 32 tokens;
+    // one shuffle per token pair gives the even lanes two neighbouring features of
+    // token j and the odd lanes two of token j + 1, so each store writes 64 bytes of
+    // each of two rows
     const int ld = args.ld[1];
+    const bool even = (lane & 1) == 0;
+    uint16_t* ycol = args.y + t.mb * kBM + q * 32 + (lane & ~1);
 #pragma unroll
     for (int i = 0; i < kPairChunks; ++i) {
       const int c0 = 32 * (g + kG * i);
       if (c0 >= t.rows) break;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) tile[j * 32 + lane] = f2bf(acc[i][j]);
-      __syncwarp();
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int idx = lane + 32 * it;
-        const int j = idx >> 2, c = idx & 3;
-        if (c0 + j < t.rows) {
-          const uint4 val = *reinterpret_cast<const uint4*>(tile + j * 32 + c * 8);
-          *reinterpret_cast<uint4*>(args.y + (size_t)(t.row0 + c0 + j) * ld + t.mb * kBM +
-                                    q * 32 + c * 8) = val;
-        }
+      for (int j = 0; j < 32; j += 2) {
+        const float x = __shfl_xor_sync(0xffffffffu, even ? acc[i][j + 1] : acc[i][j], 1);
+        const uint32_t pk = even ? pack_bf16x2(acc[i][j], x) : pack_bf16x2(x, acc[i][j + 1]);
+        const int tok = c0 + j + (even ? 0 : 1);
+        if (tok < t.rows) *reinterpret_cast<uint32_t*>(ycol + (size_t)(t.row0 + tok) * ld) = pk;
       }
-      __syncwarp();
     }
   }
 }
@@ -1181,9 +1176,12 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
       tmem_wait_ld();
       tc_fence_before_sync();
       __syncwarp();
+      // the TMEM reads are complete (tcgen05.wait::ld above), so the odd CTA's remote
+      // arrive needs no release: a release at cluster scope would first wait for this
+      // thread's global stores of the previous unit
       if (lane == 0) {
         if (leader) mbar_arrive(tempty);
-        else mbar_arrive_cluster(lead_tempty);
+        else mbar_arrive_cluster_relaxed(lead_tempty);
       }
       pair_epilogue(args, t, acc, sEpi, q, g, lane, nchunk);
       if (t.ph == 0 && args.done != nullptr) {
