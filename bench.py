@@ -75,7 +75,21 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the cpu_baseline sample")
+    ap.add_argument("--shape", default="",
+                    help="reduced copy of a single workload for profiling captures, e.g. E=32,T=2048 "
+                         "(the line then names the changed sizes; it is not a bench result)")
     return ap.parse_args(argv)
+
+
+def parse_shape(text: str) -> dict:
+    """'E=32,T=2048' -> {'E': 32, 'T': 2048} (integer fields of the workload config)."""
+    out = {}
+    for part in filter(None, (p.strip() for p in text.split(","))):
+        key, _, val = part.partition("=")
+        if key not in ("T", "H", "E", "k", "I") or not val.isdigit():
+            raise SystemExit(f"--shape: expected T/H/E/k/I=<int>, got {part!r}")
+        out[key] = int(val)
+    return out
 
 
 # ----------------------------------------------------------------- helpers ---
@@ -784,6 +798,14 @@ def main(argv=None):
     for n in names:
         if n not in W.CONFIGS:
             raise SystemExit(f"unknown workload {n}; 'all' or one of {sorted(W.CONFIGS)}")
+    if args.shape:
+        if len(names) != 1:
+            raise SystemExit("--shape applies to a single --workload")
+        base = W.CONFIGS[names[0]]
+        cfg = W.with_shape(base, name=base.name + "@" + args.shape.replace(",", "_"),
+                           **parse_shape(args.shape))
+        W.CONFIGS = {**W.CONFIGS, cfg.name: cfg}
+        names = [cfg.name]
     if len(names) == 1 and W.CONFIGS[names[0]].ep_ranks:
         return run_ep_routing(args, W.CONFIGS[names[0]])
     if args.impl == "reference":

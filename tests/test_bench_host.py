@@ -155,3 +155,12 @@ def test_profiled_traffic_lookup_and_voiding(tmp_path, monkeypatch):
     (tmp_path / "profiles" / "grouped_gemm_mxfp8_prefill.md").write_text(
         f"kernel_source_sha256_16: {mx_sha}\ntraffic_bytes_per_launch: 2.5e9\n")
     assert bench.profiled_traffic("mxfp8_prefill") == 2.5e9
+
+
+def test_parse_shape():
+    assert bench.parse_shape("E=32,T=2048") == {"E": 32, "T": 2048}
+    assert bench.parse_shape("") == {}
+    with pytest.raises(SystemExit):
+        bench.parse_shape("Z=3")
+    with pytest.raises(SystemExit):
+        bench.parse_shape("E=x")

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/moe_gb300.h"
@@ -160,6 +161,14 @@ T* at(void* base, size_t off) {
 }  // namespace
 
 namespace moe {
+
+bool pair_launch_noncooperative() {
+  static const bool on = [] {
+    const char* v = std::getenv("MOE_GB300_PAIR_NONCOOPERATIVE");
+    return v != nullptr && v[0] == '1' && v[1] == '\0';
+  }();
+  return on;
+}
 
 int device_sm_count() {
   DeviceFacts* d = nullptr;

@@ -1347,7 +1347,9 @@ cudaError_t launch_pair_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1, const
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = a.done != nullptr ? 1 : 0;  // co-residency for the phase dependency
+  // co-residency for the phase dependency; profilers refuse cooperative cluster
+  // launches, so profiling may ask for a plain cluster launch instead
+  attr[1].val.cooperative = (a.done != nullptr && !pair_launch_noncooperative()) ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_pair_kernel, tm[0], tm[1], tm[2], tm[3], tm[4],

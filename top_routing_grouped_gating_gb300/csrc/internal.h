@@ -172,6 +172,16 @@ cudaError_t launch_re_routing(const uint16_t* xin, const int32_t* cnt, int R, in
                               uint16_t* xout, int32_t* perm, int32_t* offsets, void* ws,
                               cudaStream_t s);
 
+// ---- profiling switch (api.cu)
+// True when the environment variable MOE_GB300_PAIR_NONCOOPERATIVE is set to 1 (read
+// once): the CTA-pair grouped GEMMs are then launched as plain cluster launches
+// instead of cooperative ones, because profilers refuse cooperative cluster launches.
+// The grid is one CTA per SM either way; co-residency of the two projections' CTAs is
+// then expected rather than guaranteed (on an otherwise idle GPU every CTA is
+// resident), and a phase-1 wait that could not end runs out its bounded limit and
+// sets MOE_DEV_WAIT_TIMEOUT.  Off by default; for profiling only.
+bool pair_launch_noncooperative();
+
 // ---- device facts (api.cu)
 int device_sm_count();
 int* device_status_ptr();  // the current device's status word, or null
