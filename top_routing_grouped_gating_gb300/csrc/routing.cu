@@ -164,16 +164,24 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int s = 0; s < k; ++s) {
-      const int p = s_row[s];
-      if (p < 0) continue;
-      const float ws = s_w[s];
-      const uint4 q = reinterpret_cast<const uint4*>(y2 + (size_t)p * H)[v];
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    // eight slots' loads in flight at once, then the fp32 sum in slot order
+    for (int s0 = 0; s0 < k; s0 += 8) {
+      uint4 q[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(ws, bf16_lo(u[i]), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(ws, bf16_hi(u[i]), acc[2 * i + 1]);
+      for (int i = 0; i < 8; ++i) {
+        const int p = s0 + i < k ? s_row[s0 + i] : -1;
+        q[i] = p >= 0 ? reinterpret_cast<const uint4*>(y2 + (size_t)p * H)[v] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (s0 + i >= k || s_row[s0 + i] < 0) continue;
+        const float ws = s_w[s0 + i];
+        const uint32_t u[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[2 * j] = fmaf(ws, bf16_lo(u[j]), acc[2 * j]);
+          acc[2 * j + 1] = fmaf(ws, bf16_hi(u[j]), acc[2 * j + 1]);
+        }
       }
     }
     uint4 o;
