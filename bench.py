@@ -55,7 +55,8 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+                "clocks_event_reasons.gpu_idle")
 # The measured layer shapes, the largest (the headline) last.
 SUITE = ("qwen3_30b_a3b_decode", "qwen3_30b_a3b_prefill_zipf", "qwen3_235b_a22b_decode",
          "mxfp8_prefill", "qwen3_235b_a22b_prefill")
@@ -163,7 +164,7 @@ class ClockSampler:
         except Exception:
             sel = []
         self.cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
-                    "-lms", "50"] + sel
+                    "-lms", "10"] + sel
 
     def start(self):
         try:
@@ -183,15 +184,32 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
-        if not rows:
+        return parse_clock_samples(out)
+
+
+def parse_clock_samples(text: str):
+    """Summarise nvidia-smi rows of CLOCK_FIELDS.  A sample counts as under load when
+    the driver does not report the GPU idle; sm_mhz is the median SM clock of those
+    samples (of all samples when none was under load, which samples_under_load = 0
+    then says), and reasons are the throttle reasons seen in any sample."""
+    rows = [[f.strip() for f in r.split(",")] for r in text.strip().splitlines() if r.count(",") >= 9]
+    if not rows:
+        return None
+
+    def num(v):
+        try:
+            return float(v)
+        except ValueError:
             return None
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+
+    loaded = [r for r in rows if r[9] != "Active"]
+    pick = loaded if loaded else rows
+    sm = [x for x in (num(r[1]) for r in pick) if x is not None]
+    mx = [x for x in (num(r[2]) for r in rows) if x is not None]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
 
 
 # ------------------------------------------------------ algorithmic work ---

@@ -164,3 +164,23 @@ def test_parse_shape():
         bench.parse_shape("Z=3")
     with pytest.raises(SystemExit):
         bench.parse_shape("E=x")
+
+
+def test_clock_samples_keep_the_loaded_ones():
+    # index, sm, max sm, power, active mask, hw, hw thermal, sw thermal, sw power cap, idle
+    text = "\n".join([
+        "0, 2070, 2070, 180.5, 0x0000000000000001, Not Active, Not Active, Not Active, Not Active, Active",
+        "0, 1830, 2070, 1210.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active, Not Active",
+        "0, 1800, 2070, 1390.2, 0x0000000000000004, Not Active, Not Active, Not Active, Active, Not Active",
+        "0, 1860, 2070, 1250.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active, Not Active",
+        "0, 2070, 2070, 175.0, 0x0000000000000001, Not Active, Not Active, Not Active, Not Active, Active",
+    ])
+    c = bench.parse_clock_samples(text)
+    assert c["samples"] == 5 and c["samples_under_load"] == 3
+    assert c["sm_mhz"] == 1830.0                    # median of 1830, 1800, 1860
+    assert c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+    # no loaded sample: all samples, and the count says so
+    idle = bench.parse_clock_samples(text.splitlines()[0] + "\n" + text.splitlines()[4])
+    assert idle["samples_under_load"] == 0 and idle["sm_mhz"] == 2070.0
+    assert bench.parse_clock_samples("") is None
