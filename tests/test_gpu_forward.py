@@ -98,13 +98,16 @@ def test_forward_limits(layers, T, E, k):
 
 
 @pytest.mark.parametrize("counts", [
-    [256, 257, 255, 512, 513, 1, 0, 254],   # on both sides of one and two 256-row blocks
-    [1, 16, 17, 33, 255, 256, 480, 990],    # half blocks of 8, 9, 17 (thin boxes) to 128 rows
+    [256, 257, 255, 512, 513, 33, 40, 254],  # no expert of <= 32 rows: 256-row blocks, both sides
+    [224, 225, 223, 448, 449, 1, 0, 32],     # 1 and 32 rows run light: 224-row heavy blocks
+    [1, 16, 17, 33, 255, 256, 480, 990],     # light 1-17; heavy halves of 17 to 112 rows, thin tails
 ])
 def test_forward_token_block_boundaries(layers, counts):
-    """Expert loads on both sides of the 256-row token blocks of the wide-tile GEMM
-    (and one expert with a single row, one with none), forced through designed
-    logits; also the thin boxes for units whose half block has at most 32 rows."""
+    """Expert loads forced through designed logits onto both sides of the token
+    blocks of the CTA-pair GEMM: 256-row blocks when no expert has 32 rows or fewer,
+    224-row heavy blocks next to the light pipeline's experts (up to 32 rows, one
+    with a single row, one with none), and the thin boxes of units whose half block
+    has at most 16 rows."""
     k = 2
     T = sum(counts) // k
     cfg, inp, layer = layers("tiny", T=T, E=len(counts), k=k)

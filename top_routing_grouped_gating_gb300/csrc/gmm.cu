@@ -23,11 +23,12 @@
 //
 // Warp roles (256 threads): warp 0 lane 0 = TMA producer; warp 1 lane 0 = MMA
 // issuer; warp 2 = TMEM allocator; warps 4-7 = epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. +31).  Prefill-size token tiles run on the CTA-pair variant further
-// down (grouped_gemm_pair_kernel), which keeps these units, roles and epilogue.  Shared memory holds a STAGES-deep ring of (A 128x64, B BNx64)
+// 32*(w%4) .. +31).  Shared memory holds a STAGES-deep ring of (A 128x64, B BNx64)
 // bf16 tiles in the 128-byte-swizzled K-major layout TMA writes; TMEM holds two
 // 128 x BN fp32 accumulators so the epilogue of one unit overlaps the MMAs of the
-// next.
+// next.  Prefill-size token tiles run on the CTA-pair variant further down
+// (grouped_gemm_pair_kernel): the same unit order and phase dependency on 256-row
+// weight blocks, with a second pipeline for the experts that hold only a few tokens.
 #include <atomic>
 #include <mutex>
 
@@ -534,69 +535,448 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------ CTA pairs --
 // Prefill variant on pairs of SMs (a cluster of two CTAs).  A pair unit is
-// (phase, expert, 256-row weight block, token block of up to 256 rows): one
-// tcgen05.mma.cta_group::2 of M = 256 covers both CTAs' 128-row weight blocks
-// (CTA r holds block 2*pb + r of A) and the token block's N columns, of which
-// CTA r holds rows [r*N/2, (r+1)*N/2) of B.  Each CTA's TMEM receives the full
-// 128 x N accumulator of its own weight block, so the epilogue is the one-CTA
-// kernel's.  Per SM and stage the ring then holds 16 KB of weights and 16 KB of
-// tokens instead of 16 + 32 KB: six stages fit where four did, and the L2 and
-// shared-memory traffic per FLOP drops by a third.
+// (phase, expert, 256-row weight block, token block): one tcgen05.mma.cta_group::2
+// of M = 256 covers both CTAs' 128-row weight blocks (CTA r holds block 2*pb + r of
+// A) and the token block's N columns, of which CTA r holds rows [r*N/2, (r+1)*N/2)
+// of B.  Each CTA's TMEM receives the full 128 x N accumulator of its own weight
+// block.  Per SM and stage the ring holds 16 KB of weights and at most 16 KB of
+// tokens, so six stages fit.
 //
-// Roles: warp 0 lane 0 of each CTA loads its own A and B halves onto its own
-// `full` barrier; in the odd CTA, warp 3 lane 0 passes each landed stage on to
-// the even CTA's `full` barrier (a relaxed remote arrive); warp 1 lane 0 of the
-// even CTA issues the MMAs and commits each stage's release and each
-// accumulator's completion to both CTAs (multicast commit); warps 4-7 of both
-// CTAs drain their accumulators and arrive on the even CTA's `tempty`.
-constexpr int kPairBN = 256;        // token rows per pair unit
-constexpr int kPairBoxS = 32;       // B box rows for units whose half is at most 32 rows
-constexpr int kPairTmemCols = 512;  // two 128 x 256 fp32 accumulators per CTA
+// Two pipelines share the pair.  Experts with at most kLightRows tokens (the cold
+// experts of a skewed router) stream a whole weight matrix for a handful of
+// tokens: their stages cost the MMA thread as much issue time as full ones while
+// the tensor pipe idles, and their weights come from HBM.  They run on a light
+// pipeline of their own (a second producer, MMA thread, forwarder and epilogue
+// group, a two-stage ring with 16-row token slots and two 32-column accumulators),
+// so that their weight streaming overlaps the heavy units' tensor work instead of
+// adding to it.  The other experts' units run on the heavy pipeline.  An expert's
+// units all go to one pipeline, so the down projection's wait for h never crosses
+// pipelines.  With light experts present the heavy accumulators narrow to 224
+// columns (TMEM columns 0 and 256; the light ones sit at 224 and 480) and the heavy
+// token slots to 112 rows per CTA; without them the heavy pipeline keeps 256-token
+// blocks and 128-row slots, and the light roles find no units.
+//
+// Roles (512 threads): in each CTA, warp 0 lane 0 loads the heavy tiles and warp 2
+// lane 0 the light ones, each onto its own ring's `full` barrier; in the even CTA
+// warp 1 lane 0 issues the heavy MMAs and warp 3 lane 0 the light ones, committing
+// each stage's release and each accumulator's completion to both CTAs (multicast
+// commit); in the odd CTA warps 3 and 1 forward the heavy and light stage arrivals
+// to the even CTA (a relaxed remote arrive).  Warps 4-11 drain the heavy
+// accumulators (two per TMEM lane quarter, alternating 32-token chunks) and warps
+// 12-15 the light ones, storing from registers, and arrive on the even CTA's `tempty`.
+constexpr int kPairBN = 256;         // token rows per heavy unit without light experts
+constexpr int kPairBNL = 224;        // ... and next to light experts
+constexpr int kLightRows = 32;       // experts with at most this many tokens run light
+constexpr int kLightBox = 16;        // B rows per CTA of a light unit (N <= 32)
+constexpr int kPairBoxS = 16;        // B box rows of heavy units whose half is <= 16 rows
+constexpr int kPairThreads = 512;
+constexpr int kPairStages = 6;       // heavy ring
+constexpr int kLightStages = 2;
+constexpr int kHeavyEpiWarps = 8;
+constexpr int kLightEpiWarps = 4;
+constexpr int kPairMaxUnits = 256;   // per pipeline list in shared memory
+constexpr int kPairTmemCols = 512;
 
-template <int STAGES>
 struct PairLayout {
-  static constexpr int kBBytes = 128 * kBK * 2;                // this CTA's <= 128 token rows
-  static constexpr int kA = 0;
-  static constexpr int kB = kA + STAGES * kABytes;
-  static constexpr int kEpi = kB + STAGES * kBBytes;
-  static constexpr int kBar = kEpi + kEpiBytes;                // 8-byte aligned
-  static constexpr int kNumBars = 2 * STAGES + 5;              // full, empty, tfull[2], tempty[2], fin
-  static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kTables = kMisc + 16;
-  static constexpr int kUnits = kTables + ((3 * (kMaxE + 1) + 8) * 4 + 7) / 8 * 8;
-  static constexpr int kEnd = kUnits + kMaxUnits * 8;
+  static constexpr int kHStride = kABytes + 128 * kBK * 2;     // heavy stage: A, 128 B rows
+  static constexpr int kHStrideL = kABytes + (kPairBNL / 2) * kBK * 2;   // 112 B rows
+  static constexpr int kLStride = kABytes + kLightBox * kBK * 2;         // light stage
+  static constexpr int kL = kPairStages * kHStrideL;           // light ring after the heavy one
+  static constexpr int kRing = (kL + kLightStages * kLStride) > kPairStages * kHStride
+                                   ? kL + kLightStages * kLStride
+                                   : kPairStages * kHStride;
+  static constexpr int kBar = kRing;
+  // heavy full/empty, light full/empty, and per pipeline tfull[2], tempty[2], fin
+  static constexpr int kNumBars = 2 * kPairStages + 2 * kLightStages + 2 * 5;
+  static constexpr int kMisc = kBar + kNumBars * 8;            // TMEM address, abort, heavy BN
+  static constexpr int kTables = kMisc + 16;   // off, unit offsets (heavy and light, both phases)
+  static constexpr int kTmpInts = 32;          // scan words (16 warps), epilogue flags
+  static constexpr int kUnits = kTables + ((5 * (kMaxE + 1) + kTmpInts) * 4 + 7) / 8 * 8;
+  static constexpr int kEnd = kUnits + 2 * kPairMaxUnits * 8;
+  static_assert(kL % 1024 == 0 && kLStride % 1024 == 0 && kHStrideL % 1024 == 0 &&
+                    kHStride % 1024 == 0,
+                "swizzle atoms");
   static_assert(kUnits % 8 == 0, "unit list alignment");
   static constexpr int kSmemBytes = kEnd + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
+static_assert(kPairBNL + kLightRows <= kPairBN && 2 * kPairBN <= kPairTmemCols,
+              "a light accumulator fits beside each narrowed heavy one");
 
-template <int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+// decode_unit with a token-block size chosen at run time.
+__device__ __forceinline__ Unit decode_unit_rows(int u, const int* off, const int* uoff0,
+                                                 const int* uoff1, int E, int BN) {
+  Unit r;
+  const int total0 = uoff0[E];
+  r.ph = (u < total0) ? 0 : 1;
+  if (r.ph) u -= total0;
+  const int* uo = r.ph ? uoff1 : uoff0;
+  int lo = 0, hi = E;  // uo[lo] <= u < uo[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (uo[mid] <= u) lo = mid;
+    else hi = mid;
+  }
+  r.e = lo;
+  r.ks = 0;
+  const int local = u - uo[lo];
+  const int m = off[lo + 1] - off[lo];
+  const int nb = (m + BN - 1) / BN;
+  r.mb = local / nb;
+  const int b = local - r.mb * nb;
+  r.row0 = off[lo] + b * BN;
+  r.rows = min(BN, off[lo + 1] - r.row0);
+  return r;
+}
+
+// Exclusive prefix sum over the kPairThreads threads of a CTA (s_tmp: 16 ints).
+__device__ __forceinline__ int pair_scan_excl(int v, int* s_tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) s_tmp[warp] = inc;
+  __syncthreads();
+  int pre = 0, tot = 0;
+  for (int w = 0; w < kPairThreads / 32; ++w) {
+    if (w < warp) pre += s_tmp[w];
+    tot += s_tmp[w];
+  }
+  __syncthreads();
+  *total = tot;
+  return pre + inc - v;
+}
+
+// One pipeline of the pair kernel as its roles see it.
+struct PairPipe {
+  uint8_t* ring;           // stage s: A at ring + s * stride, B kABytes after it
+  int stride;
+  int stages;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* tfull;
+  uint64_t* tempty;
+  uint64_t* fin;
+  uint32_t lead_full0;     // full[0] of the even CTA (cluster address)
+  uint32_t lead_tempty0;   // tempty[0] of the even CTA
+  const uint2* units;      // this pair's units, or null: decoded on the fly
+  const int* off;
+  const int* uoff0;
+  const int* uoff1;
+  int E;
+  int bn;                  // token rows per unit
+  int total;               // units of the pipeline (both phases)
+  uint32_t acc_base;       // accumulator a at TMEM column acc_base + a * kPairBN
+  int epi_warps;           // epilogue warps per CTA (a multiple of 4)
+  int bar_id;              // named barrier of the epilogue group
+  int* flag;               // the epilogue group's broadcast word
+};
+
+__device__ __forceinline__ Unit pipe_unit(const PairPipe& p, int u, int ui) {
+  return p.units != nullptr ? unpack_unit(p.units[ui])
+                            : decode_unit_rows(u, p.off, p.uoff0, p.uoff1, p.E, p.bn);
+}
+
+// TMA producer of one pipeline in one CTA: this CTA's weight block and token half.
+__device__ __forceinline__ void pair_producer(const PairPipe& p, const GemmArgs& args,
+                                              const CUtensorMap* tmA0, const CUtensorMap* tmA1,
+                                              const CUtensorMap* tmW0, const CUtensorMap* tmW1,
+                                              int wide_rows, const CUtensorMap* tmS0,
+                                              const CUtensorMap* tmS1, int pair, int npairs,
+                                              uint32_t rank, volatile int* s_abort) {
+  const uint64_t pol_w_reused = l2_policy_evict_normal();
+  const uint64_t pol_w_once = l2_policy_evict_first();
+  const uint64_t pol_x = l2_policy_evict_last();
+  int stage = 0;
+  uint32_t par = 0;
+  uint32_t issued_mask = 0, issued_par = 0;
+  bool ok = true;
+  for (int u = pair, ui = 0; u < p.total && ok; u += npairs, ++ui) {
+    const Unit t = pipe_unit(p, u, ui);
+    const int m = p.off[t.e + 1] - p.off[t.e];
+    if (t.ph == 1 && args.done != nullptr) {
+      // the down projection reads h of this expert's gate/up units (same pipeline)
+      const int need = ((m + p.bn - 1) / p.bn) * (args.MW[0] / kBM);
+      if (!wait_counter(args.done + t.e, need, s_abort)) {
+        ok = false;
+        break;
+      }
+      fence_proxy_async_global();
+    }
+    const int half = ((t.rows + 15) & ~15) >> 1;          // this CTA's B rows (N / 2)
+    const bool thin = half <= kPairBoxS;
+    const CUtensorMap* ta = t.ph ? tmA1 : tmA0;
+    const CUtensorMap* tbm = thin ? (t.ph ? tmS1 : tmS0) : (t.ph ? tmW1 : tmW0);
+    const uint32_t bytes = kABytes + (thin ? kPairBoxS : wide_rows) * kBK * 2;
+    const int arow = t.e * args.MW[t.ph] + (2 * t.mb + static_cast<int>(rank)) * kBM;
+    const int brow = t.row0 + static_cast<int>(rank) * half;
+    const int nk = args.K[t.ph] / kBK;
+    // weight tiles of an expert with one token block are read once: stream them
+    const uint64_t pol_w = m <= p.bn ? pol_w_once : pol_w_reused;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!mbar_wait(&p.empty[stage], par ^ 1u, s_abort)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&p.full[stage], bytes);
+      uint8_t* sa = p.ring + stage * p.stride;
+      tma_load_2d(sa, ta, &p.full[stage], kb * kBK, arow, pol_w);
+      tma_load_2d(sa + kABytes, tbm, &p.full[stage], kb * kBK, brow, pol_x);
+      issued_mask |= 1u << stage;
+      issued_par = (issued_par & ~(1u << stage)) | (par << stage);
+      if (++stage == p.stages) {
+        stage = 0;
+        par ^= 1u;
+      }
+    }
+  }
+  if (ok) {
+    // every stage released by the pair's MMAs: no multicast commit is still on
+    // its way to this CTA's barriers when it exits
+    for (int i = 0; i < p.stages; ++i) {
+      if (!mbar_wait(&p.empty[stage], par ^ 1u, s_abort)) {
+        ok = false;
+        break;
+      }
+      if (++stage == p.stages) {
+        stage = 0;
+        par ^= 1u;
+      }
+    }
+  }
+  if (!ok) {
+    *s_abort = 1;
+    flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+    for (int s = 0; s < p.stages; ++s)
+      if ((issued_mask >> s) & 1u) mbar_wait(&p.full[s], (issued_par >> s) & 1u, nullptr);
+  }
+}
+
+// Odd CTA: passes each of its landed stages on to the even CTA's `full` barrier.
+__device__ __forceinline__ void pair_forwarder(const PairPipe& p, const GemmArgs& args, int pair,
+                                               int npairs, volatile int* s_abort) {
+  int stage = 0;
+  uint32_t par = 0;
+  bool ok = true;
+  for (int u = pair, ui = 0; u < p.total && ok; u += npairs, ++ui) {
+    const Unit t = pipe_unit(p, u, ui);
+    const int nk = args.K[t.ph] / kBK;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!mbar_wait(&p.full[stage], par, s_abort)) {
+        ok = false;
+        break;
+      }
+      // the stage's bytes are in this CTA's shared memory (observed above)
+      mbar_arrive_cluster_relaxed(p.lead_full0 + stage * 8);
+      if (++stage == p.stages) {
+        stage = 0;
+        par ^= 1u;
+      }
+    }
+  }
+  if (!ok) {
+    *s_abort = 1;
+    flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+  }
+}
+
+// Even CTA: the pipeline's MMA issuer.
+__device__ __forceinline__ void pair_mma(const PairPipe& p, const GemmArgs& args, uint32_t tmem_base,
+                                         int pair, int npairs, volatile int* s_abort) {
+  int stage = 0, acc = 0;
+  uint32_t par = 0, apar = 0;
+  bool ok = true;
+  for (int u = pair, ui = 0; u < p.total && ok; u += npairs, ++ui) {
+    const Unit t = pipe_unit(p, u, ui);
+    const int n = (t.rows + 15) & ~15;
+    const uint32_t idesc = idesc_bf16_f32(2 * kBM, n);
+    // both CTAs' epilogues have drained this accumulator
+    if (!mbar_wait_cluster(&p.tempty[acc], apar ^ 1u, s_abort)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after_sync();
+    const uint32_t d = tmem_base + p.acc_base + static_cast<uint32_t>(acc * kPairBN);
+    const int nk = args.K[t.ph] / kBK;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!mbar_wait_cluster(&p.full[stage], par, s_abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t a0 = smem_u32(p.ring + stage * p.stride);
+      const uint32_t b0 = a0 + kABytes;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        tc_mma_pair_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
+                         (kb | kk) ? 1u : 0u);
+      tc_commit_pair(&p.empty[stage], 3);
+      if (++stage == p.stages) {
+        stage = 0;
+        par ^= 1u;
+      }
+    }
+    if (!ok) break;
+    tc_commit_pair(&p.tfull[acc], 3);
+    acc ^= 1;
+    if (acc == 0) apar ^= 1u;
+  }
+  if (ok) {
+    // the odd CTA's last remote tempty arrivals land before this CTA may exit
+    for (int i = 0; i < 2; ++i) {
+      if (!mbar_wait_cluster(&p.tempty[acc], apar ^ 1u, s_abort)) {
+        ok = false;
+        break;
+      }
+      acc ^= 1;
+      if (acc == 0) apar ^= 1u;
+    }
+  }
+  if (!ok) {
+    *s_abort = 1;
+    flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+    tc_commit_pair(p.fin, 1);  // drain this thread's outstanding MMAs before TMEM is freed
+    mbar_wait(p.fin, 0, nullptr);
+  }
+}
+
+// One 32-token chunk of an accumulator, stored from registers.  The warp reads TMEM
+// lane quarter q of the CTA's 128-row weight block t.mb.  Gate/up (epi 0): lanes 0-15
+// hold the gate rows of features 16q .. 16q + 15 of the block and lanes 16-31 the
+// matching up rows (the packed w13 layout), so one shuffle pairs them and lanes 0-15
+// finish tokens c0 .. c0 + 15, lanes 16-31 tokens c0 + 16 .. c0 + 31, each for feature
+// 16q + (lane & 15).  Down (epi 1): lane l holds output feature 32q + l of the block.
+// In both, a second shuffle between neighbouring lanes gives each lane two adjacent
+// features of one token, so every store writes 4 bytes and one warp-wide store covers
+// whole 32- or 64-byte row segments of two tokens.
+__device__ __forceinline__ void pair_store_chunk(const GemmArgs& args, const Unit& t,
+                                                 uint32_t tbase, int c0, int q, int lane) {
+  uint16_t* out = args.out[t.ph];
+  const int ld = args.ld[t.ph];
+  const bool odd = (lane & 1) != 0;
+  float v[32];
+  tmem_ld_32x32b_x32(tbase + c0, v);
+  if (args.epi[t.ph] == 0) {
+    const bool lo = lane < 16;
+    float h[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float send = lo ? v[16 + j] : v[j];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+      const float g = lo ? v[j] : recv;
+      const float up = lo ? recv : v[16 + j];
+      h[j] = g / (1.0f + __expf(-g)) * up;
+    }
+    // even lane f: features (f, f + 1) of token j; odd lane: (f - 1, f) of token j + 1
+    uint16_t* col = out + (size_t)t.mb * 64 + q * 16 + (lane & 14);
+    const int tb = c0 + (lo ? 0 : 16);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const float x = __shfl_xor_sync(0xffffffffu, odd ? h[j] : h[j + 1], 1);
+      const int tok = tb + j + (odd ? 1 : 0);
+      const uint32_t pk = odd ? (uint32_t)f2bf(x) | ((uint32_t)f2bf(h[j + 1]) << 16)
+                              : (uint32_t)f2bf(h[j]) | ((uint32_t)f2bf(x) << 16);
+      if (tok < t.rows) *reinterpret_cast<uint32_t*>(col + (size_t)(t.row0 + tok) * ld) = pk;
+    }
+  } else {
+    uint16_t* col = out + (size_t)t.mb * kBM + q * 32 + (lane & 30);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float x = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 1], 1);
+      const int tok = c0 + j + (odd ? 1 : 0);
+      const uint32_t pk = odd ? (uint32_t)f2bf(x) | ((uint32_t)f2bf(v[j + 1]) << 16)
+                              : (uint32_t)f2bf(v[j]) | ((uint32_t)f2bf(x) << 16);
+      if (tok < t.rows) *reinterpret_cast<uint32_t*>(col + (size_t)(t.row0 + tok) * ld) = pk;
+    }
+  }
+}
+
+// An epilogue group: p.epi_warps warps per CTA, warp ew taking TMEM lane quarter
+// ew % 4 and every (p.epi_warps / 4)-th 32-token chunk from chunk ew / 4.
+__device__ __forceinline__ void pair_epilogue(const PairPipe& p, const GemmArgs& args,
+                                              uint32_t tmem_base, int pair, int npairs,
+                                              uint32_t rank, int ew, int lane,
+                                              volatile int* s_abort) {
+  const bool leader = rank == 0;
+  const int q = ew & 3, g = ew >> 2, ng = p.epi_warps >> 2;
+  const int nthr = 32 * p.epi_warps;
+  const int et = ew * 32 + lane;
+  int acc = 0;
+  uint32_t apar = 0;
+  for (int u = pair, ui = 0; u < p.total; u += npairs, ++ui) {
+    Unit t = pipe_unit(p, u, ui);
+    t.mb = 2 * t.mb + static_cast<int>(rank);   // this CTA's 128-row weight block
+    if (et == 0) p.flag[0] = mbar_wait(&p.tfull[acc], apar, s_abort) ? 1 : 0;
+    named_bar_sync(p.bar_id, nthr);
+    const int ok = p.flag[0];
+    named_bar_sync(p.bar_id, nthr);
+    if (!ok) {
+      if (et == 0) {
+        *s_abort = 1;
+        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+      }
+      break;
+    }
+    tc_fence_after_sync();
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + p.acc_base +
+                           static_cast<uint32_t>(acc * kPairBN);
+    for (int c0 = 32 * g; c0 < t.rows; c0 += 32 * ng) pair_store_chunk(args, t, tbase, c0, q, lane);
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) {
+      if (leader) mbar_arrive(&p.tempty[acc]);
+      else mbar_arrive_cluster(p.lead_tempty0 + acc * 8);
+    }
+    if (t.ph == 0 && args.done != nullptr) {
+      // this unit's h rows are read by TMA (the async proxy) in the down projection;
+      // after the group's barrier, one release covers every thread's stores
+      fence_proxy_async_global();
+      named_bar_sync(p.bar_id, nthr);
+      if (et == 0) red_release_add_gpu(args.done + t.e, 1);
+    }
+    acc ^= 1;
+    if (acc == 0) apar ^= 1u;
+  }
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
-                             const __grid_constant__ CUtensorMap tmB0,
                              const __grid_constant__ CUtensorMap tmA1,
+                             const __grid_constant__ CUtensorMap tmB0,   // 128-row B boxes
                              const __grid_constant__ CUtensorMap tmB1,
-                             const __grid_constant__ CUtensorMap tmS0,   // kPairBoxS-row B boxes
+                             const __grid_constant__ CUtensorMap tmH0,   // 112-row B boxes
+                             const __grid_constant__ CUtensorMap tmH1,
+                             const __grid_constant__ CUtensorMap tmS0,   // 16-row B boxes
                              const __grid_constant__ CUtensorMap tmS1, const GemmArgs args) {
-  using L = PairLayout<STAGES>;
+  using L = PairLayout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem + L::kA;
-  uint8_t* sB = smem + L::kB;
-  uint8_t* sEpi = smem + L::kEpi;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;     // waited on in the even CTA only
-  uint64_t* fin = tempty + 2;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* h_full = bars;
+  uint64_t* h_empty = h_full + kPairStages;
+  uint64_t* l_full = h_empty + kPairStages;
+  uint64_t* l_empty = l_full + kLightStages;
+  uint64_t* h_tfull = l_empty + kLightStages;   // [2]
+  uint64_t* h_tempty = h_tfull + 2;             // [2], waited on in the even CTA only
+  uint64_t* l_tfull = h_tempty + 2;             // [2]
+  uint64_t* l_tempty = l_tfull + 2;             // [2], waited on in the even CTA only
+  uint64_t* h_fin = l_tempty + 2;
+  uint64_t* l_fin = h_fin + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  int* s_hbn = reinterpret_cast<int*>(smem + L::kMisc + 8);
   int* s_off = reinterpret_cast<int*>(smem + L::kTables);
-  int* s_uoff0 = s_off + (kMaxE + 1);
-  int* s_uoff1 = s_uoff0 + (kMaxE + 1);
-  int* s_tmp = s_uoff1 + (kMaxE + 1);
-  uint2* s_units = reinterpret_cast<uint2*>(smem + L::kUnits);
+  int* s_uh0 = s_off + (kMaxE + 1);
+  int* s_uh1 = s_uh0 + (kMaxE + 1);
+  int* s_ul0 = s_uh1 + (kMaxE + 1);
+  int* s_ul1 = s_ul0 + (kMaxE + 1);
+  int* s_tmp = s_ul1 + (kMaxE + 1);   // 16 scan words, then the two epilogue flags
+  uint2* s_hunits = reinterpret_cast<uint2*>(smem + L::kUnits);
+  uint2* s_lunits = s_hunits + kPairMaxUnits;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = args.E;
@@ -606,24 +986,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      // even CTA: its own producer + the odd CTA's forwarded arrival
-      mbar_init(&full[s], leader ? 2 : 1);
-      mbar_init(&empty[s], 1);
+    // even CTA: its own producer + the odd CTA's forwarded arrival
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&h_full[s], leader ? 2 : 1);
+      mbar_init(&h_empty[s], 1);
+    }
+    for (int s = 0; s < kLightStages; ++s) {
+      mbar_init(&l_full[s], leader ? 2 : 1);
+      mbar_init(&l_empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 8);   // four epilogue warps in each CTA
+      mbar_init(&h_tfull[a], 1);
+      mbar_init(&h_tempty[a], 2 * kHeavyEpiWarps);   // the group's warps in both CTAs
+      mbar_init(&l_tfull[a], 1);
+      mbar_init(&l_tempty[a], 2 * kLightEpiWarps);
     }
-    mbar_init(fin, 1);
+    mbar_init(h_fin, 1);
+    mbar_init(l_fin, 1);
     *s_abort = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA0);
-    tma_prefetch_desc(&tmB0);
     tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB0);
     tma_prefetch_desc(&tmB1);
+    tma_prefetch_desc(&tmH0);
+    tma_prefetch_desc(&tmH1);
     tma_prefetch_desc(&tmS0);
     tma_prefetch_desc(&tmS1);
   }
@@ -631,261 +1020,125 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(s_tmem, kPairTmemCols);
     tmem_relinquish_pair();
   }
-  for (int i = tid; i <= E; i += kThreads) s_off[i] = args.offsets[i];
+  for (int i = tid; i <= E; i += kPairThreads) s_off[i] = args.offsets[i];
   __syncthreads();
 
-  // Pair units per expert and their exclusive prefix, per phase.
+  // Units per expert and pipeline, and their exclusive prefix per phase.
   {
-    int u[2] = {0, 0};
+    const int m = tid < E ? s_off[tid + 1] - s_off[tid] : 0;
+    const bool light = m > 0 && m <= kLightRows;
+    int n_light = 0;
+    pair_scan_excl(light ? 1 : 0, s_tmp, &n_light);
+    const int hb = n_light > 0 ? kPairBNL : kPairBN;
+    if (tid == 0) *s_hbn = hb;
+    int uh[2] = {0, 0}, ul[2] = {0, 0};
     if (tid < E) {
-      const int m = s_off[tid + 1] - s_off[tid];
-      const int nb = (m + kPairBN - 1) / kPairBN;
-      u[0] = args.active[0] ? nb * (args.MW[0] / (2 * kBM)) : 0;
-      u[1] = args.active[1] ? nb * (args.MW[1] / (2 * kBM)) : 0;
-    }
-    for (int p = 0; p < 2; ++p) {
-      int inc = u[p];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
+      const int nb = light ? 0 : (m + hb - 1) / hb;
+      for (int ph = 0; ph < 2; ++ph) {
+        const int pb = args.active[ph] ? args.MW[ph] / (2 * kBM) : 0;
+        uh[ph] = nb * pb;
+        ul[ph] = light ? pb : 0;
       }
-      if (lane == 31) s_tmp[warp] = inc;
-      __syncthreads();
-      int pre = 0, tot = 0;
-      for (int w = 0; w < kThreads / 32; ++w) {
-        if (w < warp) pre += s_tmp[w];
-        tot += s_tmp[w];
-      }
-      int* dst = p ? s_uoff1 : s_uoff0;
-      if (tid < E) dst[tid] = pre + inc - u[p];
-      if (tid == 0) dst[E] = tot;
-      __syncthreads();
     }
+    int* dst[4] = {s_uh0, s_uh1, s_ul0, s_ul1};
+    const int val[4] = {uh[0], uh[1], ul[0], ul[1]};
+    for (int i = 0; i < 4; ++i) {
+      int tot = 0;
+      const int pre = pair_scan_excl(val[i], s_tmp, &tot);
+      if (tid < E) dst[i][tid] = pre;
+      if (tid == 0) dst[i][E] = tot;
+    }
+    __syncthreads();
   }
   tc_fence_after_sync();
   // both CTAs' barriers are initialised and TMEM allocated before any remote arrive
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *s_tmem;
-  Tables tb;
-  tb.off = s_off;
-  tb.uoff[0] = s_uoff0;
-  tb.uoff[1] = s_uoff1;
-  tb.ksplit[0] = 1;
-  tb.ksplit[1] = 1;
-  tb.E = E;
-  const int total = s_uoff0[E] + s_uoff1[E];
-  const int my_units = pair < total ? (total - pair + npairs - 1) / npairs : 0;
-  const bool use_list = my_units <= kMaxUnits;   // the same in every thread of the cluster
-  if (use_list) {
-    for (int i = tid; i < my_units; i += kThreads)
-      s_units[i] = pack_unit(decode_unit<kPairBN>(pair + i * npairs, tb));
-    __syncthreads();
-  }
-  const uint32_t lead_full0 = mapa_shared(smem_u32(&full[0]), 0);
-  const uint32_t lead_tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
+  const int hb = *s_hbn;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------ TMA producer --
-      const uint64_t pol_w_reused = l2_policy_evict_normal();
-      const uint64_t pol_w_once = l2_policy_evict_first();
-      const uint64_t pol_x = l2_policy_evict_last();
-      int stage = 0;
-      uint32_t par = 0;
-      uint32_t issued_mask = 0, issued_par = 0;
-      bool ok = true;
-      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
-        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kPairBN>(u, tb);
-        if (t.ph == 1 && args.done != nullptr) {
-          const int m = s_off[t.e + 1] - s_off[t.e];
-          const int need = ((m + kPairBN - 1) / kPairBN) * (args.MW[0] / kBM);
-          if (!wait_counter(args.done + t.e, need, s_abort)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_global();
-        }
-        const int half = ((t.rows + 15) & ~15) >> 1;        // this CTA's B rows (N / 2)
-        const bool small = half <= kPairBoxS;
-        const CUtensorMap* ta = t.ph ? &tmA1 : &tmA0;
-        const CUtensorMap* tbm = small ? (t.ph ? &tmS1 : &tmS0) : (t.ph ? &tmB1 : &tmB0);
-        const uint32_t bytes = kABytes + (small ? kPairBoxS : 128) * kBK * 2;
-        const int arow = t.e * args.MW[t.ph] + (2 * t.mb + static_cast<int>(rank)) * kBM;
-        const int brow = t.row0 + static_cast<int>(rank) * half;
-        const int nk = args.K[t.ph] / kBK;
-        // weight tiles of an expert with one token block are read once: stream them
-        const uint64_t pol_w = (s_off[t.e + 1] - s_off[t.e]) <= kPairBN ? pol_w_once : pol_w_reused;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sA + stage * kABytes, ta, &full[stage], kb * kBK, arow, pol_w);
-          tma_load_2d(sB + stage * L::kBBytes, tbm, &full[stage], kb * kBK, brow, pol_x);
-          issued_mask |= 1u << stage;
-          issued_par = (issued_par & ~(1u << stage)) | (par << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            par ^= 1u;
-          }
-        }
-      }
-      if (ok) {
-        // every stage released by the pair's MMAs: no multicast commit is still on
-        // its way to this CTA's barriers when it exits
-        for (int i = 0; i < STAGES; ++i) {
-          if (!mbar_wait(&empty[stage], par ^ 1u, s_abort)) {
-            ok = false;
-            break;
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            par ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        *s_abort = 1;
-        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued_mask >> s) & 1u) mbar_wait(&full[s], (issued_par >> s) & 1u, nullptr);
-      }
-    }
-  } else if (warp == 3) {
-    if (lane == 0 && !leader) {
-      // ------------------------------------- odd CTA: stage forwarder --
-      int stage = 0;
-      uint32_t par = 0;
-      bool ok = true;
-      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
-        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kPairBN>(u, tb);
-        const int nk = args.K[t.ph] / kBK;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&full[stage], par, s_abort)) {
-            ok = false;
-            break;
-          }
-          // the stage's bytes are in this CTA's shared memory (observed above)
-          mbar_arrive_cluster_relaxed(lead_full0 + stage * 8);
-          if (++stage == STAGES) {
-            stage = 0;
-            par ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        *s_abort = 1;
-        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ------------------------------------------- even CTA: MMA issuer --
-      int stage = 0, acc = 0;
-      uint32_t par = 0, apar = 0;
-      bool ok = true;
-      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
-        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kPairBN>(u, tb);
-        const int n = (t.rows + 15) & ~15;
-        const uint32_t idesc = idesc_bf16_f32(2 * kBM, n);
-        // both CTAs' epilogues have drained this accumulator
-        if (!mbar_wait_cluster(&tempty[acc], apar ^ 1u, s_abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairBN);
-        const int nk = args.K[t.ph] / kBK;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_cluster(&full[stage], par, s_abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t a0 = smem_u32(sA + stage * kABytes);
-          const uint32_t b0 = smem_u32(sB + stage * L::kBBytes);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_pair_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32),
-                             idesc, (kb | kk) ? 1u : 0u);
-          tc_commit_pair(&empty[stage], 3);
-          if (++stage == STAGES) {
-            stage = 0;
-            par ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit_pair(&tfull[acc], 3);
-        acc ^= 1;
-        if (acc == 0) apar ^= 1u;
-      }
-      if (ok) {
-        // the odd CTA's last remote tempty arrivals land before this CTA may exit
-        for (int i = 0; i < 2; ++i) {
-          if (!mbar_wait_cluster(&tempty[acc], apar ^ 1u, s_abort)) {
-            ok = false;
-            break;
-          }
-          acc ^= 1;
-          if (acc == 0) apar ^= 1u;
-        }
-      }
-      if (!ok) {
-        *s_abort = 1;
-        flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-        tc_commit_pair(fin, 1);  // drain this thread's outstanding MMAs before TMEM is freed
-        mbar_wait(fin, 0, nullptr);
-      }
-    }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ epilogue --
-    const int q = warp & 3;
-    const int et = tid - 128;
-    int* s_flag = s_tmp;
-    int acc = 0;
-    uint32_t apar = 0;
-    for (int u = pair, ui = 0; u < total; u += npairs, ++ui) {
-      Unit t = use_list ? unpack_unit(s_units[ui]) : decode_unit<kPairBN>(u, tb);
-      t.mb = 2 * t.mb + static_cast<int>(rank);   // this CTA's 128-row weight block
-      if (et == 0) s_flag[0] = mbar_wait(&tfull[acc], apar, s_abort) ? 1 : 0;
-      named_bar_sync(1, 128);
-      const int ok = s_flag[0];
-      named_bar_sync(1, 128);
-      if (!ok) {
-        if (et == 0) {
-          *s_abort = 1;
-          flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-        }
-        break;
-      }
-      tc_fence_after_sync();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * kPairBN);
-      epilogue_tile(args, t, tbase, sEpi, q, lane);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(&tempty[acc]);
-        else mbar_arrive_cluster(lead_tempty0 + acc * 8);
-      }
-      if (t.ph == 0 && args.done != nullptr) {
-        __threadfence();
-        fence_proxy_async_global();
-        named_bar_sync(1, 128);
-        if (et == 0) red_release_add_gpu(args.done + t.e, 1);
-      }
-      acc ^= 1;
-      if (acc == 0) apar ^= 1u;
-    }
+  PairPipe hp, lp;
+  hp.ring = smem;
+  hp.stride = hb == kPairBN ? L::kHStride : L::kHStrideL;
+  hp.stages = kPairStages;
+  hp.full = h_full;
+  hp.empty = h_empty;
+  hp.tfull = h_tfull;
+  hp.tempty = h_tempty;
+  hp.fin = h_fin;
+  hp.lead_full0 = mapa_shared(smem_u32(&h_full[0]), 0);
+  hp.lead_tempty0 = mapa_shared(smem_u32(&h_tempty[0]), 0);
+  hp.off = s_off;
+  hp.uoff0 = s_uh0;
+  hp.uoff1 = s_uh1;
+  hp.E = E;
+  hp.bn = hb;
+  hp.total = s_uh0[E] + s_uh1[E];
+  hp.acc_base = 0;                  // columns 0 and 256
+  hp.epi_warps = kHeavyEpiWarps;
+  hp.bar_id = 1;
+  hp.flag = s_tmp + 16;
+
+  lp.ring = smem + L::kL;
+  lp.stride = L::kLStride;
+  lp.stages = kLightStages;
+  lp.full = l_full;
+  lp.empty = l_empty;
+  lp.tfull = l_tfull;
+  lp.tempty = l_tempty;
+  lp.fin = l_fin;
+  lp.lead_full0 = mapa_shared(smem_u32(&l_full[0]), 0);
+  lp.lead_tempty0 = mapa_shared(smem_u32(&l_tempty[0]), 0);
+  lp.off = s_off;
+  lp.uoff0 = s_ul0;
+  lp.uoff1 = s_ul1;
+  lp.E = E;
+  lp.bn = kLightRows;
+  lp.total = s_ul0[E] + s_ul1[E];
+  lp.acc_base = kPairBNL;           // columns 224 and 480
+  lp.epi_warps = kLightEpiWarps;
+  lp.bar_id = 2;
+  lp.flag = s_tmp + 17;
+
+  // Each pair's units of both lists, decoded once (the same in every thread).
+  const int h_my = pair < hp.total ? (hp.total - pair + npairs - 1) / npairs : 0;
+  const int l_my = pair < lp.total ? (lp.total - pair + npairs - 1) / npairs : 0;
+  hp.units = h_my <= kPairMaxUnits ? s_hunits : nullptr;
+  lp.units = l_my <= kPairMaxUnits ? s_lunits : nullptr;
+  if (hp.units != nullptr)
+    for (int i = tid; i < h_my; i += kPairThreads)
+      s_hunits[i] = pack_unit(decode_unit_rows(pair + i * npairs, s_off, s_uh0, s_uh1, E, hp.bn));
+  if (lp.units != nullptr)
+    for (int i = tid; i < l_my; i += kPairThreads)
+      s_lunits[i] = pack_unit(decode_unit_rows(pair + i * npairs, s_off, s_ul0, s_ul1, E, lp.bn));
+  __syncthreads();
+
+  const CUtensorMap* hw0 = hb == kPairBN ? &tmB0 : &tmH0;
+  const CUtensorMap* hw1 = hb == kPairBN ? &tmB1 : &tmH1;
+  if (lane == 0 && warp == 0) {
+    pair_producer(hp, args, &tmA0, &tmA1, hw0, hw1, hb / 2, &tmS0, &tmS1, pair, npairs, rank,
+                  s_abort);
+  } else if (lane == 0 && warp == 2) {
+    pair_producer(lp, args, &tmA0, &tmA1, &tmS0, &tmS1, kLightBox, &tmS0, &tmS1, pair, npairs,
+                  rank, s_abort);
+  } else if (lane == 0 && warp == 1) {
+    if (leader) pair_mma(hp, args, tmem_base, pair, npairs, s_abort);
+    else pair_forwarder(lp, args, pair, npairs, s_abort);
+  } else if (lane == 0 && warp == 3) {
+    if (leader) pair_mma(lp, args, tmem_base, pair, npairs, s_abort);
+    else pair_forwarder(hp, args, pair, npairs, s_abort);
+  } else if (warp >= 4 && warp < 4 + kHeavyEpiWarps) {
+    pair_epilogue(hp, args, tmem_base, pair, npairs, rank, warp - 4, lane, s_abort);
+  } else if (warp >= 4 + kHeavyEpiWarps) {
+    pair_epilogue(lp, args, tmem_base, pair, npairs, rank, warp - 4 - kHeavyEpiWarps, lane,
+                  s_abort);
   }
 
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync_all();
   if (warp == 2) {
+    __syncwarp();   // lane 0 ran the light producer: the warp is converged for dealloc
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem_base, kPairTmemCols);
   }
@@ -989,10 +1242,9 @@ cudaError_t launch_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_
                             a);
 }
 
-template <int STAGES>
 cudaError_t launch_pair_impl(const GemmPhase* ph0, const GemmPhase* ph1, const int32_t* offsets,
                              int E, int P, int* done, int* status, cudaStream_t s) {
-  using L = PairLayout<STAGES>;
+  using L = PairLayout;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -1002,7 +1254,7 @@ cudaError_t launch_pair_impl(const GemmPhase* ph0, const GemmPhase* ph1, const i
     std::lock_guard<std::mutex> lk(mu);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-      err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<STAGES>,
+      err = cudaFuncSetAttribute(grouped_gemm_pair_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
       if (err != cudaSuccess) return err;
       attr_set[dev] = true;
@@ -1015,7 +1267,9 @@ cudaError_t launch_pair_impl(const GemmPhase* ph0, const GemmPhase* ph1, const i
   a.status = status;
   a.stall_stage = -1;
   a.wait_ns = kWaitLimitNs;
-  CUtensorMap tm[6];
+  // A0, A1, then per phase the B boxes of 128 rows (256-token units), 112 rows
+  // (224-token units) and kPairBoxS rows (thin and light units)
+  CUtensorMap tm[8];
   const GemmPhase* phs[2] = {ph0, ph1};
   for (int p = 0; p < 2; ++p) {
     const GemmPhase* g = phs[p] ? phs[p] : (ph0 ? ph0 : ph1);
@@ -1026,15 +1280,18 @@ cudaError_t launch_pair_impl(const GemmPhase* ph0, const GemmPhase* ph1, const i
     a.epi[p] = g->epi;
     a.ksplit[p] = 1;
     a.out[p] = g->out;
-    if (!encode_tmap_2d_bf16(&tm[2 * p], g->A_weights, (uint64_t)g->K, (uint64_t)E * g->MW, kBK,
+    if (!encode_tmap_2d_bf16(&tm[p], g->A_weights, (uint64_t)g->K, (uint64_t)E * g->MW, kBK,
                              kBM) ||
-        !encode_tmap_2d_bf16(&tm[2 * p + 1], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK, 128) ||
-        !encode_tmap_2d_bf16(&tm[4 + p], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK, kPairBoxS))
+        !encode_tmap_2d_bf16(&tm[2 + p], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK,
+                             kPairBN / 2) ||
+        !encode_tmap_2d_bf16(&tm[4 + p], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK,
+                             kPairBNL / 2) ||
+        !encode_tmap_2d_bf16(&tm[6 + p], g->B_act, (uint64_t)g->K, (uint64_t)P, kBK, kPairBoxS))
       return cudaErrorInvalidValue;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(device_sm_count() & ~1, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -1048,8 +1305,8 @@ cudaError_t launch_pair_impl(const GemmPhase* ph0, const GemmPhase* ph1, const i
   attr[1].val.cooperative = (a.done != nullptr && !pair_launch_noncooperative()) ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<STAGES>, tm[0], tm[1], tm[2], tm[3],
-                            tm[4], tm[5], a);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, tm[0], tm[1], tm[2], tm[3], tm[4],
+                            tm[5], tm[6], tm[7], a);
 }
 
 // The pair kernel takes plain expert GEMMs (SwiGLU or bf16 epilogue, whole K per
@@ -1081,7 +1338,7 @@ cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
   int dev = 0;
   if (pairable(ph0) && pairable(ph1) && device_sm_count() >= 2 && cudaGetDevice(&dev) == cudaSuccess &&
       dev >= 0 && dev < 64 && pair_state[dev].load() != 2) {
-    const cudaError_t err = launch_pair_impl<6>(ph0, ph1, offsets, E, P, done_counter, status, s);
+    const cudaError_t err = launch_pair_impl(ph0, ph1, offsets, E, P, done_counter, status, s);
     if (err == cudaSuccess) {
       pair_state[dev].store(1);
       return err;
