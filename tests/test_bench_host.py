@@ -184,3 +184,13 @@ def test_clock_samples_keep_the_loaded_ones():
     idle = bench.parse_clock_samples(text.splitlines()[0] + "\n" + text.splitlines()[4])
     assert idle["samples_under_load"] == 0 and idle["sm_mhz"] == 2070.0
     assert bench.parse_clock_samples("") is None
+
+
+def test_sustained_peak_is_read_when_present(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.sustained_bf16_peak() is None                    # no file
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6800, "bf16_tflops": 1900}')
+    assert bench.sustained_bf16_peak() is None                    # no sustained figure
+    (tmp_path / "MEASURED_PEAKS.json").write_text(
+        '{"hbm_gbs": 6800, "bf16_tflops": 1900, "bf16_tflops_sustained": 1700.5}')
+    assert bench.sustained_bf16_peak() == 1700.5
