@@ -133,6 +133,8 @@ def _gemm_case(cuda_dev, T, E, k, H, I, skew, seed):
     (1, 8, 8, 256, 128, None),         # 8 pairs, one per expert
     (600, 16, 4, 256, 192, 1.0),       # wide tiles, ragged, hot experts > 256 rows
     (300, 64, 8, 512, 64, 1.5),        # some empty experts, I = 64
+    (600, 16, 4, 256, 128, 1.5),       # CTA pairs, one projection a launch, light and heavy experts
+    (1024, 8, 2, 512, 256, None),      # CTA pairs without light experts (256-row token blocks)
 ])
 def test_grouped_gemms_match_oracle(cuda_dev, T, E, k, H, I, skew):
     rt, A, w13, down, w13p, downp, off = _gemm_case(cuda_dev, T, E, k, H, I, skew, seed=T + E + I)
