@@ -927,66 +927,8 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
   const int my_units = pair < total ? (total - pair + npairs - 1) / npairs : 0;
   const bool use_list = my_units <= S::kMaxUnits;   // the same in every thread of the cluster
   if (use_list) {
-    // The deal.  A unit that absorbs rows beyond 256 costs about a quarter more than
-    // one that does not, and an expert's units are neighbours in the unit list, so
-    // dealing that list round-robin gives some pairs many more absorbing units than
-    // others.  The units are instead dealt round-robin in class order: gate/up units
-    // that absorb rows, the other gate/up units, then the same two classes of down
-    // units (each class in list order), so every pair gets its share of each class.
-    // Gate/up units still come before down units in every pair.  Thread e places
-    // expert e's units of each class; position g of the class-ordered list is this
-    // pair's unit g / npairs when g % npairs == pair.
-    int cnt[4] = {0, 0, 0, 0}, nb = 0, m = 0;
-    bool tail = false;
-    if (tid < E) {
-      m = s_off[tid + 1] - s_off[tid];
-      nb = token_blocks<kBN, kTail>(m);
-      tail = nb > 0 && m - (nb - 1) * kBN > kBN;
-      for (int ph = 0; ph < 2; ++ph) {
-        const int pb = args.active[ph] ? args.MW[ph] / (2 * kBM) : 0;
-        cnt[2 * ph] = tail ? pb : 0;                 // absorbing units
-        cnt[2 * ph + 1] = nb * pb - cnt[2 * ph];     // the others
-      }
-    }
-    int base = 0;
-    for (int c = 0; c < 4; ++c) {
-      int inc = cnt[c];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-      }
-      if (lane == 31) s_tmp[warp] = inc;
-      __syncthreads();
-      int pre = 0, tot = 0;
-      for (int w = 0; w < S::kThreads / 32; ++w) {
-        if (w < warp) pre += s_tmp[w];
-        tot += s_tmp[w];
-      }
-      __syncthreads();
-      const int ph = c >> 1;
-      for (int i = 0; i < cnt[c]; ++i) {
-        const int g = base + pre + inc - cnt[c] + i;   // position in the class-ordered list
-        if (g % npairs != pair) continue;
-        Unit t;
-        t.ph = ph;
-        t.e = tid;
-        if ((c & 1) == 0) {        // absorbing: the last token block of weight block i
-          t.mb = i;
-          t.nb = nb - 1;
-        } else if (tail) {         // the other token blocks
-          t.mb = i / (nb - 1);
-          t.nb = i - t.mb * (nb - 1);
-        } else {
-          t.mb = i / nb;
-          t.nb = i - t.mb * nb;
-        }
-        t.row0 = s_poff[tid] + t.nb * kBN;
-        t.rows = t.nb == nb - 1 ? m - t.nb * kBN : kBN;
-        s_units[g / npairs] = pack_unit(t);
-      }
-      base += tot;
-    }
+    for (int i = tid; i < my_units; i += S::kThreads)
+      s_units[i] = pack_unit(decode_pair_unit(pair + i * npairs, tb));
     __syncthreads();
   }
   const uint32_t lead_full0 = mapa_shared(smem_u32(&full[0]), 0);
