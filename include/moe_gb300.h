@@ -429,6 +429,17 @@ MOE_API moe_status moe_set_gemm_events(void* ev_begin, void* ev_end);
  */
 MOE_API moe_status moe_debug_set_gemm_stall(int stage, long long wait_ns);
 
+/* Test aid: the CTA-pair grouped GEMM (prefill-size bf16 tiles) runs the experts
+ * with at most 32 rows on a second, light pipeline when, by its per-stage cost
+ * estimates, their weight streaming hides under the other experts' tensor work;
+ * else every expert runs on the one pipeline.  The choice is made on the device from
+ * the expert counts.  mode 0 restores that choice (the default), 1 uses the light
+ * pipeline whenever such experts exist, 2 never uses it.  It affects every later
+ * pair launch from any host thread; results agree in every mode.  Other modes:
+ * MOE_ERR_INVALID_ARG.
+ */
+MOE_API moe_status moe_debug_set_pair_light(int mode);
+
 #ifdef __cplusplus
 }
 #endif

@@ -105,6 +105,14 @@ def test_out_of_range_shapes_rejected_before_device_use(L):
     assert L.moe_packed_weight_bytes_mx4(8, 256, 128, 0) == 8 * 256 * 128     # 2I x H codes / 2
 
 
+def test_pair_light_hook_validates_on_the_host(L):
+    # host-only: sets the hook state, touches no device
+    assert L.moe_debug_set_pair_light(3) == 1                   # not a mode
+    assert L.moe_debug_set_pair_light(-1) == 1
+    assert L.moe_debug_set_pair_light(2) == 0
+    assert L.moe_debug_set_pair_light(0) == 0                   # automatic, the default
+
+
 def test_gemm_stall_hook_validates_on_the_host(L):
     # host-only: sets or clears the hook state, touches no device
     assert L.moe_debug_set_gemm_stall(3, 10) == 1               # wait limit below 1 us

@@ -97,24 +97,30 @@ def test_forward_limits(layers, T, E, k):
     _check_forward(cfg, inp, layer)
 
 
-@pytest.mark.parametrize("counts", [
-    [256, 257, 255, 512, 513, 33, 40, 254],  # no expert of <= 32 rows: 256-row blocks, both sides
-    [224, 225, 223, 448, 449, 1, 0, 32],     # 1 and 32 rows run light: 224-row heavy blocks
-    [1, 16, 17, 33, 255, 256, 480, 990],     # light 1-17; heavy halves of 17 to 112 rows, thin tails
+@pytest.mark.parametrize("counts,light", [
+    ([256, 257, 255, 512, 513, 33, 40, 254], 0),  # no expert of <= 32 rows: 256-row blocks
+    ([224, 225, 223, 448, 449, 1, 0, 32], 1),     # 1 and 32 rows run light: 224-row heavy blocks
+    ([224, 225, 223, 448, 449, 1, 0, 32], 2),     # the same experts all on the one pipeline
+    ([1, 16, 17, 33, 255, 256, 480, 990], 1),     # light 1-17; heavy halves of 17 to 112 rows
+    ([1, 16, 17, 33, 255, 256, 480, 990], 0),     # the kernel's own choice
 ])
-def test_forward_token_block_boundaries(layers, counts):
+def test_forward_token_block_boundaries(layers, counts, light):
     """Expert loads forced through designed logits onto both sides of the token
-    blocks of the CTA-pair GEMM: 256-row blocks when no expert has 32 rows or fewer,
-    224-row heavy blocks next to the light pipeline's experts (up to 32 rows, one
-    with a single row, one with none), and the thin boxes of units whose half block
-    has at most 16 rows."""
+    blocks of the CTA-pair GEMM: 256-row blocks when every expert runs on one
+    pipeline, 224-row heavy blocks next to the light pipeline's experts (up to 32
+    rows, one with a single row, one with none; the light pipeline forced on), and
+    the thin boxes of units whose half block has at most 16 rows."""
     k = 2
     T = sum(counts) // k
     cfg, inp, layer = layers("tiny", T=T, E=len(counts), k=k)
     lg = forced_topk_logits(counts, k, seed=7)
     x = inp["x"]
-    out, ids, w = layer(x, logits_override=torch.from_numpy(lg).to(x.device))
-    torch.cuda.synchronize()
+    moe.debug_set_pair_light(light)
+    try:
+        out, ids, w = layer(x, logits_override=torch.from_numpy(lg).to(x.device))
+        torch.cuda.synchronize()
+    finally:
+        moe.debug_set_pair_light(0)
     assert moe.get_device_status() == 0
     r_ids, r_w = O.gating_topk_softmax(lg, k)
     np.testing.assert_array_equal(np.bincount(r_ids.ravel(), minlength=cfg.E), counts)

@@ -41,5 +41,6 @@ from ._binding import (  # noqa: F401
     router_logits,
     set_gemm_events,
     debug_set_gemm_stall,
+    debug_set_pair_light,
 )
 from .workloads import CONFIGS, MoEConfig, make_inputs  # noqa: F401

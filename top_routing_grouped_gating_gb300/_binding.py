@@ -44,6 +44,7 @@ _SIGS = {
                              _vp, _vp, _c_size, _vp]),
     "moe_set_gemm_events": (_c_int, [_vp, _vp]),
     "moe_debug_set_gemm_stall": (_c_int, [_c_int, ctypes.c_longlong]),
+    "moe_debug_set_pair_light": (_c_int, [_c_int]),
     "moe_add_rmsnorm_cast": (_c_int, [_vp, _vp, _vp, _c_float, _c_int, _c_int, _vp, _vp, _vp, _vp]),
     "moe_init_routing_v2_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
     "moe_init_routing_v2": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp,
@@ -315,6 +316,12 @@ def set_gemm_events(ev_begin: Optional[torch.cuda.Event], ev_end: Optional[torch
     b = None if ev_begin is None else ev_begin.cuda_event
     e = None if ev_end is None else ev_end.cuda_event
     _check("moe_set_gemm_events", lib().moe_set_gemm_events(b, e))
+
+
+def debug_set_pair_light(mode: int) -> None:
+    """Test aid: 0 lets the CTA-pair GEMM choose its light pipeline on the device, 1
+    uses it whenever experts of at most 32 rows exist, 2 never."""
+    _check("moe_debug_set_pair_light", lib().moe_debug_set_pair_light(int(mode)))
 
 
 def debug_set_gemm_stall(stage: int, wait_ns: int = 2_000_000) -> None:

@@ -1108,6 +1108,12 @@ moe_status moe_forward_v2(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
   return MOE_OK;
 }
 
+moe_status moe_debug_set_pair_light(int mode) {
+  if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+  moe::set_pair_light(mode);
+  return MOE_OK;
+}
+
 moe_status moe_debug_set_gemm_stall(int stage, long long wait_ns) {
   if (stage >= 0 && (wait_ns < 1000 || wait_ns > 2000000000LL)) return MOE_ERR_INVALID_ARG;
   moe::set_gemm_stall(stage, static_cast<unsigned long long>(wait_ns));

@@ -73,6 +73,9 @@ struct GemmArgs {
   // off (the normal case); wait_ns is then the library-wide limit.
   int stall_stage;
   unsigned long long wait_ns;
+  // Pair kernel: 0 decides on the device whether experts of at most 32 rows run on
+  // the light pipeline; 1 runs them there whenever there are any; 2 never.
+  int light_mode;
 };
 
 template <int BN, int STAGES, int BOX>
@@ -1023,13 +1026,27 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   for (int i = tid; i <= E; i += kPairThreads) s_off[i] = args.offsets[i];
   __syncthreads();
 
-  // Units per expert and pipeline, and their exclusive prefix per phase.
+  // Units per expert and pipeline, and their exclusive prefix per phase.  The light
+  // pipeline pays off when the light experts' weight streaming can hide under the
+  // heavy units' tensor work; when light stages dominate (small skewed batches) its
+  // two-stage ring is slower than running every expert on the heavy pipeline.  Per
+  // stage (measured): ~1700 clocks on the light ring, ~690 on the heavy ring beside
+  // it (224-token units), ~660 on a heavy ring of its own (256-token units).
   {
     const int m = tid < E ? s_off[tid + 1] - s_off[tid] : 0;
-    const bool light = m > 0 && m <= kLightRows;
-    int n_light = 0;
-    pair_scan_excl(light ? 1 : 0, s_tmp, &n_light);
-    const int hb = n_light > 0 ? kPairBNL : kPairBN;
+    const bool small = m > 0 && m <= kLightRows;
+    int stg = 0;                                   // stages of one token block
+    for (int ph = 0; ph < 2; ++ph)
+      if (args.active[ph]) stg += args.MW[ph] / (2 * kBM) * (args.K[ph] / kBK);
+    int l_st = 0, h224 = 0, h256 = 0;
+    pair_scan_excl(small ? stg : 0, s_tmp, &l_st);
+    pair_scan_excl(small ? 0 : (m + kPairBNL - 1) / kPairBNL * stg, s_tmp, &h224);
+    pair_scan_excl((m + kPairBN - 1) / kPairBN * stg, s_tmp, &h256);
+    const long long t_split = 1700LL * l_st > 690LL * h224 ? 1700LL * l_st : 690LL * h224;
+    const bool with_light_run =
+        l_st > 0 && (args.light_mode == 1 || (args.light_mode == 0 && t_split < 660LL * h256));
+    const bool light = small && with_light_run;
+    const int hb = with_light_run ? kPairBNL : kPairBN;
     if (tid == 0) *s_hbn = hb;
     int uh[2] = {0, 0}, ul[2] = {0, 0};
     if (tid < E) {
@@ -1177,6 +1194,8 @@ __global__ void pack_down_kernel(const uint16_t* __restrict__ down, int H, int I
 
 // Test hook state (moe_debug_set_gemm_stall); read at each one-CTA launch.
 std::atomic<int> g_stall_stage{-1};
+// Test hook state (moe_debug_set_pair_light); read at each CTA-pair launch.
+std::atomic<int> g_pair_light{0};
 std::atomic<unsigned long long> g_stall_wait_ns{kWaitLimitNs};
 
 template <int BN, int STAGES, int BOX>
@@ -1267,6 +1286,7 @@ cudaError_t launch_pair_impl(const GemmPhase* ph0, const GemmPhase* ph1, const i
   a.status = status;
   a.stall_stage = -1;
   a.wait_ns = kWaitLimitNs;
+  a.light_mode = g_pair_light.load();
   // A0, A1, then per phase the B boxes of 128 rows (256-token units), 112 rows
   // (224-token units) and kPairBoxS rows (thin and light units)
   CUtensorMap tm[8];
@@ -1317,6 +1337,8 @@ bool pairable(const GemmPhase* g) {
 }
 
 }  // namespace
+
+void set_pair_light(int mode) { g_pair_light.store(mode); }
 
 void set_gemm_stall(int stage, unsigned long long wait_ns) {
   g_stall_wait_ns.store(stage >= 0 ? wait_ns : kWaitLimitNs);

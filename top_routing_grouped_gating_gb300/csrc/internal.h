@@ -111,6 +111,9 @@ cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
                                 int* done_counter, int* status, cudaStream_t s);
 // Test hook of the one-CTA grouped GEMM (moe_debug_set_gemm_stall); stage < 0: off.
 void set_gemm_stall(int stage, unsigned long long wait_ns);
+// Test hook of the CTA-pair grouped GEMM (moe_debug_set_pair_light): 0 automatic,
+// 1 light pipeline whenever experts of at most 32 rows exist, 2 never.
+void set_pair_light(int mode);
 cudaError_t launch_pack_w13(const uint16_t* w13, int E, int H, int I, uint16_t* out,
                             cudaStream_t s);
 cudaError_t launch_pack_down(const uint16_t* down, int E, int H, int I, uint16_t* out,
