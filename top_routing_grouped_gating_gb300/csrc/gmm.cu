@@ -554,10 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // so that their weight streaming overlaps the heavy units' tensor work instead of
 // adding to it.  The other experts' units run on the heavy pipeline.  An expert's
 // units all go to one pipeline, so the down projection's wait for h never crosses
-// pipelines.  With light experts present the heavy accumulators narrow to 224
-// columns (TMEM columns 0 and 256; the light ones sit at 224 and 480) and the heavy
-// token slots to 112 rows per CTA; without them the heavy pipeline keeps 256-token
-// blocks and 128-row slots, and the light roles find no units.
+// pipelines.  The kernel uses the light pipeline only when its per-stage cost
+// estimates say the overlap pays (see the prologue); then the heavy accumulators
+// narrow to 224 columns (TMEM columns 0 and 256; the light ones sit at 224 and 480)
+// and the heavy token slots to 112 rows per CTA.  Otherwise every expert runs on the
+// heavy pipeline with 256-token blocks and 128-row slots, and the light roles find no
+// units.
 //
 // Roles (512 threads): in each CTA, warp 0 lane 0 loads the heavy tiles and warp 2
 // lane 0 the light ones, each onto its own ring's `full` barrier; in the even CTA
