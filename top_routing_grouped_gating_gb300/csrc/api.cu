@@ -141,7 +141,7 @@ ForwardLayout forward_layout(int T, int H, int E, int k, int I) {
   L.offsets = take((size_t)(E + 1) * sizeof(int32_t));
   L.eri = take(P * sizeof(int32_t));
   L.sri = take(P * sizeof(int32_t));
-  L.done = take((size_t)E * sizeof(int32_t));
+  L.done = take((size_t)(E + 1) * sizeof(int32_t));   // + the GEMM's unit counter
   L.counter = take(sizeof(int32_t));
   L.xe = take(P * H * 2);
   L.h = take(P * I * 2);
@@ -587,7 +587,7 @@ ForwardMxLayout forward_mx_layout(int T, int H, int E, int k, int I) {
   L.offsets = take((size_t)(E + 1) * 4);
   L.eri = take(P * 4);
   L.sri = take(P * 4);
-  L.done = take((size_t)E * 4);
+  L.done = take((size_t)(E + 1) * 4);   // + the GEMM's unit counter
   L.counter = take(4);
   L.xe = take(R * H);
   L.xe_sf = take(R / L.pad * (H / 128) * 512);

@@ -134,6 +134,7 @@ struct MxArgs {
   uint8_t* h_sf;            // phase-0 output scale atoms [Ppad/128][ld0/128][512]
   uint16_t* y;              // phase-1 output (Ppad, ld1) bf16
   int* done;
+  int* sched;               // CTA pairs: counter the pairs draw units from (or null)
   int* status;
 };
 
@@ -812,6 +813,69 @@ __device__ __forceinline__ Unit decode_pair_unit(int u, const Tables& tb) {
   return decode_unit<PairMx::kBN, PairMx::kTail>(u, tb);
 }
 
+// The units a pair runs, in increasing unit order.  Round-robin (units pair,
+// pair + npairs, ...) unless the launch has a unit counter: then a pair's first two
+// units are those of the round-robin walk and each further one is drawn from the
+// counter (unit 2 * npairs + ticket) by the even CTA's weight producer, which draws
+// the entry after next at the start of each unit and publishes the next one then, in
+// both CTAs' lists, so pairs whose units ran faster take more of them.  An entry is
+// one 64-bit word (pending until published; an end entry closes the list), written
+// and polled with relaxed accesses at cluster scope: the word is its own flag.  Every
+// role walks the same list, and a pair's list increases like a round-robin one, so a
+// down-projection unit still only waits for gate/up units that pairs drew before it.
+constexpr uint32_t kEndUnitWord = 0xFFFFFFFFu;       // word y of the end entry
+constexpr uint32_t kPendingUnitWord = 0xFFFFFFFEu;   // word y of an entry not yet drawn
+
+struct PairList {
+  uint32_t units_addr;   // shared::cta address of the CTA's list
+  int pair, npairs, total;
+  bool drawn, use_list;
+};
+
+__device__ __forceinline__ uint64_t ld_relaxed_cluster_u64(uint32_t cta_addr) {
+  uint64_t v;
+  asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(cta_addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_cluster_u64(uint32_t cluster_addr, uint64_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr), "l"(v)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t unit_word(const uint2 w) {
+  return static_cast<uint64_t>(w.x) | (static_cast<uint64_t>(w.y) << 32);
+}
+
+// 1: unit ui is in t; 0: the list ended before ui; -1: the wait for entry ui ran
+// out (or the CTA is aborting).
+__device__ __forceinline__ int pair_unit(const PairList& pl, const Tables& tb, int ui, Unit& t,
+                                         const volatile int* abort) {
+  if (!pl.drawn) {
+    const int u = pl.pair + ui * pl.npairs;
+    if (u >= pl.total) return 0;
+    if (pl.use_list) {
+      const uint64_t v = ld_relaxed_cluster_u64(pl.units_addr + 8u * static_cast<uint32_t>(ui));
+      t = unpack_unit(make_uint2(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32)));
+    } else {
+      t = decode_pair_unit(u, tb);
+    }
+    return 1;
+  }
+  const uint32_t a = pl.units_addr + 8u * static_cast<uint32_t>(ui);
+  uint64_t v = ld_relaxed_cluster_u64(a);
+  if (static_cast<uint32_t>(v >> 32) == kPendingUnitWord) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+      __nanosleep(32);
+      v = ld_relaxed_cluster_u64(a);
+      if (static_cast<uint32_t>(v >> 32) != kPendingUnitWord) break;
+      if ((n & 15u) == 0 && (*abort || globaltimer() - t0 > kWaitLimitNs)) return -1;
+    }
+  }
+  if (static_cast<uint32_t>(v >> 32) == kEndUnitWord) return 0;
+  t = unpack_unit(make_uint2(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32)));
+  return 1;
+}
+
 __global__ void __launch_bounds__(PairMx::kThreads, 1)
     grouped_gemm_mx_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
                                 const __grid_constant__ CUtensorMap tmB0,
@@ -912,11 +976,6 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
       __syncthreads();
     }
   }
-  tc_fence_after_sync();
-  // both CTAs' barriers are initialised and TMEM allocated before any remote arrive
-  cluster_sync_all();
-  tc_fence_after_sync();
-  const uint32_t tmem_base = *s_tmem;
   Tables tb;
   tb.off = s_off;
   tb.poff = s_poff;
@@ -925,12 +984,35 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
   tb.E = E;
   const int total = s_uoff0[E] + s_uoff1[E];
   const int my_units = pair < total ? (total - pair + npairs - 1) / npairs : 0;
-  const bool use_list = my_units <= S::kMaxUnits;   // the same in every thread of the cluster
-  if (use_list) {
+  // the same in every thread of the grid.  A drawn list holds at most kMaxUnits - 1
+  // units; at most half of the pairs can fill theirs, so the others draw the rest.
+  PairList pl;
+  pl.units_addr = smem_u32(s_units);
+  pl.pair = pair;
+  pl.npairs = npairs;
+  pl.total = total;
+  pl.drawn = args.sched != nullptr && total <= (S::kMaxUnits - 1) * (npairs / 2);
+  pl.use_list = pl.drawn || my_units <= S::kMaxUnits;
+  if (pl.drawn) {
+    // entries 0 and 1 are the round-robin walk's, the others pending; both CTAs
+    // write theirs before the cluster barrier below, ahead of any published entry
+    for (int i = tid; i < S::kMaxUnits; i += S::kThreads) {
+      const int u = pair + i * npairs;
+      s_units[i] = i >= 2            ? make_uint2(0, kPendingUnitWord)
+                   : u < total ? pack_unit(decode_pair_unit(u, tb))
+                               : make_uint2(0, kEndUnitWord);
+    }
+  } else if (pl.use_list) {
     for (int i = tid; i < my_units; i += S::kThreads)
       s_units[i] = pack_unit(decode_pair_unit(pair + i * npairs, tb));
-    __syncthreads();
   }
+  __syncthreads();
+  tc_fence_after_sync();
+  // both CTAs' barriers are initialised, their lists started and TMEM allocated
+  // before any remote arrive or store
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
   const uint32_t lead_full0 = mapa_shared(smem_u32(&full[0]), 0);
   const uint32_t lead_tempty = mapa_shared(smem_u32(tempty), 0);
   // Registers: the role warpgroup needs few, the epilogue warpgroups hold up to
@@ -947,8 +1029,32 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
       uint32_t par = 0;
       uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
-      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
-        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_pair_unit(u, tb);
+      // the even CTA's weight producer draws the units of a drawn list: at the start
+      // of unit ui it publishes entry ui + 1 (drawn one unit earlier; entries 0 and 1
+      // are the round-robin walk's) and draws entry ui + 2 (the list's last entry is
+      // kept for the end entry)
+      const bool drawer = pl.drawn && leader && weights;
+      bool open = drawer && pair + npairs < total;   // entry 1 is a unit
+      int ticket = 0;
+      for (int ui = 0; ok; ++ui) {
+        Unit t;
+        const int got = pair_unit(pl, tb, ui, t, s_abort);
+        if (got <= 0) {
+          ok = got == 0;
+          break;
+        }
+        if (open) {
+          if (ui >= 1) {
+            const int un = ticket >= 0 ? 2 * npairs + ticket : total;
+            const uint64_t w = un < total ? unit_word(pack_unit(decode_pair_unit(un, tb)))
+                                          : unit_word(make_uint2(0, kEndUnitWord));
+            const uint32_t entry = pl.units_addr + 8u * static_cast<uint32_t>(ui + 1);
+            st_relaxed_cluster_u64(mapa_shared(entry, 1), w);
+            st_relaxed_cluster_u64(mapa_shared(entry, 0), w);
+            open = un < total;
+          }
+          if (open) ticket = ui + 2 <= S::kMaxUnits - 2 ? atomicAdd(args.sched, 1) : -1;
+        }
         if (!weights && t.ph == 1 && args.done != nullptr) {
           // the down projection's activations are h of this expert's gate/up units
           const int m = s_off[t.e + 1] - s_off[t.e];
@@ -1038,8 +1144,13 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
       int stage = 0;
       uint32_t par = 0;
       bool ok = true;
-      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
-        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_pair_unit(u, tb);
+      for (int ui = 0; ok; ++ui) {
+        Unit t;
+        const int got = pair_unit(pl, tb, ui, t, s_abort);
+        if (got <= 0) {
+          ok = got == 0;
+          break;
+        }
         const int nk = args.K[t.ph] / kBK;
         const bool tail = t.rows > kBN;
         const bool two = tail || t.rows > 128;
@@ -1085,8 +1196,13 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
       int stage = 0;
       uint32_t par = 0, apar = 0;
       bool ok = true;
-      for (int u = pair, ui = 0; u < total && ok; u += npairs, ++ui) {
-        const Unit t = use_list ? unpack_unit(s_units[ui]) : decode_pair_unit(u, tb);
+      for (int ui = 0; ok; ++ui) {
+        Unit t;
+        const int got = pair_unit(pl, tb, ui, t, s_abort);
+        if (got <= 0) {
+          ok = got == 0;
+          break;
+        }
         const bool tail = t.rows > kBN;
         const int nmain = tail ? kBN : ((t.rows + 15) & ~15);
         const uint32_t fp4 = args.a_fp4[t.ph] ? (5u << 7) : 0u;
@@ -1149,20 +1265,32 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
     int* s_flag = s_tmp;
     int nchunk = 0;                          // gate/up chunks so far (the xs slot parity)
     uint32_t apar = 0;
-    for (int u = pair, ui = 0; u < total; u += npairs, ++ui) {
-      Unit t = use_list ? unpack_unit(s_units[ui]) : decode_pair_unit(u, tb);
-      t.mb = 2 * t.mb + static_cast<int>(rank);
-      if (et == 0) s_flag[0] = mbar_wait(tfull, apar, s_abort) ? 1 : 0;
+    for (int ui = 0;; ++ui) {
+      // one thread waits for the unit and its accumulator; s_flag[0]: 1 go, 0 the
+      // list has ended, -1 a wait ran out
+      if (et == 0) {
+        Unit t0;
+        int st = pair_unit(pl, tb, ui, t0, s_abort);
+        if (st == 1) {
+          if (!mbar_wait(tfull, apar, s_abort)) st = -1;
+          const uint2 w = pack_unit(t0);
+          s_flag[1] = static_cast<int>(w.x);
+          s_flag[2] = static_cast<int>(w.y);
+        }
+        s_flag[0] = st;
+      }
       named_bar_sync(1, 32 * S::kEpiWarps);
-      const int ok = s_flag[0];
+      const int st = s_flag[0];
+      Unit t = unpack_unit(make_uint2(static_cast<uint32_t>(s_flag[1]), static_cast<uint32_t>(s_flag[2])));
       named_bar_sync(1, 32 * S::kEpiWarps);
-      if (!ok) {
-        if (et == 0) {
+      if (st <= 0) {
+        if (st < 0 && et == 0) {
           *s_abort = 1;
           flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
         }
         break;
       }
+      t.mb = 2 * t.mb + static_cast<int>(rank);
       tc_fence_after_sync();
       // read this warp's chunks into registers, then hand the accumulator back to the
       // MMA thread before working on them
@@ -1308,6 +1436,7 @@ cudaError_t launch_pair_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1, const
   a.offsets = offsets;
   a.E = E;
   a.done = (ph0 && ph1) ? done : nullptr;
+  a.sched = a.done != nullptr ? done + E : nullptr;   // zeroed with the dependency counters
   a.status = status;
   CUtensorMap tm[6];   // A0, B0, A1, B1 (128-row boxes), then the 16-row tail boxes
   const GemmPhaseMx* phs[2] = {ph0, ph1};

@@ -53,7 +53,8 @@ struct GatingRouting {
   int32_t* offsets;
   int32_t* eri;
   int32_t* sri;
-  int* done;     // E ints cleared for the grouped GEMM's dependency
+  int* done;     // E + 1 ints cleared for the grouped GEMM (per-expert dependency
+                 // counters, then its unit counter)
   int E_routed;  // experts [0, E_routed) are routed; ids >= E_routed (zero-computation
                  // experts) are skipped.  0: all E gating columns are routed experts.
 };
@@ -71,7 +72,8 @@ struct RoutingPlan {
 RoutingPlan routing_plan(int P, int E);
 size_t routing_ws_bytes(int P, int E);
 // ids (P); writes counts (may be null), offsets (E+1), eri (P), sri (P).
-// zero_counter (E ints, may be null) is cleared for the fused GEMM dependency.
+// zero_counter (E + 1 ints, may be null) is cleared for the fused GEMM: the
+// per-expert dependency counters and its unit counter.
 cudaError_t launch_routing(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets,
                            int32_t* eri, int32_t* sri, void* ws, int* zero_counter, int* status,
                            cudaStream_t s);
@@ -105,7 +107,7 @@ struct GemmPhase {
 };
 // phases[0] and/or phases[1] (null A_weights = phase absent).  When both are
 // present they run in one persistent launch with a per-expert dependency on
-// done_counter (E ints, zeroed beforehand).
+// done_counter (E + 1 ints, zeroed beforehand; the last one counts drawn units).
 cudaError_t launch_grouped_gemm(const GemmPhase* ph0, const GemmPhase* ph1,
                                 const int32_t* offsets, int E, int P, int max_rows_hint,
                                 int* done_counter, int* status, cudaStream_t s);
@@ -158,7 +160,9 @@ struct GemmPhaseMx {
   bool a_fp4 = false;       // weights are packed e2m1 (two per byte) instead of e4m3
 };
 // pad = mx_pad_rows(P, E) of the activation layout (selects the tile shape);
-// P_pad_rows = rows of that padded layout.
+// P_pad_rows = rows of that padded layout.  With both phases, done holds E + 1
+// zeroed ints: the per-expert dependency counters, then a unit counter from which
+// the CTA-pair kernel's pairs draw their units.
 cudaError_t launch_grouped_gemm_mx(const GemmPhaseMx* ph0, const GemmPhaseMx* ph1,
                                    const int32_t* offsets, int E, int pad, int P_pad_rows,
                                    int* done, int* status, cudaStream_t s);

@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(256) routing_scan_kernel(int32_t* __restrict__
     if (counts != nullptr) counts[e] = run;
     offsets[e] = off;
     if (zero_counter != nullptr) zero_counter[e] = 0;
+    if (zero_counter != nullptr && e == 0) zero_counter[E] = 0;
     for (int c = 0; c < chunks; ++c) chunk_hist[(size_t)c * E + e] += off;
   }
   if (e == 0) offsets[E] = total;

@@ -107,7 +107,7 @@ struct RoutingSmem {
 
 // Histogram, exclusive scan and stable scatter of all P pairs by one CTA
 // (blockDim.x == 32 * NWARPS >= 256) for the local experts of rm.  zero_counter
-// (rm.E ints, may be null) is cleared on the way.
+// (rm.E + 1 ints, may be null) is cleared on the way.
 template <int NWARPS>
 __device__ __forceinline__ void routing_single_cta(const int32_t* __restrict__ ids, int P,
                                                    const RouteMap& rm,
@@ -122,7 +122,7 @@ __device__ __forceinline__ void routing_single_cta(const int32_t* __restrict__ i
   for (int i = tid; i < kMaxExperts; i += blockDim.x) sm.hist[i] = 0;
   for (int i = tid; i < NWARPS * E; i += blockDim.x) sm.wcnt[i] = 0;
   if (zero_counter != nullptr)
-    for (int i = tid; i < E; i += blockDim.x) zero_counter[i] = 0;
+    for (int i = tid; i <= E; i += blockDim.x) zero_counter[i] = 0;
   __syncthreads();
   bool bad = false;
   for (int j = tid; j < P; j += blockDim.x) {
