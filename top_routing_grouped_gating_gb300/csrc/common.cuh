@@ -344,6 +344,25 @@ MOE_DEVINL void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Unit lists that a CTA pair's even CTA publishes into both CTAs' shared memory
+// while the pair runs: an entry is one 64-bit word (a packed unit, whose high word
+// is never one of the two markers below), stored and polled with relaxed accesses
+// at cluster scope, so that the word is its own flag and the publishing thread waits
+// for nothing.
+constexpr uint32_t kEndUnitWord = 0xFFFFFFFFu;       // high word of a list's end entry
+constexpr uint32_t kPendingUnitWord = 0xFFFFFFFEu;   // high word of an entry not yet published
+MOE_DEVINL uint64_t ld_relaxed_cluster_u64(uint32_t cta_addr) {
+  uint64_t v;
+  asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(cta_addr) : "memory");
+  return v;
+}
+MOE_DEVINL void st_relaxed_cluster_u64(uint32_t cluster_addr, uint64_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr), "l"(v)
+               : "memory");
+}
+MOE_DEVINL uint64_t unit_word(uint2 w) {
+  return static_cast<uint64_t>(w.x) | (static_cast<uint64_t>(w.y) << 32);
+}
 MOE_DEVINL bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -66,6 +66,7 @@ struct GemmArgs {
   uint16_t* out[2];
   float* out_f32[2];
   int* done;        // per-expert count of finished phase-0 units, or null
+  int* sched;       // CTA pairs: counter the pairs draw heavy units from, or null
   int* status;
   // Test hook of the one-CTA kernel (moe_debug_set_gemm_stall): a producer that
   // reaches its stall_stage-th stage issues nothing more and waits for another role
@@ -668,6 +669,7 @@ struct PairPipe {
   uint32_t lead_full0;     // full[0] of the even CTA (cluster address)
   uint32_t lead_tempty0;   // tempty[0] of the even CTA
   const uint2* units;      // this pair's units, or null: decoded on the fly
+  bool drawn;              // units after the first two are drawn from args.sched
   const int* off;
   const int* uoff0;
   const int* uoff1;
@@ -680,9 +682,38 @@ struct PairPipe {
   int* flag;               // the epilogue group's broadcast word
 };
 
-__device__ __forceinline__ Unit pipe_unit(const PairPipe& p, int u, int ui) {
-  return p.units != nullptr ? unpack_unit(p.units[ui])
-                            : decode_unit_rows(u, p.off, p.uoff0, p.uoff1, p.E, p.bn);
+// A pipeline's units, in increasing unit order: round-robin (units pair, pair +
+// npairs, ...), or, for a drawn list, the round-robin walk's first two and then units
+// 2 * npairs + ticket drawn from a counter by the even CTA's producer, which at the
+// start of each unit publishes the next entry (drawn one unit earlier) in both CTAs'
+// lists and draws the one after, so pairs whose units ran faster take more of them.
+// A pair's list increases like a round-robin one, so a down-projection unit still
+// only waits for gate/up units that pairs drew before it.
+// Returns 1 with unit ui in t, 0 when the list ended before ui, -1 when the wait
+// for a drawn entry ran out (or the CTA is aborting).
+__device__ __forceinline__ int pipe_unit(const PairPipe& p, int pair, int npairs, int ui, Unit& t,
+                                         const volatile int* abort) {
+  if (!p.drawn) {
+    const int u = pair + ui * npairs;
+    if (u >= p.total) return 0;
+    t = p.units != nullptr ? unpack_unit(p.units[ui])
+                           : decode_unit_rows(u, p.off, p.uoff0, p.uoff1, p.E, p.bn);
+    return 1;
+  }
+  const uint32_t a = smem_u32(p.units + ui);
+  uint64_t v = ld_relaxed_cluster_u64(a);
+  if (static_cast<uint32_t>(v >> 32) == kPendingUnitWord) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+      __nanosleep(32);
+      v = ld_relaxed_cluster_u64(a);
+      if (static_cast<uint32_t>(v >> 32) != kPendingUnitWord) break;
+      if ((n & 15u) == 0 && (*abort || globaltimer() - t0 > kWaitLimitNs)) return -1;
+    }
+  }
+  if (static_cast<uint32_t>(v >> 32) == kEndUnitWord) return 0;
+  t = unpack_unit(make_uint2(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32)));
+  return 1;
 }
 
 // TMA producer of one pipeline in one CTA: this CTA's weight block and token half.
@@ -699,8 +730,31 @@ __device__ __forceinline__ void pair_producer(const PairPipe& p, const GemmArgs&
   uint32_t par = 0;
   uint32_t issued_mask = 0, issued_par = 0;
   bool ok = true;
-  for (int u = pair, ui = 0; u < p.total && ok; u += npairs, ++ui) {
-    const Unit t = pipe_unit(p, u, ui);
+  // the even CTA's producer of a drawn list: entry ui + 1 is published at the start
+  // of unit ui (entries 0 and 1 are the round-robin walk's), entry ui + 2 drawn then
+  // (the list's last entry is kept for the end entry)
+  bool open = p.drawn && rank == 0 && pair + npairs < p.total;   // entry 1 is a unit
+  int ticket = 0;
+  for (int ui = 0; ok; ++ui) {
+    Unit t;
+    const int got = pipe_unit(p, pair, npairs, ui, t, s_abort);
+    if (got <= 0) {
+      ok = got == 0;
+      break;
+    }
+    if (open) {
+      if (ui >= 1) {
+        const int un = ticket >= 0 ? 2 * npairs + ticket : p.total;
+        const uint64_t w =
+            un < p.total ? unit_word(pack_unit(decode_unit_rows(un, p.off, p.uoff0, p.uoff1, p.E, p.bn)))
+                         : unit_word(make_uint2(0, kEndUnitWord));
+        const uint32_t entry = smem_u32(p.units + ui + 1);
+        st_relaxed_cluster_u64(mapa_shared(entry, 1), w);
+        st_relaxed_cluster_u64(mapa_shared(entry, 0), w);
+        open = un < p.total;
+      }
+      if (open) ticket = ui + 2 <= kPairMaxUnits - 2 ? atomicAdd(args.sched, 1) : -1;
+    }
     const int m = p.off[t.e + 1] - p.off[t.e];
     if (t.ph == 1 && args.done != nullptr) {
       // the down projection reads h of this expert's gate/up units (same pipeline)
@@ -766,8 +820,13 @@ __device__ __forceinline__ void pair_forwarder(const PairPipe& p, const GemmArgs
   int stage = 0;
   uint32_t par = 0;
   bool ok = true;
-  for (int u = pair, ui = 0; u < p.total && ok; u += npairs, ++ui) {
-    const Unit t = pipe_unit(p, u, ui);
+  for (int ui = 0; ok; ++ui) {
+    Unit t;
+    const int got = pipe_unit(p, pair, npairs, ui, t, s_abort);
+    if (got <= 0) {
+      ok = got == 0;
+      break;
+    }
     const int nk = args.K[t.ph] / kBK;
     for (int kb = 0; kb < nk; ++kb) {
       if (!mbar_wait(&p.full[stage], par, s_abort)) {
@@ -794,8 +853,13 @@ __device__ __forceinline__ void pair_mma(const PairPipe& p, const GemmArgs& args
   int stage = 0, acc = 0;
   uint32_t par = 0, apar = 0;
   bool ok = true;
-  for (int u = pair, ui = 0; u < p.total && ok; u += npairs, ++ui) {
-    const Unit t = pipe_unit(p, u, ui);
+  for (int ui = 0; ok; ++ui) {
+    Unit t;
+    const int got = pipe_unit(p, pair, npairs, ui, t, s_abort);
+    if (got <= 0) {
+      ok = got == 0;
+      break;
+    }
     const int n = (t.rows + 15) & ~15;
     const uint32_t idesc = idesc_bf16_f32(2 * kBM, n);
     // both CTAs' epilogues have drained this accumulator
@@ -911,20 +975,32 @@ __device__ __forceinline__ void pair_epilogue(const PairPipe& p, const GemmArgs&
   const int et = ew * 32 + lane;
   int acc = 0;
   uint32_t apar = 0;
-  for (int u = pair, ui = 0; u < p.total; u += npairs, ++ui) {
-    Unit t = pipe_unit(p, u, ui);
-    t.mb = 2 * t.mb + static_cast<int>(rank);   // this CTA's 128-row weight block
-    if (et == 0) p.flag[0] = mbar_wait(&p.tfull[acc], apar, s_abort) ? 1 : 0;
+  for (int ui = 0;; ++ui) {
+    // one thread waits for the unit and its accumulator; p.flag[0]: 1 go, 0 the
+    // list has ended, -1 a wait ran out
+    if (et == 0) {
+      Unit t0;
+      int st = pipe_unit(p, pair, npairs, ui, t0, s_abort);
+      if (st == 1) {
+        const uint2 w = pack_unit(t0);
+        p.flag[1] = static_cast<int>(w.x);
+        p.flag[2] = static_cast<int>(w.y);
+        if (!mbar_wait(&p.tfull[acc], apar, s_abort)) st = -1;
+      }
+      p.flag[0] = st;
+    }
     named_bar_sync(p.bar_id, nthr);
-    const int ok = p.flag[0];
+    const int st = p.flag[0];
+    Unit t = unpack_unit(make_uint2(static_cast<uint32_t>(p.flag[1]), static_cast<uint32_t>(p.flag[2])));
     named_bar_sync(p.bar_id, nthr);
-    if (!ok) {
-      if (et == 0) {
+    if (st <= 0) {
+      if (st < 0 && et == 0) {
         *s_abort = 1;
         flag_status(args.status, MOE_DEV_WAIT_TIMEOUT);
       }
       break;
     }
+    t.mb = 2 * t.mb + static_cast<int>(rank);   // this CTA's 128-row weight block
     tc_fence_after_sync();
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + p.acc_base +
                            static_cast<uint32_t>(acc * kPairBN);
@@ -979,7 +1055,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   int* s_uh1 = s_uh0 + (kMaxE + 1);
   int* s_ul0 = s_uh1 + (kMaxE + 1);
   int* s_ul1 = s_ul0 + (kMaxE + 1);
-  int* s_tmp = s_ul1 + (kMaxE + 1);   // 16 scan words, then the two epilogue flags
+  int* s_tmp = s_ul1 + (kMaxE + 1);   // 16 scan words, then the two epilogue groups' words
   uint2* s_hunits = reinterpret_cast<uint2*>(smem + L::kUnits);
   uint2* s_lunits = s_hunits + kPairMaxUnits;
 
@@ -1069,11 +1145,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
     __syncthreads();
   }
-  tc_fence_after_sync();
-  // both CTAs' barriers are initialised and TMEM allocated before any remote arrive
-  cluster_sync_all();
-  tc_fence_after_sync();
-  const uint32_t tmem_base = *s_tmem;
   const int hb = *s_hbn;
 
   PairPipe hp, lp;
@@ -1096,7 +1167,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   hp.acc_base = 0;                  // columns 0 and 256
   hp.epi_warps = kHeavyEpiWarps;
   hp.bar_id = 1;
-  hp.flag = s_tmp + 16;
+  hp.flag = s_tmp + 16;             // three words each
 
   lp.ring = smem + L::kL;
   lp.stride = L::kLStride;
@@ -1117,20 +1188,43 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   lp.acc_base = kPairBNL;           // columns 224 and 480
   lp.epi_warps = kLightEpiWarps;
   lp.bar_id = 2;
-  lp.flag = s_tmp + 17;
+  lp.flag = s_tmp + 20;
 
-  // Each pair's units of both lists, decoded once (the same in every thread).
+  // Each pair's units of both lists, decoded once (the same in every thread).  The
+  // heavy list is drawn when the launch has a unit counter, the light pipeline does
+  // not run (beside it, drawing measured slower) and at most half of the pairs can
+  // fill a list (kPairMaxUnits - 1 units), so that the others draw the rest.
   const int h_my = pair < hp.total ? (hp.total - pair + npairs - 1) / npairs : 0;
   const int l_my = pair < lp.total ? (lp.total - pair + npairs - 1) / npairs : 0;
-  hp.units = h_my <= kPairMaxUnits ? s_hunits : nullptr;
+  hp.drawn = args.sched != nullptr && lp.total == 0 &&
+             hp.total <= (kPairMaxUnits - 1) * (npairs / 2);
+  lp.drawn = false;
+  hp.units = hp.drawn || h_my <= kPairMaxUnits ? s_hunits : nullptr;
   lp.units = l_my <= kPairMaxUnits ? s_lunits : nullptr;
-  if (hp.units != nullptr)
+  if (hp.drawn) {
+    // entries 0 and 1 are the round-robin walk's, the others pending; both CTAs
+    // write theirs before the cluster barrier below, ahead of any published entry
+    for (int i = tid; i < kPairMaxUnits; i += kPairThreads) {
+      const int u = pair + i * npairs;
+      s_hunits[i] = i >= 2 ? make_uint2(0, kPendingUnitWord)
+                    : u < hp.total
+                        ? pack_unit(decode_unit_rows(u, s_off, s_uh0, s_uh1, E, hp.bn))
+                        : make_uint2(0, kEndUnitWord);
+    }
+  } else if (hp.units != nullptr) {
     for (int i = tid; i < h_my; i += kPairThreads)
       s_hunits[i] = pack_unit(decode_unit_rows(pair + i * npairs, s_off, s_uh0, s_uh1, E, hp.bn));
+  }
   if (lp.units != nullptr)
     for (int i = tid; i < l_my; i += kPairThreads)
       s_lunits[i] = pack_unit(decode_unit_rows(pair + i * npairs, s_off, s_ul0, s_ul1, E, lp.bn));
   __syncthreads();
+  tc_fence_after_sync();
+  // both CTAs' barriers are initialised, their lists started and TMEM allocated
+  // before any remote arrive or store
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
 
   const CUtensorMap* hw0 = hb == kPairBN ? &tmB0 : &tmH0;
   const CUtensorMap* hw1 = hb == kPairBN ? &tmB1 : &tmH1;
@@ -1285,6 +1379,7 @@ cudaError_t launch_pair_impl(const GemmPhase* ph0, const GemmPhase* ph1, const i
   a.offsets = offsets;
   a.E = E;
   a.done = (ph0 && ph1) ? done : nullptr;
+  a.sched = a.done != nullptr ? done + E : nullptr;   // zeroed with the dependency counters
   a.status = status;
   a.stall_stage = -1;
   a.wait_ns = kWaitLimitNs;

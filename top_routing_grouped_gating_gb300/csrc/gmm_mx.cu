@@ -823,27 +823,11 @@ __device__ __forceinline__ Unit decode_pair_unit(int u, const Tables& tb) {
 // and polled with relaxed accesses at cluster scope: the word is its own flag.  Every
 // role walks the same list, and a pair's list increases like a round-robin one, so a
 // down-projection unit still only waits for gate/up units that pairs drew before it.
-constexpr uint32_t kEndUnitWord = 0xFFFFFFFFu;       // word y of the end entry
-constexpr uint32_t kPendingUnitWord = 0xFFFFFFFEu;   // word y of an entry not yet drawn
-
 struct PairList {
   uint32_t units_addr;   // shared::cta address of the CTA's list
   int pair, npairs, total;
   bool drawn, use_list;
 };
-
-__device__ __forceinline__ uint64_t ld_relaxed_cluster_u64(uint32_t cta_addr) {
-  uint64_t v;
-  asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(cta_addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_relaxed_cluster_u64(uint32_t cluster_addr, uint64_t v) {
-  asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr), "l"(v)
-               : "memory");
-}
-__device__ __forceinline__ uint64_t unit_word(const uint2 w) {
-  return static_cast<uint64_t>(w.x) | (static_cast<uint64_t>(w.y) << 32);
-}
 
 // 1: unit ui is in t; 0: the list ended before ui; -1: the wait for entry ui ran
 // out (or the CTA is aborting).
