@@ -1007,7 +1007,8 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
     if ((warp == 0 || warp == 2) && lane == 0) {
       // ------------------------------------------------------ TMA producers --
       const bool weights = warp == 0;
-      const uint64_t pol_w = l2_policy_evict_normal();
+      const uint64_t pol_w_reused = l2_policy_evict_normal();
+      const uint64_t pol_w_once = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t par = 0;
@@ -1054,6 +1055,9 @@ __global__ void __launch_bounds__(PairMx::kThreads, 1)
         const bool tail = t.rows > kBN;
         const int nmain = tail ? kBN : ((t.rows + 15) & ~15);
         const int half = nmain >> 1;
+        // weight tiles of an expert with one token block are read once: stream them
+        const uint64_t pol_w =
+            token_blocks<kBN, kTail>(s_off[t.e + 1] - s_off[t.e]) == 1 ? pol_w_once : pol_w_reused;
         const int nsfb = nmain > 128 ? 2 : 1;
         const uint32_t abytes = args.a_fp4[t.ph] ? kABytes / 2 : kABytes;
         const uint32_t bytes = weights ? abytes + kSfBytes
