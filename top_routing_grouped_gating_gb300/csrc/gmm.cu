@@ -691,9 +691,11 @@ struct PairPipe {
 // only waits for gate/up units that pairs drew before it.
 // Returns 1 with unit ui in t, 0 when the list ended before ui, -1 when the wait
 // for a drawn entry ran out (or the CTA is aborting).
+// The roles are instantiated for round-robin (kDrawn false) and drawn lists.
+template <bool kDrawn>
 __device__ __forceinline__ int pipe_unit(const PairPipe& p, int pair, int npairs, int ui, Unit& t,
                                          const volatile int* abort) {
-  if (!p.drawn) {
+  if (!kDrawn) {
     const int u = pair + ui * npairs;
     if (u >= p.total) return 0;
     t = p.units != nullptr ? unpack_unit(p.units[ui])
@@ -717,6 +719,7 @@ __device__ __forceinline__ int pipe_unit(const PairPipe& p, int pair, int npairs
 }
 
 // TMA producer of one pipeline in one CTA: this CTA's weight block and token half.
+template <bool kDrawn>
 __device__ __forceinline__ void pair_producer(const PairPipe& p, const GemmArgs& args,
                                               const CUtensorMap* tmA0, const CUtensorMap* tmA1,
                                               const CUtensorMap* tmW0, const CUtensorMap* tmW1,
@@ -733,11 +736,11 @@ __device__ __forceinline__ void pair_producer(const PairPipe& p, const GemmArgs&
   // the even CTA's producer of a drawn list: entry ui + 1 is published at the start
   // of unit ui (entries 0 and 1 are the round-robin walk's), entry ui + 2 drawn then
   // (the list's last entry is kept for the end entry)
-  bool open = p.drawn && rank == 0 && pair + npairs < p.total;   // entry 1 is a unit
+  bool open = kDrawn && rank == 0 && pair + npairs < p.total;   // entry 1 is a unit
   int ticket = 0;
   for (int ui = 0; ok; ++ui) {
     Unit t;
-    const int got = pipe_unit(p, pair, npairs, ui, t, s_abort);
+    const int got = pipe_unit<kDrawn>(p, pair, npairs, ui, t, s_abort);
     if (got <= 0) {
       ok = got == 0;
       break;
@@ -815,6 +818,7 @@ __device__ __forceinline__ void pair_producer(const PairPipe& p, const GemmArgs&
 }
 
 // Odd CTA: passes each of its landed stages on to the even CTA's `full` barrier.
+template <bool kDrawn>
 __device__ __forceinline__ void pair_forwarder(const PairPipe& p, const GemmArgs& args, int pair,
                                                int npairs, volatile int* s_abort) {
   int stage = 0;
@@ -822,7 +826,7 @@ __device__ __forceinline__ void pair_forwarder(const PairPipe& p, const GemmArgs
   bool ok = true;
   for (int ui = 0; ok; ++ui) {
     Unit t;
-    const int got = pipe_unit(p, pair, npairs, ui, t, s_abort);
+    const int got = pipe_unit<kDrawn>(p, pair, npairs, ui, t, s_abort);
     if (got <= 0) {
       ok = got == 0;
       break;
@@ -848,6 +852,7 @@ __device__ __forceinline__ void pair_forwarder(const PairPipe& p, const GemmArgs
 }
 
 // Even CTA: the pipeline's MMA issuer.
+template <bool kDrawn>
 __device__ __forceinline__ void pair_mma(const PairPipe& p, const GemmArgs& args, uint32_t tmem_base,
                                          int pair, int npairs, volatile int* s_abort) {
   int stage = 0, acc = 0;
@@ -855,7 +860,7 @@ __device__ __forceinline__ void pair_mma(const PairPipe& p, const GemmArgs& args
   bool ok = true;
   for (int ui = 0; ok; ++ui) {
     Unit t;
-    const int got = pipe_unit(p, pair, npairs, ui, t, s_abort);
+    const int got = pipe_unit<kDrawn>(p, pair, npairs, ui, t, s_abort);
     if (got <= 0) {
       ok = got == 0;
       break;
@@ -965,6 +970,7 @@ __device__ __forceinline__ void pair_store_chunk(const GemmArgs& args, const Uni
 
 // An epilogue group: p.epi_warps warps per CTA, warp ew taking TMEM lane quarter
 // ew % 4 and every (p.epi_warps / 4)-th 32-token chunk from chunk ew / 4.
+template <bool kDrawn>
 __device__ __forceinline__ void pair_epilogue(const PairPipe& p, const GemmArgs& args,
                                               uint32_t tmem_base, int pair, int npairs,
                                               uint32_t rank, int ew, int lane,
@@ -980,7 +986,7 @@ __device__ __forceinline__ void pair_epilogue(const PairPipe& p, const GemmArgs&
     // list has ended, -1 a wait ran out
     if (et == 0) {
       Unit t0;
-      int st = pipe_unit(p, pair, npairs, ui, t0, s_abort);
+      int st = pipe_unit<kDrawn>(p, pair, npairs, ui, t0, s_abort);
       if (st == 1) {
         const uint2 w = pack_unit(t0);
         p.flag[1] = static_cast<int>(w.x);
@@ -1229,22 +1235,31 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const CUtensorMap* hw0 = hb == kPairBN ? &tmB0 : &tmH0;
   const CUtensorMap* hw1 = hb == kPairBN ? &tmB1 : &tmH1;
   if (lane == 0 && warp == 0) {
-    pair_producer(hp, args, &tmA0, &tmA1, hw0, hw1, hb / 2, &tmS0, &tmS1, pair, npairs, rank,
-                  s_abort);
+    if (hp.drawn)
+      pair_producer<true>(hp, args, &tmA0, &tmA1, hw0, hw1, hb / 2, &tmS0, &tmS1, pair, npairs,
+                          rank, s_abort);
+    else
+      pair_producer<false>(hp, args, &tmA0, &tmA1, hw0, hw1, hb / 2, &tmS0, &tmS1, pair, npairs,
+                           rank, s_abort);
   } else if (lane == 0 && warp == 2) {
-    pair_producer(lp, args, &tmA0, &tmA1, &tmS0, &tmS1, kLightBox, &tmS0, &tmS1, pair, npairs,
-                  rank, s_abort);
+    pair_producer<false>(lp, args, &tmA0, &tmA1, &tmS0, &tmS1, kLightBox, &tmS0, &tmS1, pair,
+                         npairs, rank, s_abort);
   } else if (lane == 0 && warp == 1) {
-    if (leader) pair_mma(hp, args, tmem_base, pair, npairs, s_abort);
-    else pair_forwarder(lp, args, pair, npairs, s_abort);
+    if (!leader) pair_forwarder<false>(lp, args, pair, npairs, s_abort);
+    else if (hp.drawn) pair_mma<true>(hp, args, tmem_base, pair, npairs, s_abort);
+    else pair_mma<false>(hp, args, tmem_base, pair, npairs, s_abort);
   } else if (lane == 0 && warp == 3) {
-    if (leader) pair_mma(lp, args, tmem_base, pair, npairs, s_abort);
-    else pair_forwarder(hp, args, pair, npairs, s_abort);
+    if (leader) pair_mma<false>(lp, args, tmem_base, pair, npairs, s_abort);
+    else if (hp.drawn) pair_forwarder<true>(hp, args, pair, npairs, s_abort);
+    else pair_forwarder<false>(hp, args, pair, npairs, s_abort);
   } else if (warp >= 4 && warp < 4 + kHeavyEpiWarps) {
-    pair_epilogue(hp, args, tmem_base, pair, npairs, rank, warp - 4, lane, s_abort);
+    if (hp.drawn)
+      pair_epilogue<true>(hp, args, tmem_base, pair, npairs, rank, warp - 4, lane, s_abort);
+    else
+      pair_epilogue<false>(hp, args, tmem_base, pair, npairs, rank, warp - 4, lane, s_abort);
   } else if (warp >= 4 + kHeavyEpiWarps) {
-    pair_epilogue(lp, args, tmem_base, pair, npairs, rank, warp - 4 - kHeavyEpiWarps, lane,
-                  s_abort);
+    pair_epilogue<false>(lp, args, tmem_base, pair, npairs, rank, warp - 4 - kHeavyEpiWarps, lane,
+                         s_abort);
   }
 
   tc_fence_before_sync();
