@@ -274,7 +274,7 @@ moe_status moe_router_logits(const moe_bf16* x, const float* Wg, int T, int H, i
     float* partial = static_cast<float*>(ws);
     if (rp.tc) {
       void* extra = at<uint8_t>(ws, align256((size_t)rp.splits * T * E * sizeof(float)));
-      MOE_CUDA(moe::launch_router_tc(x, false, Wg, T, H, E, rp, partial, extra, nullptr,
+      MOE_CUDA(moe::launch_router_tc(x, false, false, Wg, T, H, E, rp, partial, extra, nullptr,
                                      d->status, stream));
     } else {
       MOE_CUDA(moe::launch_router(x, Wg, T, H, E, rp, partial, nullptr, stream));
@@ -465,7 +465,7 @@ moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_o
     int* zw = fused_routing ? fr.counter : nullptr;
     if (rp.tc) {
       void* extra = at<uint8_t>(ws, L.router + align256((size_t)rp.splits * T * E * sizeof(float)));
-      MOE_CUDA(moe::launch_router_tc(x, false, Wg, T, H, E, rp, part, extra, zw, d->status,
+      MOE_CUDA(moe::launch_router_tc(x, false, false, Wg, T, H, E, rp, part, extra, zw, d->status,
                                      stream));
     } else {
       const size_t hint = decode_l2_hint_bytes(*d, moe_packed_weight_bytes(E, H, I, 0), 2u * H);
@@ -512,7 +512,7 @@ moe_status moe_add_rmsnorm_mxquant(const moe_bf16* x, const moe_bf16* r, const m
   if (T < 1 || H < 256 || H % 256 != 0 || H > 32768) return MOE_ERR_UNSUPPORTED_SHAPE;
   DeviceFacts* d = nullptr;
   MOE_TRY(current_device(&d));
-  MOE_CUDA(moe::launch_add_rmsnorm_mxquant(x, r, w, eps, T, H, residual_out, y32_out, q, scale,
+  MOE_CUDA(moe::launch_add_rmsnorm_mxquant(x, r, w, eps, T, H, residual_out, y32_out, nullptr, q, scale,
                                            stream));
   return MOE_OK;
 }
@@ -648,8 +648,16 @@ moe_status forward_mx_impl(const moe_bf16* x, const moe_bf16* r, const moe_bf16*
   int32_t* eri = at<int32_t>(ws, L.eri);
   int32_t* sri = at<int32_t>(ws, L.sri);
   int* done = at<int>(ws, L.done);
-  MOE_CUDA(moe::launch_add_rmsnorm_mxquant(x, r, norm_w, eps, T, H, residual_out, y32, xq, xs,
-                                           stream));
+  // The router reads the fp32 RMSNorm output: the tensor-core router as its exact
+  // bf16 split, which the norm kernel writes straight into the router's scratch;
+  // with given logits nothing reads it.
+  const moe::RouterPlan rp = moe::router_plan_ex(T, H, E, true);
+  void* router_extra = at<uint8_t>(ws, L.router + align256((size_t)rp.splits * T * E * sizeof(float)));
+  const bool presplit = !logits_override && rp.tc;
+  uint16_t* ys = presplit ? moe::router_split_rows(router_extra, rp, H, E) : nullptr;
+  float* y32_used = (logits_override || presplit) ? nullptr : y32;
+  MOE_CUDA(moe::launch_add_rmsnorm_mxquant(x, r, norm_w, eps, T, H, residual_out, y32_used, ys,
+                                           xq, xs, stream));
   const bool fused_routing = moe::routing_plan(P, E).single_cta;
   moe::GatingRouting fr{};
   fr.counter = at<int>(ws, L.counter);
@@ -663,13 +671,11 @@ moe_status forward_mx_impl(const moe_bf16* x, const moe_bf16* r, const moe_bf16*
     if (fused_routing) MOE_CUDA(cudaMemsetAsync(fr.counter, 0, sizeof(int), stream));
     MOE_CUDA(moe::launch_gating(logits_override, 1, T, E, k, 1, ids, w, fuse, d->status, stream));
   } else {
-    const moe::RouterPlan rp = moe::router_plan_ex(T, H, E, true);
     float* part = at<float>(ws, L.router);
     int* zw = fused_routing ? fr.counter : nullptr;
     if (rp.tc) {
-      void* extra = at<uint8_t>(ws, L.router + align256((size_t)rp.splits * T * E * sizeof(float)));
-      MOE_CUDA(moe::launch_router_tc(y32, true, Wg, T, H, E, rp, part, extra, zw, d->status,
-                                     stream));
+      MOE_CUDA(moe::launch_router_tc(nullptr, true, true, Wg, T, H, E, rp, part, router_extra, zw,
+                                     d->status, stream));
     } else {
       // e4m3 rows are H bytes, packed e2m1 rows H / 2
       const size_t row = w4 ? (size_t)H / 2 : (size_t)H;
@@ -1069,7 +1075,7 @@ moe_status moe_forward_v2(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
     int* zw = fused_routing ? fr.counter : nullptr;
     if (rp.tc) {
       void* extra = at<uint8_t>(ws, L.router + align256((size_t)rp.splits * T * Eg * 4));
-      MOE_CUDA(moe::launch_router_tc(f32in ? static_cast<const void*>(y32) : x, f32in, Wg, T, H,
+      MOE_CUDA(moe::launch_router_tc(f32in ? static_cast<const void*>(y32) : x, f32in, false, Wg, T, H,
                                      Eg, rp, part, extra, zw, d->status, stream));
     } else if (f32in) {
       MOE_CUDA(moe::launch_router_f32(y32, Wg, T, H, Eg, rp, part, zw, stream, w13_packed,

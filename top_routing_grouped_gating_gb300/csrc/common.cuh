@@ -43,6 +43,35 @@ MOE_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
   return *reinterpret_cast<uint32_t*>(&p);
 }
+// Exact three-piece bf16 split v = p0 + p1 + p2 (8 + 8 + 8 significand bits): each
+// piece is the bf16 rounding of what the pieces before it left over.
+MOE_DEVINL void split3_bf16(float v, uint16_t (&p)[3]) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  p[0] = *reinterpret_cast<uint16_t*>(&b);
+  const float r1 = v - bf16_lo(p[0]);
+  b = __float2bfloat16_rn(r1);
+  p[1] = *reinterpret_cast<uint16_t*>(&b);
+  const float r2 = r1 - bf16_lo(p[1]);
+  b = __float2bfloat16_rn(r2);
+  p[2] = *reinterpret_cast<uint16_t*>(&b);
+}
+// Eight consecutive fp32 values split into three rows of eight bf16 pieces, stored
+// at dst, dst + stride and dst + 2 * stride (16-byte aligned).
+MOE_DEVINL void store_split3_x8(const float (&v)[8], uint16_t* dst, size_t stride) {
+  uint32_t w[3][4];
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    uint16_t p0[3], p1[3];
+    split3_bf16(v[i], p0);
+    split3_bf16(v[i + 1], p1);
+#pragma unroll
+    for (int s = 0; s < 3; ++s)
+      w[s][i / 2] = static_cast<uint32_t>(p0[s]) | (static_cast<uint32_t>(p1[s]) << 16);
+  }
+#pragma unroll
+  for (int s = 0; s < 3; ++s)
+    *reinterpret_cast<uint4*>(dst + s * stride) = make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
+}
 
 // ------------------------------------------------------------- mbarrier ----
 MOE_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {

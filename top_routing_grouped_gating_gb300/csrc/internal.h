@@ -25,10 +25,14 @@ RouterPlan router_plan_ex(int T, int H, int E, bool f32in);
 // Workspace of a router launch under router_plan_ex: partials + extra.
 size_t router_ws_bytes(int T, int H, int E, bool f32in);
 // Tensor-core router: x is (T,H) bf16, or fp32 when f32in.  Writes partial
-// sums part[plan.splits][T][E]; extra holds plan.extra_bytes of scratch.
-cudaError_t launch_router_tc(const void* x, bool f32in, const float* Wg, int T, int H, int E,
-                             const RouterPlan& plan, float* partial, void* extra, int* zero_word,
-                             int* status, cudaStream_t s);
+// sums part[plan.splits][T][E]; extra holds plan.extra_bytes of scratch.  With
+// f32in and presplit, x is unused: the launch before wrote the exact three-piece
+// bf16 split of the fp32 activations, (T, 3H) = [y1 | y2 | y3], at
+// router_split_rows(extra, plan, H, E).
+cudaError_t launch_router_tc(const void* x, bool f32in, bool presplit, const float* Wg, int T,
+                             int H, int E, const RouterPlan& plan, float* partial, void* extra,
+                             int* zero_word, int* status, cudaStream_t s);
+uint16_t* router_split_rows(void* extra, const RouterPlan& plan, int H, int E);
 // partial[s][T][E] when splits > 1, else writes out directly.  zero_word (may be
 // null) is set to 0 by the launch (the fused gating/routing counter).  With a
 // decode-size plan, the launch also asks L2 to prefetch [l2_hint, l2_hint +
@@ -122,9 +126,12 @@ cudaError_t launch_pack_down(const uint16_t* down, int E, int H, int I, uint16_t
                              cudaStream_t s);
 
 // ---- MXFP8 (mx.cu, gmm_mx.cu)
+// ys_out (may be null): the exact three-piece bf16 split of y, (T, 3H) = [y1 | y2 | y3],
+// the tensor-core router's activations.
 cudaError_t launch_add_rmsnorm_mxquant(const uint16_t* x, const uint16_t* r, const uint16_t* w,
                                        float eps, int T, int H, uint16_t* residual_out,
-                                       float* y32_out, uint8_t* q, uint8_t* scale, cudaStream_t s);
+                                       float* y32_out, uint16_t* ys_out, uint8_t* q,
+                                       uint8_t* scale, cudaStream_t s);
 cudaError_t launch_mx_quantize(const float* y, int rows, int n, uint8_t* q, uint8_t* scale,
                                cudaStream_t s);
 cudaError_t launch_pack_mx(const uint16_t* w13, const uint16_t* down, int E, int H, int I,

@@ -63,7 +63,7 @@ MOE_DEVINL int atom_offset(int row, int kb) { return (row & 31) * 16 + ((row >> 
 __global__ void __launch_bounds__(256) add_rmsnorm_mxquant_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ r, const uint16_t* __restrict__ w,
     float eps, int H, uint16_t* __restrict__ residual_out, float* __restrict__ y32_out,
-    uint8_t* __restrict__ q, uint8_t* __restrict__ scale) {
+    uint16_t* __restrict__ ys_out, uint8_t* __restrict__ q, uint8_t* __restrict__ scale) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ float srow[];  // H floats: s = x + r
@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(256) add_rmsnorm_mxquant_kernel(
       dst[0] = make_float4(y[0], y[1], y[2], y[3]);
       dst[1] = make_float4(y[4], y[5], y[6], y[7]);
     }
+    if (ys_out != nullptr) store_split3_x8(y, ys_out + 3 * base + c, H);
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(y[i]));
@@ -391,8 +392,8 @@ cudaError_t launch_mx_unpad(const uint8_t* pq, const uint8_t* psf, const uint16_
 
 cudaError_t launch_add_rmsnorm_mxquant(const uint16_t* x, const uint16_t* r, const uint16_t* w,
                                        float eps, int T, int H, uint16_t* residual_out,
-                                       float* y32_out, uint8_t* q, uint8_t* scale,
-                                       cudaStream_t s) {
+                                       float* y32_out, uint16_t* ys_out, uint8_t* q,
+                                       uint8_t* scale, cudaStream_t s) {
   const size_t smem = (size_t)H * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(add_rmsnorm_mxquant_kernel,
@@ -400,7 +401,7 @@ cudaError_t launch_add_rmsnorm_mxquant(const uint16_t* x, const uint16_t* r, con
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(add_rmsnorm_mxquant_kernel, dim3(T), dim3(256), smem, s, x, r, w, eps, H,
-                    residual_out, y32_out, q, scale);
+                    residual_out, y32_out, ys_out, q, scale);
 }
 
 cudaError_t launch_mx_quantize(const float* y, int rows, int n, uint8_t* q, uint8_t* scale,

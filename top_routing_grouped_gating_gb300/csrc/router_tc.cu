@@ -24,21 +24,6 @@ namespace {
 
 constexpr int kTcMinTokens = 65;    // below: CUDA-core decode router
 
-MOE_DEVINL uint16_t bf16_bits(float f) {
-  __nv_bfloat16 b = __float2bfloat16_rn(f);
-  return *reinterpret_cast<uint16_t*>(&b);
-}
-MOE_DEVINL float bf16_val(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
-
-// Exact three-piece bf16 split of v.
-MOE_DEVINL void split3(float v, uint16_t (&p)[3]) {
-  p[0] = bf16_bits(v);
-  const float r1 = v - bf16_val(p[0]);
-  p[1] = bf16_bits(r1);
-  const float r2 = r1 - bf16_val(p[1]);
-  p[2] = bf16_bits(r2);
-}
-
 // Wg (H, E) fp32 -> A (mrows, nseg * H) bf16: row e = the weight pieces of expert e
 // in segment order (bf16 activations: W1 W2 W3; fp32: W1 W2 W1 W3 W2 W1); rows
 // e >= E are zero.  Also writes the one-expert offsets {0, T} and clears zero_word.
@@ -62,7 +47,7 @@ __global__ void __launch_bounds__(256) router_pack_kernel(const float* __restric
     const int e = e0 + i, h = h0 + tx;
     if (h >= H) continue;
     uint16_t p[3];
-    split3(tile[tx][i], p);
+    split3_bf16(tile[tx][i], p);
     uint16_t* row = A + (size_t)e * kp + h;
     if (nseg == 3) {
       row[0] = p[0];
@@ -98,21 +83,7 @@ __global__ void __launch_bounds__(256) split_f32_kernel(const float* __restrict_
     const float4* src = reinterpret_cast<const float4*>(y + (size_t)t * H) + 2 * g;
     const float4 a = src[0], b = src[1];
     const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t w[3][4];
-#pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-      uint16_t p0[3], p1[3];
-      split3(v[i], p0);
-      split3(v[i + 1], p1);
-#pragma unroll
-      for (int s = 0; s < 3; ++s)
-        w[s][i / 2] = static_cast<uint32_t>(p0[s]) | (static_cast<uint32_t>(p1[s]) << 16);
-    }
-    uint16_t* row = ys + (size_t)t * 3 * H + 8 * g;
-#pragma unroll
-    for (int s = 0; s < 3; ++s)
-      *reinterpret_cast<uint4*>(row + (size_t)s * H) =
-          make_uint4(w[s][0], w[s][1], w[s][2], w[s][3]);
+    store_split3_x8(v, ys + (size_t)t * 3 * H + 8 * g, H);
   }
 }
 
@@ -148,20 +119,28 @@ size_t router_ws_bytes(int T, int H, int E, bool f32in) {
   return align256((size_t)p.splits * T * E * sizeof(float)) + p.extra_bytes;
 }
 
-cudaError_t launch_router_tc(const void* x, bool f32in, const float* Wg, int T, int H, int E,
-                             const RouterPlan& plan, float* partial, void* extra, int* zero_word,
-                             int* status, cudaStream_t s) {
+uint16_t* router_split_rows(void* extra, const RouterPlan& plan, int H, int E) {
+  const int mrows = ((E + 127) / 128) * 128;
+  return reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(extra) +
+                                     align256((size_t)mrows * plan.nseg * H * 2) + 256);
+}
+
+cudaError_t launch_router_tc(const void* x, bool f32in, bool presplit, const float* Wg, int T,
+                             int H, int E, const RouterPlan& plan, float* partial, void* extra,
+                             int* zero_word, int* status, cudaStream_t s) {
   const int mrows = ((E + 127) / 128) * 128;
   const int kp = plan.nseg * H;
   uint8_t* base = static_cast<uint8_t*>(extra);
   uint16_t* A = reinterpret_cast<uint16_t*>(base);
   int32_t* offs2 = reinterpret_cast<int32_t*>(base + align256((size_t)mrows * kp * 2));
-  uint16_t* ys = reinterpret_cast<uint16_t*>(base + align256((size_t)mrows * kp * 2) + 256);
+  uint16_t* ys = router_split_rows(extra, plan, H, E);
   cudaError_t err = launch_pdl(router_pack_kernel, dim3((H + 31) / 32, mrows / 32), dim3(32, 8), 0,
                                s, Wg, H, E, plan.nseg, T, A, offs2, zero_word);
   if (err != cudaSuccess) return err;
   const uint16_t* B = static_cast<const uint16_t*>(x);
-  if (f32in) {
+  if (f32in && presplit) {
+    B = ys;   // written by the producing kernel
+  } else if (f32in) {
     const dim3 grid((unsigned)((H / 8 + 255) / 256), (unsigned)(T < 65535 ? T : 65535));
     err = launch_pdl(split_f32_kernel, grid, dim3(256), 0, s, static_cast<const float*>(x), T, H,
                      ys);
