@@ -325,8 +325,8 @@ moe_status moe_init_routing(const moe_bf16* x, const int32_t* topk_ids, int T, i
   MOE_CUDA(moe::launch_routing(topk_ids, P, E, cnt, expert_offsets, expanded_row_idx,
                                sorted_row_idx, ws, nullptr, d->status, stream));
   if (expanded_x)
-    MOE_CUDA(moe::launch_gather_rows(x, sorted_row_idx, expert_offsets, E, P, H, k, expanded_x,
-                                     stream));
+    MOE_CUDA(moe::launch_expand_rows(x, expanded_row_idx, sorted_row_idx, expert_offsets, E, T, H,
+                                     k, expanded_x, stream));
   return MOE_OK;
 }
 
@@ -476,7 +476,7 @@ moe_status moe_forward(const moe_bf16* x, const float* Wg, const float* logits_o
   if (!fused_routing)
     MOE_CUDA(moe::launch_routing(ids, P, E, fr.counts, offsets, eri, sri,
                                  at<void>(ws, L.routing), done, d->status, stream));
-  MOE_CUDA(moe::launch_gather_rows(x, sri, offsets, E, P, H, k, xe, stream));
+  MOE_CUDA(moe::launch_expand_rows(x, eri, sri, offsets, E, T, H, k, xe, stream));
   moe::GemmPhase g1{}, g2{};
   g1.A_weights = w13_packed;
   g1.B_act = xe;
@@ -935,8 +935,8 @@ moe_status moe_init_routing_v2(const moe_bf16* x, const int32_t* topk_ids, int T
                                      expanded_row_idx, sorted_row_idx, ws, nullptr, d->status,
                                      stream));
   if (expanded_x)
-    MOE_CUDA(moe::launch_gather_rows(x, sorted_row_idx, expert_offsets, El, P, H, k, expanded_x,
-                                     stream));
+    MOE_CUDA(moe::launch_expand_rows(x, expanded_row_idx, sorted_row_idx, expert_offsets, El, T,
+                                     H, k, expanded_x, stream));
   return MOE_OK;
 }
 
@@ -1091,7 +1091,7 @@ moe_status moe_forward_v2(const moe_bf16* x, const moe_bf16* r, const moe_bf16* 
   uint16_t* xe = at<uint16_t>(ws, L.xe);
   uint16_t* h = at<uint16_t>(ws, L.h);
   uint16_t* y2 = at<uint16_t>(ws, L.y2);
-  MOE_CUDA(moe::launch_gather_rows(expert_in, sri, offsets, E, P, H, k, xe, stream));
+  MOE_CUDA(moe::launch_expand_rows(expert_in, eri, sri, offsets, E, T, H, k, xe, stream));
   moe::GemmPhase g1{}, g2{};
   g1.A_weights = w13_packed;
   g1.B_act = xe;

@@ -85,6 +85,13 @@ cudaError_t launch_routing(const int32_t* ids, int P, int E, int32_t* counts, in
 cudaError_t launch_routing_range(const int32_t* ids, int P, int e_begin, int E, int E_total,
                                  int32_t* counts, int32_t* offsets, int32_t* eri, int32_t* sri,
                                  void* ws, int* zero_counter, int* status, cudaStream_t s);
+// expanded_x = the token rows in expert order, from the routing's eri (k slots per
+// token, -1 for a pair routed elsewhere) and sri: at T >= kScatterMinTokens each
+// token row is read once and written to its slots, below by a gather per sorted row.
+constexpr int kScatterMinTokens = 256;
+cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* eri, const int32_t* sri,
+                               const int32_t* offsets, int E, int T, int H, int k, uint16_t* xe,
+                               cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sri, const int32_t* offsets,
                                int E, int P, int H, int k, uint16_t* expanded_x, cudaStream_t s);
 cudaError_t launch_expert_tokens(const int32_t* ids, int P, int E, int32_t* counts,

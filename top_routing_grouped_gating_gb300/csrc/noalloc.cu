@@ -87,8 +87,8 @@ extern "C" moe_status moe_init_routing_noalloc(const moe_bf16* x, const int32_t*
                           scratch, nullptr, dev_status, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (expanded_x &&
-      moe::launch_gather_rows(x, sorted_row_idx, expert_offsets, E, P, H, k, expanded_x,
-                              stream) != cudaSuccess)
+      moe::launch_expand_rows(x, expanded_row_idx, sorted_row_idx, expert_offsets, E, T, H, k,
+                              expanded_x, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

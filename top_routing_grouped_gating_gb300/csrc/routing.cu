@@ -121,6 +121,41 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   for (; v < nv; v += 32) dst[v] = src[v];
 }
 
+// expanded_x[eri[t * k + j]] = x[t] for every pair with eri >= 0: the same rows as
+// the gather above, but each token row is read once, in row order.  (Gathering by
+// sorted row reads each token row k times, far apart in time; at prefill sizes the
+// expanded rows streaming through L2 evict x in between.)  One warp per token and
+// 2 KB column chunk of its row: each lane loads four 16-byte pieces, then stores them
+// to each of the token's expanded rows.
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __restrict__ x,
+                                                           const int32_t* __restrict__ eri, int T,
+                                                           int k, int H,
+                                                           uint16_t* __restrict__ xe) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nv = H / 8;                       // 16-byte pieces per row
+  const int chunks = (nv + 127) / 128;
+  const long long t = w / chunks;
+  if (t >= T) return;
+  const int v0 = static_cast<int>(w - t * chunks) * 128 + lane;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  uint4 a[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (v0 + 32 * i < nv) a[i] = src[v0 + 32 * i];
+  const int my_p = lane < k ? eri[(size_t)t * k + lane] : -1;
+  for (int j = 0; j < k; ++j) {
+    const int p = __shfl_sync(0xffffffffu, my_p, j);
+    if (p < 0) continue;
+    uint4* dst = reinterpret_cast<uint4*>(xe + (size_t)p * H);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (v0 + 32 * i < nv) dst[v0 + 32 * i] = a[i];
+  }
+}
+
 __global__ void __launch_bounds__(kRouteThreads) expert_tokens_kernel(
     const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int* status) {
@@ -241,6 +276,15 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sri, const int3
   const int blocks = (P + 7) / 8;
   return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, x, sri, offsets, E, P, H, k,
                     xe);
+}
+
+cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* eri, const int32_t* sri,
+                               const int32_t* offsets, int E, int T, int H, int k, uint16_t* xe,
+                               cudaStream_t s) {
+  if (T < kScatterMinTokens) return launch_gather_rows(x, sri, offsets, E, T * k, H, k, xe, s);
+  const long long warps = (long long)T * ((H / 8 + 127) / 128);
+  const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+  return launch_pdl(scatter_rows_kernel, dim3(blocks), dim3(256), 0, s, x, eri, T, k, H, xe);
 }
 
 cudaError_t launch_expert_tokens(const int32_t* ids, int P, int E, int32_t* counts,
