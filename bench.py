@@ -300,13 +300,14 @@ def tensor_roofline(flops: float, kernel_ms: float, step_ms: float, peak_tflops:
 def launches_per_step(cfg, router: bool = True) -> int:
     """Kernels one forward call launches: the fused norm kernel (MXFP8 and pre-norm
     layers), the router (one CUDA-core kernel for T <= 64; else weight split/pack,
-    an activation split for fp32 inputs, and the tensor-core GEMM), gating (routing
+    an activation split for the pre-norm layer's fp32 activations (the MXFP8 norm
+    kernel writes that split itself), and the tensor-core GEMM), gating (routing
     fused into it when P <= 4096, else histogram + scan + scatter), row expansion,
     grouped GEMM, finalize."""
     P = cfg.T * cfg.k
     routing = 0 if P <= 4096 else 3
-    f32_router = cfg.mx or cfg.prenorm
-    router_k = (1 if cfg.T <= 64 else (3 if f32_router else 2)) if router else 0
+    split_kernel = cfg.prenorm and not cfg.mx
+    router_k = (1 if cfg.T <= 64 else (3 if split_kernel else 2)) if router else 0
     norm = 1 if (cfg.mx or cfg.prenorm) else 0
     return norm + router_k + 1 + routing + 1 + 1 + 1
 

@@ -112,8 +112,9 @@ def test_gemm_flops():
     ("qwen3_30b_a3b_decode", True, 5),          # router, gating+routing, gather, GEMM, finalize
     ("qwen3_30b_a3b_decode", False, 4),         # logits given: no router launch
     ("qwen3_30b_a3b_prefill_zipf", True, 9),    # split/pack + TC GEMM router, 3 routing kernels
-    ("mxfp8_prefill", True, 11),                # norm/quant, 3 router, gating, 3 routing,
-                                                # expand, GEMM, finalize
+    ("mxfp8_prefill", True, 10),                # norm/quant (+ the router's split), pack +
+                                                # TC GEMM router, gating, 3 routing, expand,
+                                                # GEMM, finalize
     ("qwen3_30b_a3b_decode_prenorm", True, 6),  # + fused add+RMSNorm+cast
 ])
 def test_launches_per_step(name, router, expect):
