@@ -196,7 +196,8 @@ __global__ void __launch_bounds__(kRouteThreads) expert_tokens_kernel(
   if (tid == 0 && offsets != nullptr) offsets[E] = total;
 }
 
-// out[t] = sum_s w[t,s] * y2[eri[t*k+s]] in fp32, slot order; one CTA per token.
+// out[t] = sum_s w[t,s] * y2[eri[t*k+s]] in fp32, slot order; one CTA per token and
+// chunk of blockDim.x * 8 columns (gridDim.y chunks).
 __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restrict__ y2,
                                                        const float* __restrict__ w,
                                                        const int32_t* __restrict__ eri, int k,
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
     s_w[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
   }
   __syncthreads();
-  for (int v = threadIdx.x; v < H / 8; v += blockDim.x) {
+  for (int v = blockIdx.y * blockDim.x + threadIdx.x; v < H / 8; v += gridDim.y * blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -309,8 +310,19 @@ cudaError_t launch_expert_tokens(const int32_t* ids, int P, int E, int32_t* coun
 
 cudaError_t launch_finalize(const uint16_t* y2, const float* w, const int32_t* eri, int T, int k,
                             int H, uint16_t* out, cudaStream_t s) {
-  const int threads = (H / 8) >= 256 ? 256 : ((H / 8 + 31) / 32) * 32;
-  return launch_pdl(finalize_kernel, dim3(T), dim3(threads), 0, s, y2, w, eri, k, H, out);
+  // one CTA per token; with few tokens, each token's columns are spread over several
+  // CTAs (about two per SM in all), so more SMs have the slot rows' loads in flight
+  const int groups = H / 8;
+  int threads = groups >= 256 ? 256 : ((groups + 31) / 32) * 32;
+  int ysplit = 1;
+  const int want = 2 * device_sm_count();
+  if (T < want) {
+    const int max_split = (groups + 31) / 32;
+    ysplit = (want + T - 1) / T < max_split ? (want + T - 1) / T : max_split;
+    threads = ((groups + ysplit - 1) / ysplit + 31) / 32 * 32;
+    ysplit = (groups + threads - 1) / threads;
+  }
+  return launch_pdl(finalize_kernel, dim3(T, ysplit), dim3(threads), 0, s, y2, w, eri, k, H, out);
 }
 
 }  // namespace moe
