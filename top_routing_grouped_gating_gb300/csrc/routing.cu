@@ -317,7 +317,7 @@ cudaError_t launch_finalize(const uint16_t* y2, const float* w, const int32_t* e
   int ysplit = 1;
   const int want = 2 * device_sm_count();
   if (T < want) {
-    const int max_split = (groups + 31) / 32;
+    const int max_split = (groups + 127) / 128;   // at least 128 threads per CTA
     ysplit = (want + T - 1) / T < max_split ? (want + T - 1) / T : max_split;
     threads = ((groups + ysplit - 1) / ysplit + 31) / 32 * 32;
     ysplit = (groups + threads - 1) / threads;
